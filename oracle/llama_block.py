@@ -1,0 +1,312 @@
+"""fp64 oracle of the Llama pre-norm decoder block (test infrastructure only).
+
+Pages restated (cited by title and section):
+  [EVT]  "The Evolving Transformer 04 · LLaMA" -- §00 Config, §01 Embeddings,
+         §02 RoPE, §03 RMSNorm, §04 SwiGLU, §05 GQA, §06 Block, §07 Assemble.
+  [L3B]  "Full Llama 3 transformer block" -- Overview, How it works, Watch-outs.
+  [L4S]  "Llama 4 From Scratch" -- The idea, Worked example, In code.
+  [ML2]  "Mini Llama 2 Implementation" -- RMS normalization, Rotary positional
+         embeddings, Self-attention and transformer blocks.
+  [G2L]  "From GPT-2 to Llama: four changes and the reason for each" --
+         Positions become a rotation, The norm stops centring, The feed-forward
+         grows a gate, Keys and values get shared, What the ML engineer watches.
+
+Readings taken where the pages are open or disagree (each also listed in the
+design notes):
+  * RoPE pairs are interleaved (2i, 2i+1) ([EVT] §02, [ML2] Rotary), not the
+    halves layout of [G2L]; frequency of pair i is theta^(-2i/D) ([ML2]
+    Rotary, [L4S] Worked example); the position of query/key s is
+    start_pos + s ([L3B] How it works: freqs_cis slice from start_pos).
+  * RMSNorm adds eps to mean(x^2) inside the root ([EVT] §03, [L4S] In code,
+    [ML2] RMS normalization, [G2L] The norm stops centring); no rounding.
+  * Query head h reads KV head h // (H / G) ([EVT] §05 repeat_kv expands each
+    KV head n_rep times in place); the cache stores K after RoPE and V as
+    projected ([L3B] How it works: RoPE rotates Q and K, then keys/values are
+    written into the cache).
+  * Causal mask with cache offset: key j is visible to query i iff
+    j <= start_pos + i ([L3B] How it works: mask shaped for the query length
+    against the cached key length; [EVT] §05 tril mask is the start_pos = 0 case).
+  * SwiGLU names follow [L3B]: W1 = gate, W3 = up, W2 = down; [EVT] §04 labels
+    w2 up / w3 down -- the arithmetic is the same.
+
+Parity pins (tests/test_oracle_pins.py) cover every function below; the whole
+block has no printed worked example on the pages, so the block composition is
+pinned through the special cases and invariants listed there (single-token
+closed form, residual identity, pre-norm scale invariance, GQA == duplicated
+MHA, causality, chunked prefill == one-shot == token-by-token decode).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "rms_norm", "rope_frequencies", "rope", "silu", "linear", "gqa_attention",
+    "gqa_attention_rows", "block_forward", "block_forward_rows", "stack_forward",
+    "ffn_hidden_dim", "kv_values_per_token", "block_param_count", "model_param_count",
+]
+
+
+def rms_norm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
+    """u = x / sqrt(mean(x^2) + eps) * g over the last (model) axis.
+
+    [EVT] §03 RMSNorm; [L3B] How it works (eps = norm_eps); [G2L] The norm stops
+    centring (no mean subtraction, no shift).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * np.asarray(g, dtype=np.float64)
+
+
+def rope_frequencies(d_head: int, theta: float) -> np.ndarray:
+    """Angular frequency of pair i: theta^(-2i / d_head), i = 0 .. d_head/2 - 1.
+
+    [ML2] Rotary positional embeddings (theta ** (-2 * arange(D/2) / D));
+    [L4S] Worked example; [EVT] §02 (base^(arange(0, D, 2) / D) inverted).
+    """
+    i = np.arange(d_head // 2, dtype=np.float64)
+    return np.power(float(theta), -2.0 * i / d_head)
+
+
+def rope(x: np.ndarray, positions: np.ndarray, theta: float) -> np.ndarray:
+    """Rotate interleaved pairs (x[2i], x[2i+1]) of x[..., S, heads, D] by p_s * f_i.
+
+    (a, b) -> (a cos - b sin, a sin + b cos) with p_s = positions[s].
+    [EVT] §02 RoPE (even/odd split, rotate, stack); [ML2] Rotary positional
+    embeddings (reshape(-1, 2) real/imag form); [L3B] How it works (positions
+    start_pos .. start_pos + S - 1).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * rope_frequencies(D, theta)[None, :]
+    cos = np.cos(ang)[:, None, :]  # [S, 1, D/2] broadcast over heads
+    sin = np.sin(ang)[:, None, :]
+    a = x[..., 0::2]
+    b = x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = a * cos - b * sin
+    out[..., 1::2] = a * sin + b * cos
+    return out
+
+
+def silu(z: np.ndarray) -> np.ndarray:
+    """SiLU(z) = z * sigmoid(z) = z / (1 + e^-z).  [EVT] §04; [L4S] In code (Swish)."""
+    z = np.asarray(z, dtype=np.float64)
+    return z / (1.0 + np.exp(-z))
+
+
+def linear(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """nn.Linear without bias: y = x W^T with W stored [out, in].  [EVT] §05, §04."""
+    return np.asarray(x, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T
+
+
+def _softmax_rows(s: np.ndarray) -> np.ndarray:
+    s = s - np.max(s, axis=-1, keepdims=True)
+    p = np.exp(s)
+    return p / np.sum(p, axis=-1, keepdims=True)
+
+
+def gqa_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, start_pos: int) -> np.ndarray:
+    """Causal grouped-query attention over the cache.
+
+    q: [B, S, H, D] (already rotated); k_cache, v_cache: [B, G, L_max, D] holding
+    keys/values of positions 0 .. start_pos + S - 1.  Query head h of token i
+    attends to KV head h // (H / G) at key positions j <= start_pos + i with
+    weights softmax_j(q . k_j / sqrt(D)); returns o [B, S, H, D].
+    [EVT] §05 GQA (scores / sqrt(dk), -inf mask, softmax, @ value, repeat_kv);
+    [L3B] How it works (cache read, offset mask).
+    """
+    B, S, H, D = q.shape
+    G = k_cache.shape[1]
+    r = H // G
+    L = start_pos + S
+    i = np.arange(S)[:, None]
+    j = np.arange(L)[None, :]
+    visible = j <= start_pos + i  # [S, L]
+    o = np.empty((B, S, H, D), dtype=np.float64)
+    scale = 1.0 / math.sqrt(D)
+    for b in range(B):
+        for h in range(H):
+            g = h // r
+            K = np.asarray(k_cache[b, g, :L], dtype=np.float64)
+            V = np.asarray(v_cache[b, g, :L], dtype=np.float64)
+            s = (np.asarray(q[b, :, h, :], dtype=np.float64) @ K.T) * scale
+            s = np.where(visible, s, -np.inf)
+            o[b, :, h, :] = _softmax_rows(s) @ V
+    return o
+
+
+def gqa_attention_rows(q_rows: np.ndarray, batch_idx, query_pos, k_cache, v_cache) -> np.ndarray:
+    """Same attention for a list of single queries.
+
+    q_rows: [n, H, D]; row n belongs to sequence batch_idx[n] and sits at absolute
+    position query_pos[n], so it sees keys 0 .. query_pos[n].  Returns [n, H, D].
+    """
+    n, H, D = q_rows.shape
+    G = k_cache.shape[1]
+    r = H // G
+    out = np.empty((n, H, D), dtype=np.float64)
+    scale = 1.0 / math.sqrt(D)
+    for t in range(n):
+        b = int(batch_idx[t])
+        L = int(query_pos[t]) + 1
+        for h in range(H):
+            g = h // r
+            K = np.asarray(k_cache[b, g, :L], dtype=np.float64)
+            V = np.asarray(v_cache[b, g, :L], dtype=np.float64)
+            s = (K @ np.asarray(q_rows[t, h], dtype=np.float64)) * scale
+            s = s - np.max(s)
+            p = np.exp(s)
+            out[t, h] = (p / np.sum(p)) @ V
+    return out
+
+
+def _dims(cfg):
+    d = int(cfg["d_model"])
+    H = int(cfg["n_heads"])
+    G = int(cfg["n_kv_heads"])
+    return d, H, G, d // H
+
+
+def _project_qkv(cfg, w, x, start_pos):
+    """attention_norm, Wq/Wk/Wv and RoPE on Q, K for all tokens of x [B, S, d]."""
+    d, H, G, D = _dims(cfg)
+    B, S, _ = x.shape
+    u = rms_norm(x, w["attn_norm"], cfg["norm_eps"])
+    q = linear(u, w["wq"]).reshape(B, S, H, D)
+    k = linear(u, w["wk"]).reshape(B, S, G, D)
+    v = linear(u, w["wv"]).reshape(B, S, G, D)
+    pos = start_pos + np.arange(S)
+    q = rope(q, pos, cfg["rope_theta"])
+    k = rope(k, pos, cfg["rope_theta"])
+    return q, k, v
+
+
+def _write_cache(k_cache, v_cache, k, v, start_pos):
+    """Store rotated K and V of positions start_pos .. start_pos + S - 1 ([L3B] How it works)."""
+    S = k.shape[1]
+    kc = np.array(k_cache, dtype=np.float64, copy=True)
+    vc = np.array(v_cache, dtype=np.float64, copy=True)
+    kc[:, :, start_pos:start_pos + S, :] = k.transpose(0, 2, 1, 3)
+    vc[:, :, start_pos:start_pos + S, :] = v.transpose(0, 2, 1, 3)
+    return kc, vc
+
+
+def _ffn(cfg, w, h):
+    """ffn_norm then SwiGLU: W2(SiLU(W1 v) * W3 v).  [L3B] How it works; [EVT] §04."""
+    v2 = rms_norm(h, w["ffn_norm"], cfg["norm_eps"])
+    a = silu(linear(v2, w["w_gate"])) * linear(v2, w["w_up"])
+    return linear(a, w["w_down"])
+
+
+def block_forward(cfg: dict, w: dict, x: np.ndarray, start_pos: int, k_cache: np.ndarray,
+                  v_cache: np.ndarray):
+    """One pre-norm block: h = x + Attn(RMSNorm(x)); y = h + FFN(RMSNorm(h)).
+
+    x: [B, S, d]; caches [B_max, G, L_max, D] (B_max >= B; rows >= B untouched).
+    Returns (y, k_cache', v_cache') -- the caches are new fp64 arrays with
+    positions start_pos .. start_pos + S - 1 of sequences 0 .. B - 1 written.
+    [L3B] Overview / How it works (the two residual branches, untied norms);
+    [EVT] §06 Block; [ML2] Self-attention and transformer blocks.
+    """
+    d, H, G, D = _dims(cfg)
+    x = np.asarray(x, dtype=np.float64)
+    B, S, _ = x.shape
+    q, k, v = _project_qkv(cfg, w, x, start_pos)
+    kc, vc = _write_cache(np.asarray(k_cache, dtype=np.float64)[:B], np.asarray(v_cache, dtype=np.float64)[:B],
+                          k, v, start_pos)
+    o = gqa_attention(q, kc, vc, start_pos).reshape(B, S, H * D)
+    h = x + linear(o, w["wo"])
+    y = h + _ffn(cfg, w, h)
+    kfull = np.array(k_cache, dtype=np.float64, copy=True)
+    vfull = np.array(v_cache, dtype=np.float64, copy=True)
+    kfull[:B] = kc
+    vfull[:B] = vc
+    return y, kfull, vfull
+
+
+def block_forward_rows(cfg: dict, w: dict, x: np.ndarray, start_pos: int, k_cache, v_cache, rows):
+    """The block output y at selected (b, s) rows only, plus the written K/V slice.
+
+    Every key/value of positions < start_pos + S is still computed (all queries
+    may see them); queries, the O projection and the FFN run only for the
+    selected rows.  Same definition as :func:`block_forward`, restricted.
+    Returns (y_rows [n, d], k_new [B, G, S, D], v_new [B, G, S, D]).
+    """
+    d, H, G, D = _dims(cfg)
+    x = np.asarray(x, dtype=np.float64)
+    B, S, _ = x.shape
+    u = rms_norm(x, w["attn_norm"], cfg["norm_eps"])
+    pos = start_pos + np.arange(S)
+    k = rope(linear(u, w["wk"]).reshape(B, S, G, D), pos, cfg["rope_theta"])
+    v = linear(u, w["wv"]).reshape(B, S, G, D)
+    kc, vc = _write_cache(np.asarray(k_cache[:B], dtype=np.float64), np.asarray(v_cache[:B], dtype=np.float64),
+                          k, v, start_pos)
+    rows = np.asarray(rows, dtype=np.int64).reshape(-1, 2)
+    bi, si = rows[:, 0], rows[:, 1]
+    ur = u[bi, si]  # [n, d]
+    qr = linear(ur, w["wq"]).reshape(-1, 1, H, D)
+    qr = np.stack([rope(qr[t:t + 1], np.array([start_pos + si[t]]), cfg["rope_theta"])[0, 0]
+                   for t in range(len(si))]) if len(si) else qr.reshape(0, H, D)
+    o = gqa_attention_rows(qr, bi, start_pos + si, kc, vc).reshape(-1, H * D)
+    h = x[bi, si] + linear(o, w["wo"])
+    y = h + _ffn(cfg, w, h)
+    k_new = kc[:, :, start_pos:start_pos + S, :]
+    v_new = vc[:, :, start_pos:start_pos + S, :]
+    return y, k_new, v_new
+
+
+def stack_forward(cfg: dict, layers, embed, final_norm, lm_head, tokens, start_pos: int, caches):
+    """Token embedding -> N blocks -> final RMSNorm -> untied LM head (logits).
+
+    tokens: int [B, S]; layers: list of weight dicts; caches: list of (k, v).
+    [EVT] §01 Embeddings (wte only, no position table), §07 Assemble (blocks,
+    final norm, lm_head); untied per [EVT] §00 (~8.0B with untied embeddings).
+    Returns (logits [B, S, vocab], new caches).
+    """
+    x = np.asarray(embed, dtype=np.float64)[np.asarray(tokens)]
+    new_caches = []
+    for w, (kc, vc) in zip(layers, caches):
+        x, kc2, vc2 = block_forward(cfg, w, x, start_pos, kc, vc)
+        new_caches.append((kc2, vc2))
+    n = rms_norm(x, final_norm, cfg["norm_eps"])
+    return linear(n, lm_head), new_caches
+
+
+# ---------------------------------------------------------------------------
+# Shape arithmetic the pages fix.
+# ---------------------------------------------------------------------------
+
+def ffn_hidden_dim(d_model: int, multiple_of: int, ffn_dim_multiplier=None) -> int:
+    """SwiGLU inner width: 4d, then 2/3 (floor), then x multiplier (floor), then
+    round up to a multiple of multiple_of.  [L3B] How it works (FeedForward
+    constructor: hidden_dim = 4 * dim, 2/3 shrink, optional ffn_dim_multiplier,
+    multiple_of rounding); [G2L] The feed-forward grows a gate (f = 8d/3)."""
+    h = 4 * d_model
+    h = int(2 * h / 3)
+    if ffn_dim_multiplier is not None:
+        h = int(ffn_dim_multiplier * h)
+    return multiple_of * ((h + multiple_of - 1) // multiple_of)
+
+
+def kv_values_per_token(n_layers: int, n_kv_heads: int, d_head: int) -> int:
+    """Cached numbers per token: 2 (K and V) x layers x KV heads x head width.
+    [L4S] Worked example; [G2L] What the ML engineer watches."""
+    return 2 * n_layers * n_kv_heads * d_head
+
+
+def block_param_count(d_model: int, n_heads: int, n_kv_heads: int, d_ff: int, norms: bool = True) -> dict:
+    """Parameter counts of one block (no biases): attention, FFN, norms, total."""
+    D = d_model // n_heads
+    attn = d_model * n_heads * D + 2 * d_model * n_kv_heads * D + n_heads * D * d_model
+    ffn = 3 * d_model * d_ff
+    nrm = 2 * d_model if norms else 0
+    return {"attention": attn, "ffn": ffn, "norms": nrm, "total": attn + ffn + nrm}
+
+
+def model_param_count(d_model, n_heads, n_kv_heads, d_ff, n_layers, vocab, tied: bool) -> int:
+    """Embedding + N blocks + final norm (+ LM head when untied).  [EVT] §07; §00."""
+    blk = block_param_count(d_model, n_heads, n_kv_heads, d_ff)["total"]
+    emb = vocab * d_model
+    return n_layers * blk + emb + d_model + (0 if tied else emb)
