@@ -1,0 +1,218 @@
+"""Python binding of libllama_block.so (the GB300 Llama decoder-block library).
+
+Argument marshalling only: every function here forwards to the C entry point of
+the same name (include/llama_block.h, include/llama_ops.h) and returns its
+status code; create functions return (status, handle).  Device memory and
+streams come from the caller (PyTorch tensors' data_ptr() and
+torch.cuda.Stream.cuda_stream work).  There is no fallback: if the compiled
+library is missing, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, byref, c_char_p, c_float, c_int32, c_size_t, c_void_p
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libllama_block.so")
+
+LLAMA_OK = 0
+LLAMA_ERR_INVALID_ARG = 1
+LLAMA_ERR_SHAPE = 2
+LLAMA_ERR_ALIGN = 3
+LLAMA_ERR_RANGE = 4
+LLAMA_ERR_UNSUPPORTED = 5
+LLAMA_ERR_OOM = 6
+LLAMA_ERR_CUDA = 7
+LLAMA_ERR_DEVICE_TIMEOUT = 8
+
+LLAMA_F32 = 0
+LLAMA_BF16 = 1
+
+EPI_STORE = 0
+EPI_RESIDUAL = 1
+EPI_F32OUT = 2
+
+
+class LlamaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {llama_status_string(status)} ({status})")
+
+
+class llama_config(ctypes.Structure):
+    _fields_ = [("d_model", c_int32), ("n_heads", c_int32), ("n_kv_heads", c_int32), ("d_ff", c_int32),
+                ("max_seq_len", c_int32), ("norm_eps", c_float), ("rope_theta", c_float), ("dtype", c_int32)]
+
+
+WEIGHT_FIELDS = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")
+
+
+class llama_block_weights(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in WEIGHT_FIELDS]
+
+
+class llama_kv_cache(ctypes.Structure):
+    _fields_ = [("k", c_void_p), ("v", c_void_p), ("max_batch", c_int32), ("max_seq_len", c_int32)]
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load the library (once).  Raises OSError when it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise OSError(f"{LIB_PATH} is missing: build it with decoder_block_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    st = c_int32
+    sigs = {
+        "llama_block_create": (st, [POINTER(llama_config), POINTER(llama_block_weights), c_int32, POINTER(c_void_p)]),
+        "llama_block_forward": (st, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
+                                     POINTER(llama_kv_cache), c_void_p]),
+        "llama_block_forward_host": (st, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
+                                          POINTER(llama_kv_cache), c_void_p]),
+        "llama_block_destroy": (None, [c_void_p]),
+        "llama_block_device_status": (st, [c_void_p]),
+        "llama_stack_create": (st, [POINTER(llama_config), c_int32, c_int32, c_void_p, POINTER(llama_block_weights),
+                                    c_void_p, c_void_p, c_int32, POINTER(c_void_p)]),
+        "llama_stack_forward": (st, [c_void_p, c_void_p, c_int32, c_int32, c_int32, POINTER(llama_kv_cache),
+                                     c_void_p, c_void_p]),
+        "llama_stack_destroy": (None, [c_void_p]),
+        "llama_stack_device_status": (st, [c_void_p]),
+        "llama_kv_cache_bytes": (c_size_t, [POINTER(llama_config), c_int32, c_int32]),
+        "llama_ffn_hidden_dim": (c_int32, [c_int32, c_int32, c_float]),
+        "llama_status_string": (c_char_p, [c_int32]),
+        "llama_op_rmsnorm": (st, [c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_void_p]),
+        "llama_op_linear": (st, [c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
+                                 c_void_p]),
+        "llama_op_attention": (st, [c_int32, c_void_p, POINTER(llama_kv_cache), c_void_p, c_int32, c_int32, c_int32,
+                                    c_int32, c_int32, c_int32, c_void_p]),
+        "llama_op_rope_table": (st, [c_void_p, c_int32, c_int32, c_float, c_void_p]),
+        "llama_op_rope_kv_write": (st, [c_int32, c_void_p, c_void_p, POINTER(llama_kv_cache), c_void_p, c_int32,
+                                        c_int32, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _p(x):
+    """A raw pointer from an int, None, or anything with data_ptr()."""
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream
+    return int(s)
+
+
+# ---------------------------------------------------------------- structs ---
+
+def make_config(d_model, n_heads, n_kv_heads, d_ff, max_seq_len, norm_eps, rope_theta, dtype) -> llama_config:
+    return llama_config(d_model, n_heads, n_kv_heads, d_ff, max_seq_len, norm_eps, rope_theta, dtype)
+
+
+def make_weights(w: dict) -> llama_block_weights:
+    return llama_block_weights(*[_p(w[n]) for n in WEIGHT_FIELDS])
+
+
+def make_kv_cache(k, v, max_batch, max_seq_len) -> llama_kv_cache:
+    return llama_kv_cache(_p(k), _p(v), max_batch, max_seq_len)
+
+
+# ------------------------------------------------------------ entry points ---
+
+def llama_block_create(cfg: llama_config, weights: llama_block_weights, max_tokens: int):
+    h = c_void_p()
+    s = load().llama_block_create(byref(cfg), byref(weights), max_tokens, byref(h))
+    return s, h.value
+
+
+def llama_block_forward(blk, x, y, B, S, start_pos, kv: llama_kv_cache, stream=None) -> int:
+    return load().llama_block_forward(blk, _p(x), _p(y), B, S, start_pos, byref(kv), _stream(stream))
+
+
+def llama_block_forward_host(blk, x_host, y_host, B, S, start_pos, kv: llama_kv_cache, stream=None) -> int:
+    return load().llama_block_forward_host(blk, _p(x_host), _p(y_host), B, S, start_pos, byref(kv), _stream(stream))
+
+
+def llama_block_destroy(blk) -> None:
+    load().llama_block_destroy(blk)
+
+
+def llama_block_device_status(blk) -> int:
+    return load().llama_block_device_status(blk)
+
+
+def llama_stack_create(cfg: llama_config, n_layers, vocab, embed, layers, final_norm, lm_head, max_tokens):
+    arr = (llama_block_weights * max(n_layers, 1))(*layers)
+    h = c_void_p()
+    s = load().llama_stack_create(byref(cfg), n_layers, vocab, _p(embed), arr, _p(final_norm), _p(lm_head),
+                                  max_tokens, byref(h))
+    return s, h.value
+
+
+def llama_stack_forward(stk, tokens, B, S, start_pos, kv_list, logits, stream=None) -> int:
+    arr = (llama_kv_cache * max(len(kv_list), 1))(*kv_list)
+    return load().llama_stack_forward(stk, _p(tokens), B, S, start_pos, arr, _p(logits), _stream(stream))
+
+
+def llama_stack_destroy(stk) -> None:
+    load().llama_stack_destroy(stk)
+
+
+def llama_stack_device_status(stk) -> int:
+    return load().llama_stack_device_status(stk)
+
+
+def llama_kv_cache_bytes(cfg: llama_config, max_batch, max_seq_len) -> int:
+    return load().llama_kv_cache_bytes(byref(cfg), max_batch, max_seq_len)
+
+
+def llama_ffn_hidden_dim(d_model, multiple_of, ffn_dim_multiplier) -> int:
+    return load().llama_ffn_hidden_dim(d_model, multiple_of, ffn_dim_multiplier)
+
+
+def llama_status_string(status) -> str:
+    return load().llama_status_string(status).decode()
+
+
+def llama_op_rmsnorm(dtype, x, g, out, T, d, eps, stream=None) -> int:
+    return load().llama_op_rmsnorm(dtype, _p(x), _p(g), _p(out), T, d, eps, _stream(stream))
+
+
+def llama_op_linear(dtype, A, W, R, C, M, N, K, epilogue, stream=None) -> int:
+    return load().llama_op_linear(dtype, _p(A), _p(W), _p(R), _p(C), M, N, K, epilogue, _stream(stream))
+
+
+def llama_op_attention(dtype, q, kv: llama_kv_cache, o, B, S, start_pos, H, G, D, stream=None) -> int:
+    return load().llama_op_attention(dtype, _p(q), byref(kv), _p(o), B, S, start_pos, H, G, D, _stream(stream))
+
+
+def llama_op_rope_table(table, max_seq, D, theta, stream=None) -> int:
+    return load().llama_op_rope_table(_p(table), max_seq, D, theta, _stream(stream))
+
+
+def llama_op_rope_kv_write(dtype, qkv, q_out, kv: llama_kv_cache, table, table_max_seq, B, S, start_pos, H, G, D,
+                           stream=None) -> int:
+    return load().llama_op_rope_kv_write(dtype, _p(qkv), _p(q_out), byref(kv), _p(table), table_max_seq, B, S,
+                                         start_pos, H, G, D, _stream(stream))
+
+
+def check(status: int, what: str = "llama call") -> None:
+    """Raise LlamaError for a non-OK status."""
+    if status != LLAMA_OK:
+        raise LlamaError(status, what)

@@ -1,0 +1,77 @@
+// Shared device helpers for the decoder-block kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace llama {
+
+typedef __nv_bfloat16 bf16;
+
+// Each block / stack handle owns one device status word (an int in device
+// memory).  A kernel whose bounded wait runs out, or that meets an invalid
+// token id, records the first such event there instead of trapping; the host
+// reads and clears it with llama_block_device_status().
+enum DeviceStatusCode : int {
+  DEV_OK = 0,
+  DEV_TIMEOUT_PRODUCER = 1,
+  DEV_TIMEOUT_MMA = 2,
+  DEV_TIMEOUT_EPILOGUE = 3,
+  DEV_TIMEOUT_ATTN = 4,
+  DEV_BAD_TOKEN = 16,
+};
+
+__device__ __forceinline__ void report_status(int *status, int code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<bf16>(bf16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+// 16-byte vector of T: 4 floats or 8 bf16.
+template <typename T> struct Vec16 {
+  static constexpr int N = 16 / sizeof(T);
+  uint4 raw;
+  __device__ __forceinline__ float get(int i) const {
+    const T *p = reinterpret_cast<const T *>(&raw);
+    return to_f32<T>(p[i]);
+  }
+  __device__ __forceinline__ void set(int i, float v) {
+    T *p = reinterpret_cast<T *>(&raw);
+    p[i] = from_f32<T>(v);
+  }
+};
+
+template <typename T> __device__ __forceinline__ Vec16<T> load16(const T *p) {
+  Vec16<T> v;
+  v.raw = *reinterpret_cast<const uint4 *>(p);
+  return v;
+}
+template <typename T> __device__ __forceinline__ void store16(T *p, const Vec16<T> &v) {
+  *reinterpret_cast<uint4 *>(p) = v.raw;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + __expf(-z)); }
+
+// Budget for a bounded spin on an mbarrier or flag, in SM clock cycles
+// (about 2 s at 2 GHz); long enough that no legitimate wait reaches it.
+constexpr long long kWaitBudgetCycles = 4000000000LL;
+
+}  // namespace llama

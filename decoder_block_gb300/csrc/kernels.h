@@ -1,0 +1,47 @@
+// Internal launch wrappers shared by the runtime (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace llama {
+
+enum Epilogue : int {
+  EPI_STORE = 0,     // C = A W^T                 (C in the input dtype)
+  EPI_RESIDUAL = 1,  // C = R + A W^T             (R, C in the input dtype)
+  EPI_F32OUT = 2,    // C = A W^T, C fp32
+  EPI_SWIGLU = 3,    // C = SiLU(A W1^T) * (A W3^T)
+};
+
+// RMSNorm of `rows` rows of width d (d % (16 / sizeof(T)) == 0).
+template <typename T>
+cudaError_t launch_rmsnorm(const T *x, const T *g, T *out, int rows, int d, float eps, cudaStream_t st);
+
+// Portable tiled GEMM with fp32 accumulation: C[M,N] = epi(A[M,K] W[N,K]^T).
+// W3 is only read by EPI_SWIGLU.
+template <typename T>
+cudaError_t launch_gemm_simt(const T *A, const T *W, const T *W3, const T *R, void *C, int M, int N, int K,
+                             int epi, cudaStream_t st);
+
+// cos/sin table [max_seq][D/2] (float2 = {cos, sin}) of p * theta^(-2i/D), computed in fp64.
+cudaError_t launch_rope_table(float2 *table, int max_seq, int D, double theta, cudaStream_t st);
+
+// RoPE on q and k of qkv [T][(H + 2G) D] and the KV-cache write.
+//   q_out [T][H D] (rotated q); kc/vc [cache_batch][G][cache_seq][D].
+template <typename T>
+cudaError_t launch_rope_kv(const T *qkv, T *q_out, T *kc, T *vc, const float2 *table, int B, int S,
+                           int start_pos, int H, int G, int D, int cache_seq, cudaStream_t st);
+
+// Reference causal GQA attention: one warp per (token, query head), online softmax in fp32.
+template <typename T>
+cudaError_t launch_attention_simt(const T *q, const T *kc, const T *vc, T *o, int B, int S, int start_pos,
+                                  int H, int G, int D, int cache_seq, cudaStream_t st);
+
+// x[t] = E[tokens[t]]; an out-of-range id writes zeros and sets the status word.
+template <typename T>
+cudaError_t launch_embed(const int32_t *tokens, const T *E, T *x, int ntok, int d, int vocab, int *status,
+                         cudaStream_t st);
+
+}  // namespace llama

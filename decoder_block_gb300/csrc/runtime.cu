@@ -1,0 +1,504 @@
+// Host runtime behind the C ABI: argument validation, weight repacking,
+// workspace ownership and the per-forward kernel sequence.
+//
+// Forward sequence of one block ("Full Llama 3 transformer block", How it
+// works; "The Evolving Transformer 04 · LLaMA", §06 Block):
+//   1. u   = RMSNorm(x; attention_norm)
+//   2. qkv = u [Wq; Wk; Wv]^T                 (one fused projection)
+//   3. q   = RoPE(q); K cache <- RoPE(k); V cache <- v   at start_pos + s
+//   4. o   = causal GQA attention over the cache
+//   5. h   = x + o Wo^T                       (residual in the epilogue)
+//   6. v2  = RMSNorm(h; ffn_norm)
+//   7. a   = SiLU(v2 W_gate^T) * (v2 W_up^T)  (SwiGLU in the epilogue)
+//   8. y   = h + a W_down^T                   (residual in the epilogue)
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "llama_block.h"
+#include "kernels.h"
+#include "tc_kernels.h"
+
+using namespace llama;
+
+namespace {
+
+struct Dims {
+  int d, H, G, D, F, QKV, max_seq;
+  float eps;
+  double theta;
+  int dtype;
+  size_t esize;
+};
+
+// Device allocations owned by one handle, freed together.
+struct Allocs {
+  std::vector<void *> ptrs;
+  bool failed = false;
+  void *alloc(size_t bytes) {
+    void *p = nullptr;
+    if (bytes == 0) bytes = 16;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) {
+      failed = true;
+      cudaGetLastError();
+      return nullptr;
+    }
+    ptrs.push_back(p);
+    return p;
+  }
+  void free_all() {
+    for (void *p : ptrs) cudaFree(p);
+    ptrs.clear();
+  }
+};
+
+struct Weights {
+  void *attn_norm = nullptr, *ffn_norm = nullptr;
+  void *wqkv = nullptr;  // [(H + 2G) D, d]: rows of Wq, then Wk, then Wv
+  void *wo = nullptr;    // [d, H D]
+  void *w_gate = nullptr, *w_up = nullptr;  // [F, d] each
+  void *w_gu = nullptr;  // bf16 tensor-core path: gate/up rows interleaved per 16-row group, [2F, d]
+  void *w_down = nullptr;  // [d, F]
+};
+
+struct Workspace {
+  int max_tokens = 0;
+  void *xn = nullptr, *qkv = nullptr, *q = nullptr, *o = nullptr, *h = nullptr, *act = nullptr, *hn = nullptr;
+  void *xin = nullptr, *yout = nullptr;  // staging for the host-buffer entry point
+  AttnScratch attn;                      // split-KV partials of the decode path
+};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_device_ptr(const void *p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+llama_status check_ptr(const void *p) {
+  if (p == nullptr) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(p)) return LLAMA_ERR_ALIGN;
+  if (!is_device_ptr(p)) return LLAMA_ERR_INVALID_ARG;
+  return LLAMA_OK;
+}
+
+llama_status validate_config(const llama_config *c, Dims *dm) {
+  if (c == nullptr) return LLAMA_ERR_INVALID_ARG;
+  if (c->dtype != LLAMA_F32 && c->dtype != LLAMA_BF16) return LLAMA_ERR_INVALID_ARG;
+  if (c->d_model <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->d_ff <= 0 || c->max_seq_len <= 0)
+    return LLAMA_ERR_INVALID_ARG;
+  if (!(c->norm_eps >= 0.f) || !(c->rope_theta > 0.f)) return LLAMA_ERR_INVALID_ARG;
+  if (c->d_model % c->n_heads != 0) return LLAMA_ERR_SHAPE;
+  if (c->n_heads % c->n_kv_heads != 0) return LLAMA_ERR_SHAPE;
+  const int D = c->d_model / c->n_heads;
+  if (D % 2 != 0) return LLAMA_ERR_SHAPE;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return LLAMA_ERR_UNSUPPORTED;
+  const int vec = c->dtype == LLAMA_BF16 ? 8 : 4;
+  if (c->d_model % vec != 0 || c->d_ff % vec != 0) return LLAMA_ERR_UNSUPPORTED;
+  if (c->dtype == LLAMA_BF16 && c->d_ff % 16 != 0) return LLAMA_ERR_UNSUPPORTED;  // gate/up interleave groups
+  dm->d = c->d_model;
+  dm->H = c->n_heads;
+  dm->G = c->n_kv_heads;
+  dm->D = D;
+  dm->F = c->d_ff;
+  dm->QKV = (c->n_heads + 2 * c->n_kv_heads) * D;
+  dm->max_seq = c->max_seq_len;
+  dm->eps = c->norm_eps;
+  dm->theta = (double)c->rope_theta;
+  dm->dtype = c->dtype;
+  dm->esize = c->dtype == LLAMA_BF16 ? 2 : 4;
+  return LLAMA_OK;
+}
+
+llama_status copy_weights(const Dims &dm, const llama_block_weights *w, Allocs &al, Weights *out) {
+  if (w == nullptr) return LLAMA_ERR_INVALID_ARG;
+  const void *ptrs[9] = {w->attn_norm, w->wq, w->wk, w->wv, w->wo, w->ffn_norm, w->w_gate, w->w_up, w->w_down};
+  for (const void *p : ptrs) {
+    llama_status s = check_ptr(p);
+    if (s != LLAMA_OK) return s;
+  }
+  const size_t e = dm.esize;
+  const size_t dq = (size_t)dm.H * dm.D * dm.d * e, dkv = (size_t)dm.G * dm.D * dm.d * e;
+  out->attn_norm = al.alloc(dm.d * e);
+  out->ffn_norm = al.alloc(dm.d * e);
+  out->wqkv = al.alloc(dq + 2 * dkv);
+  out->wo = al.alloc((size_t)dm.d * dm.H * dm.D * e);
+  out->w_down = al.alloc((size_t)dm.d * dm.F * e);
+  const bool tc = dm.dtype == LLAMA_BF16;
+  if (tc) {
+    out->w_gu = al.alloc((size_t)2 * dm.F * dm.d * e);
+  } else {
+    out->w_gate = al.alloc((size_t)dm.F * dm.d * e);
+    out->w_up = al.alloc((size_t)dm.F * dm.d * e);
+  }
+  if (al.failed) return LLAMA_ERR_OOM;
+  char *qkv = static_cast<char *>(out->wqkv);
+  cudaError_t err = cudaSuccess;
+  auto cp = [&](void *dst, const void *src, size_t n) {
+    if (err == cudaSuccess) err = cudaMemcpy(dst, src, n, cudaMemcpyDeviceToDevice);
+  };
+  cp(out->attn_norm, w->attn_norm, dm.d * e);
+  cp(out->ffn_norm, w->ffn_norm, dm.d * e);
+  cp(qkv, w->wq, dq);
+  cp(qkv + dq, w->wk, dkv);
+  cp(qkv + dq + dkv, w->wv, dkv);
+  cp(out->wo, w->wo, (size_t)dm.d * dm.H * dm.D * e);
+  cp(out->w_down, w->w_down, (size_t)dm.d * dm.F * e);
+  if (tc) {
+    if (err == cudaSuccess)
+      err = launch_interleave_rows((const bf16 *)w->w_gate, (const bf16 *)w->w_up, (bf16 *)out->w_gu, dm.F, dm.d,
+                                   nullptr);
+    if (err == cudaSuccess) err = cudaDeviceSynchronize();
+  } else {
+    cp(out->w_gate, w->w_gate, (size_t)dm.F * dm.d * e);
+    cp(out->w_up, w->w_up, (size_t)dm.F * dm.d * e);
+  }
+  return err == cudaSuccess ? LLAMA_OK : LLAMA_ERR_CUDA;
+}
+
+llama_status alloc_workspace(const Dims &dm, int max_tokens, bool staging, Allocs &al, Workspace *ws) {
+  const size_t e = dm.esize, T = (size_t)max_tokens;
+  ws->max_tokens = max_tokens;
+  ws->xn = al.alloc(T * dm.d * e);
+  ws->qkv = al.alloc(T * dm.QKV * e);
+  ws->q = al.alloc(T * dm.H * dm.D * e);
+  ws->o = al.alloc(T * dm.H * dm.D * e);
+  ws->h = al.alloc(T * dm.d * e);
+  ws->act = al.alloc(T * dm.F * e);
+  ws->hn = al.alloc(T * dm.d * e);
+  if (staging) {
+    ws->xin = al.alloc(T * dm.d * e);
+    ws->yout = al.alloc(T * dm.d * e);
+  }
+  if (dm.dtype == LLAMA_BF16) {
+    const size_t bytes = attn_decode_scratch_bytes(max_tokens, dm.H, dm.D, dm.max_seq);
+    ws->attn.partial = al.alloc(bytes);
+    ws->attn.bytes = bytes;
+  }
+  return al.failed ? LLAMA_ERR_OOM : LLAMA_OK;
+}
+
+#define LAUNCH(expr)                                 \
+  do {                                               \
+    cudaError_t _e = (expr);                         \
+    if (_e != cudaSuccess) return LLAMA_ERR_CUDA;    \
+  } while (0)
+
+template <typename T>
+llama_status forward_simt(const Dims &dm, const Weights &w, const Workspace &ws, const float2 *rope, const T *x,
+                          T *y, int B, int S, int start_pos, const llama_kv_cache *kv, cudaStream_t st) {
+  const int M = B * S;
+  T *xn = (T *)ws.xn, *qkv = (T *)ws.qkv, *q = (T *)ws.q, *o = (T *)ws.o, *h = (T *)ws.h, *act = (T *)ws.act,
+    *hn = (T *)ws.hn;
+  LAUNCH(launch_rmsnorm<T>(x, (const T *)w.attn_norm, xn, M, dm.d, dm.eps, st));
+  LAUNCH(launch_gemm_simt<T>(xn, (const T *)w.wqkv, nullptr, nullptr, qkv, M, dm.QKV, dm.d, EPI_STORE, st));
+  LAUNCH(launch_rope_kv<T>(qkv, q, (T *)kv->k, (T *)kv->v, rope, B, S, start_pos, dm.H, dm.G, dm.D,
+                           kv->max_seq_len, st));
+  LAUNCH(launch_attention_simt<T>(q, (const T *)kv->k, (const T *)kv->v, o, B, S, start_pos, dm.H, dm.G, dm.D,
+                                  kv->max_seq_len, st));
+  LAUNCH(launch_gemm_simt<T>(o, (const T *)w.wo, nullptr, x, h, M, dm.d, dm.H * dm.D, EPI_RESIDUAL, st));
+  LAUNCH(launch_rmsnorm<T>(h, (const T *)w.ffn_norm, hn, M, dm.d, dm.eps, st));
+  LAUNCH(launch_gemm_simt<T>(hn, (const T *)w.w_gate, (const T *)w.w_up, nullptr, act, M, dm.F, dm.d, EPI_SWIGLU,
+                             st));
+  LAUNCH(launch_gemm_simt<T>(act, (const T *)w.w_down, nullptr, h, y, M, dm.d, dm.F, EPI_RESIDUAL, st));
+  return LLAMA_OK;
+}
+
+llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, const float2 *rope, const bf16 *x,
+                        bf16 *y, int B, int S, int start_pos, const llama_kv_cache *kv, int *status,
+                        cudaStream_t st) {
+  const int M = B * S;
+  bf16 *xn = (bf16 *)ws.xn, *qkv = (bf16 *)ws.qkv, *q = (bf16 *)ws.q, *o = (bf16 *)ws.o, *h = (bf16 *)ws.h,
+       *act = (bf16 *)ws.act, *hn = (bf16 *)ws.hn;
+  bf16 *kc = (bf16 *)kv->k, *vc = (bf16 *)kv->v;
+  LAUNCH(launch_rmsnorm<bf16>(x, (const bf16 *)w.attn_norm, xn, M, dm.d, dm.eps, st));
+  LAUNCH(launch_gemm_tc(xn, (const bf16 *)w.wqkv, nullptr, qkv, M, dm.QKV, dm.d, EPI_STORE, status, st));
+  LAUNCH(launch_rope_kv<bf16>(qkv, q, kc, vc, rope, B, S, start_pos, dm.H, dm.G, dm.D, kv->max_seq_len, st));
+  LAUNCH(launch_attention(q, kc, vc, o, B, S, start_pos, dm.H, dm.G, dm.D, kv->max_seq_len, ws.attn, status, st));
+  LAUNCH(launch_gemm_tc(o, (const bf16 *)w.wo, x, h, M, dm.d, dm.H * dm.D, EPI_RESIDUAL, status, st));
+  LAUNCH(launch_rmsnorm<bf16>(h, (const bf16 *)w.ffn_norm, hn, M, dm.d, dm.eps, st));
+  LAUNCH(launch_gemm_tc(hn, (const bf16 *)w.w_gu, nullptr, act, M, 2 * dm.F, dm.d, EPI_SWIGLU, status, st));
+  LAUNCH(launch_gemm_tc(act, (const bf16 *)w.w_down, h, y, M, dm.d, dm.F, EPI_RESIDUAL, status, st));
+  return LLAMA_OK;
+}
+
+llama_status forward_any(const Dims &dm, const Weights &w, const Workspace &ws, const float2 *rope, const void *x,
+                         void *y, int B, int S, int start_pos, const llama_kv_cache *kv, int *status,
+                         cudaStream_t st) {
+  if (dm.dtype == LLAMA_BF16)
+    return forward_tc(dm, w, ws, rope, (const bf16 *)x, (bf16 *)y, B, S, start_pos, kv, status, st);
+  return forward_simt<float>(dm, w, ws, rope, (const float *)x, (float *)y, B, S, start_pos, kv, st);
+}
+
+llama_status validate_call(const Dims &dm, int max_tokens, int B, int S, int start_pos, const llama_kv_cache *kv) {
+  if (kv == nullptr) return LLAMA_ERR_INVALID_ARG;
+  if (B <= 0 || S <= 0 || start_pos < 0) return LLAMA_ERR_INVALID_ARG;
+  if ((long long)B * S > max_tokens) return LLAMA_ERR_RANGE;
+  if (B > kv->max_batch) return LLAMA_ERR_RANGE;
+  if ((long long)start_pos + S > dm.max_seq || (long long)start_pos + S > kv->max_seq_len) return LLAMA_ERR_RANGE;
+  llama_status s = check_ptr(kv->k);
+  if (s != LLAMA_OK) return s;
+  return check_ptr(kv->v);
+}
+
+llama_status read_status(int *dev_status, int device) {
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return LLAMA_ERR_CUDA;
+  if (prev != device && cudaSetDevice(device) != cudaSuccess) return LLAMA_ERR_CUDA;
+  int v = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&v, dev_status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(dev_status, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (prev != device) cudaSetDevice(prev);
+  if (e != cudaSuccess) return LLAMA_ERR_CUDA;
+  if (v == 0) return LLAMA_OK;
+  return v == DEV_BAD_TOKEN ? LLAMA_ERR_RANGE : LLAMA_ERR_DEVICE_TIMEOUT;
+}
+
+}  // namespace
+
+struct llama_block {
+  Dims dm;
+  int device = 0;
+  Allocs al;
+  Weights w;
+  Workspace ws;
+  float2 *rope = nullptr;
+  int *status = nullptr;
+};
+
+struct llama_stack {
+  Dims dm;
+  int device = 0, n_layers = 0, vocab = 0;
+  Allocs al;
+  std::vector<Weights> layers;
+  Workspace ws;
+  float2 *rope = nullptr;
+  int *status = nullptr;
+  void *embed = nullptr, *final_norm = nullptr, *lm_head = nullptr;
+  void *x0 = nullptr, *x1 = nullptr, *xn = nullptr;
+};
+
+extern "C" {
+
+llama_status llama_block_create(const llama_config *cfg, const llama_block_weights *w, int32_t max_tokens,
+                                llama_block **out) {
+  if (out == nullptr) return LLAMA_ERR_INVALID_ARG;
+  *out = nullptr;
+  Dims dm;
+  llama_status s = validate_config(cfg, &dm);
+  if (s != LLAMA_OK) return s;
+  if (max_tokens <= 0) return LLAMA_ERR_INVALID_ARG;
+  llama_block *b = new (std::nothrow) llama_block();
+  if (b == nullptr) return LLAMA_ERR_OOM;
+  b->dm = dm;
+  cudaGetDevice(&b->device);
+  s = copy_weights(dm, w, b->al, &b->w);
+  if (s == LLAMA_OK) s = alloc_workspace(dm, max_tokens, true, b->al, &b->ws);
+  if (s == LLAMA_OK) {
+    b->rope = (float2 *)b->al.alloc((size_t)dm.max_seq * (dm.D / 2) * sizeof(float2));
+    b->status = (int *)b->al.alloc(sizeof(int));
+    if (b->al.failed) s = LLAMA_ERR_OOM;
+  }
+  if (s == LLAMA_OK) {
+    if (launch_rope_table(b->rope, dm.max_seq, dm.D, dm.theta, nullptr) != cudaSuccess ||
+        cudaMemset(b->status, 0, sizeof(int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+      s = LLAMA_ERR_CUDA;
+  }
+  if (s != LLAMA_OK) {
+    b->al.free_all();
+    delete b;
+    return s;
+  }
+  *out = b;
+  return LLAMA_OK;
+}
+
+llama_status llama_block_forward(llama_block *blk, const void *x, void *y, int32_t B, int32_t S, int32_t start_pos,
+                                 const llama_kv_cache *kv, llama_stream stream) {
+  if (blk == nullptr) return LLAMA_ERR_INVALID_ARG;
+  llama_status s = check_ptr(x);
+  if (s == LLAMA_OK) s = check_ptr(y);
+  if (s == LLAMA_OK) s = validate_call(blk->dm, blk->ws.max_tokens, B, S, start_pos, kv);
+  if (s != LLAMA_OK) return s;
+  return forward_any(blk->dm, blk->w, blk->ws, blk->rope, x, y, B, S, start_pos, kv, blk->status,
+                     (cudaStream_t)stream);
+}
+
+llama_status llama_block_forward_host(llama_block *blk, const void *x_host, void *y_host, int32_t B, int32_t S,
+                                      int32_t start_pos, const llama_kv_cache *kv, llama_stream stream) {
+  if (blk == nullptr || x_host == nullptr || y_host == nullptr) return LLAMA_ERR_INVALID_ARG;
+  llama_status s = validate_call(blk->dm, blk->ws.max_tokens, B, S, start_pos, kv);
+  if (s != LLAMA_OK) return s;
+  const size_t bytes = (size_t)B * S * blk->dm.d * blk->dm.esize;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(blk->ws.xin, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return LLAMA_ERR_CUDA;
+  s = forward_any(blk->dm, blk->w, blk->ws, blk->rope, blk->ws.xin, blk->ws.yout, B, S, start_pos, kv,
+                  blk->status, st);
+  if (s != LLAMA_OK) return s;
+  if (cudaMemcpyAsync(y_host, blk->ws.yout, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return LLAMA_ERR_CUDA;
+  return LLAMA_OK;
+}
+
+void llama_block_destroy(llama_block *blk) {
+  if (blk == nullptr) return;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(blk->device);
+  cudaDeviceSynchronize();
+  blk->al.free_all();
+  cudaSetDevice(prev);
+  delete blk;
+}
+
+llama_status llama_block_device_status(llama_block *blk) {
+  if (blk == nullptr) return LLAMA_ERR_INVALID_ARG;
+  return read_status(blk->status, blk->device);
+}
+
+llama_status llama_stack_create(const llama_config *cfg, int32_t n_layers, int32_t vocab, const void *embed,
+                                const llama_block_weights *layers, const void *final_norm, const void *lm_head,
+                                int32_t max_tokens, llama_stack **out) {
+  if (out == nullptr) return LLAMA_ERR_INVALID_ARG;
+  *out = nullptr;
+  Dims dm;
+  llama_status s = validate_config(cfg, &dm);
+  if (s != LLAMA_OK) return s;
+  if (n_layers < 0 || vocab <= 0 || max_tokens <= 0 || (n_layers > 0 && layers == nullptr))
+    return LLAMA_ERR_INVALID_ARG;
+  for (const void *p : {embed, final_norm, lm_head}) {
+    s = check_ptr(p);
+    if (s != LLAMA_OK) return s;
+  }
+  llama_stack *k = new (std::nothrow) llama_stack();
+  if (k == nullptr) return LLAMA_ERR_OOM;
+  k->dm = dm;
+  k->n_layers = n_layers;
+  k->vocab = vocab;
+  cudaGetDevice(&k->device);
+  k->layers.resize(n_layers);
+  for (int l = 0; l < n_layers && s == LLAMA_OK; ++l) s = copy_weights(dm, &layers[l], k->al, &k->layers[l]);
+  if (s == LLAMA_OK) s = alloc_workspace(dm, max_tokens, false, k->al, &k->ws);
+  const size_t e = dm.esize;
+  if (s == LLAMA_OK) {
+    k->embed = k->al.alloc((size_t)vocab * dm.d * e);
+    k->lm_head = k->al.alloc((size_t)vocab * dm.d * e);
+    k->final_norm = k->al.alloc(dm.d * e);
+    k->x0 = k->al.alloc((size_t)max_tokens * dm.d * e);
+    k->x1 = k->al.alloc((size_t)max_tokens * dm.d * e);
+    k->xn = k->al.alloc((size_t)max_tokens * dm.d * e);
+    k->rope = (float2 *)k->al.alloc((size_t)dm.max_seq * (dm.D / 2) * sizeof(float2));
+    k->status = (int *)k->al.alloc(sizeof(int));
+    if (k->al.failed) s = LLAMA_ERR_OOM;
+  }
+  if (s == LLAMA_OK) {
+    cudaError_t err = cudaMemcpy(k->embed, embed, (size_t)vocab * dm.d * e, cudaMemcpyDeviceToDevice);
+    if (err == cudaSuccess) err = cudaMemcpy(k->lm_head, lm_head, (size_t)vocab * dm.d * e, cudaMemcpyDeviceToDevice);
+    if (err == cudaSuccess) err = cudaMemcpy(k->final_norm, final_norm, dm.d * e, cudaMemcpyDeviceToDevice);
+    if (err == cudaSuccess) err = launch_rope_table(k->rope, dm.max_seq, dm.D, dm.theta, nullptr);
+    if (err == cudaSuccess) err = cudaMemset(k->status, 0, sizeof(int));
+    if (err == cudaSuccess) err = cudaDeviceSynchronize();
+    if (err != cudaSuccess) s = LLAMA_ERR_CUDA;
+  }
+  if (s != LLAMA_OK) {
+    k->al.free_all();
+    delete k;
+    return s;
+  }
+  *out = k;
+  return LLAMA_OK;
+}
+
+llama_status llama_stack_forward(llama_stack *stk, const int32_t *tokens, int32_t B, int32_t S, int32_t start_pos,
+                                 const llama_kv_cache *kv, float *logits, llama_stream stream) {
+  if (stk == nullptr || (kv == nullptr && stk->n_layers > 0)) return LLAMA_ERR_INVALID_ARG;
+  llama_status s = check_ptr(tokens);
+  if (s == LLAMA_OK) s = check_ptr(logits);
+  if (s != LLAMA_OK) return s;
+  if (B <= 0 || S <= 0 || start_pos < 0) return LLAMA_ERR_INVALID_ARG;
+  if ((long long)B * S > stk->ws.max_tokens || (long long)start_pos + S > stk->dm.max_seq) return LLAMA_ERR_RANGE;
+  for (int l = 0; l < stk->n_layers; ++l) {
+    s = validate_call(stk->dm, stk->ws.max_tokens, B, S, start_pos, &kv[l]);
+    if (s != LLAMA_OK) return s;
+  }
+  const Dims &dm = stk->dm;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int M = B * S;
+  void *cur = stk->x0, *nxt = stk->x1;
+  if (dm.dtype == LLAMA_BF16)
+    LAUNCH(launch_embed<bf16>(tokens, (const bf16 *)stk->embed, (bf16 *)cur, M, dm.d, stk->vocab, stk->status, st));
+  else
+    LAUNCH(launch_embed<float>(tokens, (const float *)stk->embed, (float *)cur, M, dm.d, stk->vocab, stk->status, st));
+  for (int l = 0; l < stk->n_layers; ++l) {
+    s = forward_any(dm, stk->layers[l], stk->ws, stk->rope, cur, nxt, B, S, start_pos, &kv[l], stk->status, st);
+    if (s != LLAMA_OK) return s;
+    void *t = cur;
+    cur = nxt;
+    nxt = t;
+  }
+  if (dm.dtype == LLAMA_BF16) {
+    LAUNCH(launch_rmsnorm<bf16>((const bf16 *)cur, (const bf16 *)stk->final_norm, (bf16 *)stk->xn, M, dm.d, dm.eps, st));
+    LAUNCH(launch_gemm_tc((const bf16 *)stk->xn, (const bf16 *)stk->lm_head, nullptr, logits, M, stk->vocab, dm.d,
+                          EPI_F32OUT, stk->status, st));
+  } else {
+    LAUNCH(launch_rmsnorm<float>((const float *)cur, (const float *)stk->final_norm, (float *)stk->xn, M, dm.d, dm.eps,
+                                 st));
+    LAUNCH(launch_gemm_simt<float>((const float *)stk->xn, (const float *)stk->lm_head, nullptr, nullptr, logits, M,
+                                   stk->vocab, dm.d, EPI_F32OUT, st));
+  }
+  return LLAMA_OK;
+}
+
+void llama_stack_destroy(llama_stack *stk) {
+  if (stk == nullptr) return;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(stk->device);
+  cudaDeviceSynchronize();
+  stk->al.free_all();
+  cudaSetDevice(prev);
+  delete stk;
+}
+
+llama_status llama_stack_device_status(llama_stack *stk) {
+  if (stk == nullptr) return LLAMA_ERR_INVALID_ARG;
+  return read_status(stk->status, stk->device);
+}
+
+size_t llama_kv_cache_bytes(const llama_config *cfg, int32_t max_batch, int32_t max_seq_len) {
+  Dims dm;
+  if (validate_config(cfg, &dm) != LLAMA_OK || max_batch <= 0 || max_seq_len <= 0) return 0;
+  return 2 * (size_t)max_batch * dm.G * (size_t)max_seq_len * dm.D * dm.esize;
+}
+
+int32_t llama_ffn_hidden_dim(int32_t d_model, int32_t multiple_of, float ffn_dim_multiplier) {
+  if (d_model <= 0 || multiple_of <= 0) return -1;
+  long long h = 4LL * d_model;
+  h = (2 * h) / 3;
+  if (ffn_dim_multiplier > 0.f) h = (long long)((double)ffn_dim_multiplier * (double)h);
+  h = (long long)multiple_of * ((h + multiple_of - 1) / multiple_of);
+  return h > 0x7fffffffLL ? -1 : (int32_t)h;
+}
+
+const char *llama_status_string(llama_status s) {
+  switch (s) {
+    case LLAMA_OK: return "ok";
+    case LLAMA_ERR_INVALID_ARG: return "invalid argument";
+    case LLAMA_ERR_SHAPE: return "inconsistent shape";
+    case LLAMA_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case LLAMA_ERR_RANGE: return "size or position out of range";
+    case LLAMA_ERR_UNSUPPORTED: return "unsupported shape";
+    case LLAMA_ERR_OOM: return "device out of memory";
+    case LLAMA_ERR_CUDA: return "CUDA error";
+    case LLAMA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,325 @@
+// Portable CUDA-core kernels of the decoder block: RMSNorm, RoPE + KV-cache
+// write, embedding gather, and the fp32-accumulating GEMM / attention used by
+// the fp32 path (tiny configuration) and as the fallback for shapes the tensor
+// core kernels do not cover.
+#include "kernels.h"
+
+namespace llama {
+
+// ---------------------------------------------------------------- RMSNorm ---
+// "The Evolving Transformer 04 · LLaMA", §03 RMSNorm: x * rsqrt(mean(x^2) + eps) * g.
+// One warp per row, 16-byte vectors, fp32 sum of squares; second pass re-reads
+// the row (L1/L2 resident) to normalise and scale.
+template <typename T>
+__global__ void rmsnorm_kernel(const T *__restrict__ x, const T *__restrict__ g, T *__restrict__ out, int rows,
+                               int d, float eps) {
+  constexpr int V = Vec16<T>::N;
+  const int row = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const T *xr = x + (size_t)row * d;
+  T *orow = out + (size_t)row * d;
+  const int nv = d / V;
+  float ss = 0.f;
+  for (int i = lane; i < nv; i += 32) {
+    Vec16<T> v = load16(xr + (size_t)i * V);
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      float f = v.get(k);
+      ss = fmaf(f, f, ss);
+    }
+  }
+  ss = warp_sum(ss);
+  const float r = rsqrtf(ss / (float)d + eps);
+  for (int i = lane; i < nv; i += 32) {
+    Vec16<T> v = load16(xr + (size_t)i * V);
+    Vec16<T> gv = load16(g + (size_t)i * V);
+    Vec16<T> o;
+#pragma unroll
+    for (int k = 0; k < V; ++k) o.set(k, v.get(k) * r * gv.get(k));
+    store16(orow + (size_t)i * V, o);
+  }
+}
+
+template <typename T>
+cudaError_t launch_rmsnorm(const T *x, const T *g, T *out, int rows, int d, float eps, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  const int threads = 256;
+  const int blocks = (int)(((size_t)rows * 32 + threads - 1) / threads);
+  rmsnorm_kernel<T><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ SIMT GEMM ---
+// C[M,N] = A[M,K] W[N,K]^T (nn.Linear, no bias), fp32 accumulation.
+// 64x64 output tile per 256-thread CTA, 4x4 per thread, K step 16.
+constexpr int SG_BM = 64, SG_BN = 64, SG_BK = 16;
+
+template <typename T, int EPI>
+__global__ void __launch_bounds__(256) gemm_simt_kernel(const T *__restrict__ A, const T *__restrict__ W,
+                                                        const T *__restrict__ W3, const T *__restrict__ R,
+                                                        void *__restrict__ C, int M, int N, int K) {
+  __shared__ float As[SG_BK][SG_BM + 4];
+  __shared__ float Ws[SG_BK][SG_BN + 4];
+  __shared__ float W3s[EPI == EPI_SWIGLU ? SG_BK : 1][EPI == EPI_SWIGLU ? SG_BN + 4 : 1];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  const int m0 = blockIdx.y * SG_BM, n0 = blockIdx.x * SG_BN;
+  float acc[4][4], acc3[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = acc3[i][j] = 0.f;
+
+  for (int k0 = 0; k0 < K; k0 += SG_BK) {
+    for (int i = threadIdx.x; i < SG_BM * SG_BK; i += 256) {
+      const int r = i / SG_BK, kk = i % SG_BK;
+      const int k = k0 + kk;
+      const int m = m0 + r, n = n0 + r;
+      As[kk][r] = (m < M && k < K) ? to_f32<T>(A[(size_t)m * K + k]) : 0.f;
+      Ws[kk][r] = (n < N && k < K) ? to_f32<T>(W[(size_t)n * K + k]) : 0.f;
+      if constexpr (EPI == EPI_SWIGLU) W3s[kk][r] = (n < N && k < K) ? to_f32<T>(W3[(size_t)n * K + k]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < SG_BK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Ws[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) b[j] = W3s[kk][tx * 4 + j];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc3[i][j] = fmaf(a[i], b[j], acc3[i][j]);
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty * 4 + i;
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx * 4 + j;
+      if (n >= N) continue;
+      const size_t idx = (size_t)m * N + n;
+      float v = acc[i][j];
+      if constexpr (EPI == EPI_RESIDUAL) v += to_f32<T>(R[idx]);
+      if constexpr (EPI == EPI_SWIGLU) v = silu_f32(v) * acc3[i][j];
+      if constexpr (EPI == EPI_F32OUT)
+        reinterpret_cast<float *>(C)[idx] = v;
+      else
+        reinterpret_cast<T *>(C)[idx] = from_f32<T>(v);
+    }
+  }
+}
+
+template <typename T>
+cudaError_t launch_gemm_simt(const T *A, const T *W, const T *W3, const T *R, void *C, int M, int N, int K,
+                             int epi, cudaStream_t st) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  dim3 grid((N + SG_BN - 1) / SG_BN, (M + SG_BM - 1) / SG_BM);
+  switch (epi) {
+    case EPI_STORE: gemm_simt_kernel<T, EPI_STORE><<<grid, 256, 0, st>>>(A, W, W3, R, C, M, N, K); break;
+    case EPI_RESIDUAL: gemm_simt_kernel<T, EPI_RESIDUAL><<<grid, 256, 0, st>>>(A, W, W3, R, C, M, N, K); break;
+    case EPI_F32OUT: gemm_simt_kernel<T, EPI_F32OUT><<<grid, 256, 0, st>>>(A, W, W3, R, C, M, N, K); break;
+    case EPI_SWIGLU: gemm_simt_kernel<T, EPI_SWIGLU><<<grid, 256, 0, st>>>(A, W, W3, R, C, M, N, K); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ RoPE table ---
+// "Mini Llama 2 Implementation", Rotary positional embeddings: angle of pair i
+// at position p is p * theta^(-2i/D).  Built once per block in fp64, stored fp32.
+__global__ void rope_table_kernel(float2 *table, int max_seq, int D, double theta) {
+  const int half = D / 2;
+  const size_t n = (size_t)max_seq * half;
+  for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < n; idx += (size_t)gridDim.x * blockDim.x) {
+    const int p = (int)(idx / half), i = (int)(idx % half);
+    const double f = pow(theta, -2.0 * (double)i / (double)D);
+    double s, c;
+    sincos((double)p * f, &s, &c);
+    table[idx] = make_float2((float)c, (float)s);
+  }
+}
+
+cudaError_t launch_rope_table(float2 *table, int max_seq, int D, double theta, cudaStream_t st) {
+  const size_t n = (size_t)max_seq * (D / 2);
+  const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  rope_table_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(table, max_seq, D, theta);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------ RoPE + KV write ---
+// Each thread owns one 16-byte vector of a token's fused [q | k | v] row; a
+// vector never straddles a head (D % 8 == 0) and holds whole (2i, 2i+1) pairs.
+// q: rotated into q_out; k: rotated into the K cache at position start_pos + s;
+// v: copied into the V cache ("Full Llama 3 transformer block", How it works:
+// RoPE rotates Q and K, keys/values are written into a cache).
+template <typename T>
+__global__ void rope_kv_kernel(const T *__restrict__ qkv, T *__restrict__ q_out, T *__restrict__ kc,
+                               T *__restrict__ vc, const float2 *__restrict__ table, int ntok, int S, int start_pos,
+                               int H, int G, int D, int cache_seq) {
+  constexpr int V = Vec16<T>::N;
+  const int row_vecs = (H + 2 * G) * D / V;
+  const size_t total = (size_t)ntok * row_vecs;
+  const size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  if (idx >= total) return;
+  const int t = (int)(idx / row_vecs);
+  const int col = (int)(idx % row_vecs) * V;
+  const int head = col / D, e = col % D;
+  const int b = t / S, s = t % S, p = start_pos + s;
+  Vec16<T> x = load16(qkv + (size_t)t * (H + 2 * G) * D + col);
+  if (head < H + G) {
+    const float2 *cs = table + (size_t)p * (D / 2) + e / 2;
+    Vec16<T> o;
+#pragma unroll
+    for (int k = 0; k < V / 2; ++k) {
+      const float2 c = cs[k];
+      const float a = x.get(2 * k), bb = x.get(2 * k + 1);
+      o.set(2 * k, a * c.x - bb * c.y);
+      o.set(2 * k + 1, a * c.y + bb * c.x);
+    }
+    if (head < H) {
+      store16(q_out + (size_t)t * H * D + col, o);
+    } else {
+      const int g = head - H;
+      store16(kc + (((size_t)b * G + g) * cache_seq + p) * D + e, o);
+    }
+  } else {
+    const int g = head - H - G;
+    store16(vc + (((size_t)b * G + g) * cache_seq + p) * D + e, x);
+  }
+}
+
+template <typename T>
+cudaError_t launch_rope_kv(const T *qkv, T *q_out, T *kc, T *vc, const float2 *table, int B, int S,
+                           int start_pos, int H, int G, int D, int cache_seq, cudaStream_t st) {
+  constexpr int V = Vec16<T>::N;
+  const size_t total = (size_t)B * S * ((H + 2 * G) * D / V);
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  rope_kv_kernel<T><<<(unsigned)((total + threads - 1) / threads), threads, 0, st>>>(
+      qkv, q_out, kc, vc, table, B * S, S, start_pos, H, G, D, cache_seq);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------ SIMT attention ---
+// "The Evolving Transformer 04 · LLaMA", §05 GQA: softmax(q k^T / sqrt(D)) v
+// with query head h reading KV head h / (H / G) and keys j <= start_pos + s.
+// One warp per (token, head); lanes split the head dimension; online softmax.
+template <typename T>
+__global__ void attention_simt_kernel(const T *__restrict__ q, const T *__restrict__ kc, const T *__restrict__ vc,
+                                      T *__restrict__ o, int ntok, int S, int start_pos, int H, int G, int D,
+                                      int cache_seq, float scale) {
+  const size_t wid = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= (size_t)ntok * H) return;
+  const int t = (int)(wid / H), h = (int)(wid % H);
+  const int b = t / S, s = t % S;
+  const int g = h / (H / G);
+  const int L = start_pos + s + 1;
+  constexpr int MAXE = 4;  // D <= 128
+  float qv[MAXE], acc[MAXE];
+#pragma unroll
+  for (int k = 0; k < MAXE; ++k) {
+    const int e = lane + 32 * k;
+    qv[k] = e < D ? to_f32<T>(q[((size_t)t * H + h) * D + e]) * scale : 0.f;
+    acc[k] = 0.f;
+  }
+  const T *kb = kc + ((size_t)b * G + g) * cache_seq * D;
+  const T *vb = vc + ((size_t)b * G + g) * cache_seq * D;
+  float m = -INFINITY, l = 0.f;
+  for (int j = 0; j < L; ++j) {
+    float dot = 0.f;
+#pragma unroll
+    for (int k = 0; k < MAXE; ++k) {
+      const int e = lane + 32 * k;
+      if (e < D) dot = fmaf(qv[k], to_f32<T>(kb[(size_t)j * D + e]), dot);
+    }
+    dot = warp_sum(dot);
+    const float mn = fmaxf(m, dot);
+    const float corr = expf(m - mn);
+    const float p = expf(dot - mn);
+    l = l * corr + p;
+#pragma unroll
+    for (int k = 0; k < MAXE; ++k) {
+      const int e = lane + 32 * k;
+      if (e < D) acc[k] = fmaf(p, to_f32<T>(vb[(size_t)j * D + e]), acc[k] * corr);
+    }
+    m = mn;
+  }
+  const float inv = 1.f / l;
+#pragma unroll
+  for (int k = 0; k < MAXE; ++k) {
+    const int e = lane + 32 * k;
+    if (e < D) o[((size_t)t * H + h) * D + e] = from_f32<T>(acc[k] * inv);
+  }
+}
+
+template <typename T>
+cudaError_t launch_attention_simt(const T *q, const T *kc, const T *vc, T *o, int B, int S, int start_pos, int H,
+                                  int G, int D, int cache_seq, cudaStream_t st) {
+  const size_t warps = (size_t)B * S * H;
+  if (warps == 0) return cudaSuccess;
+  const int threads = 256;
+  const unsigned blocks = (unsigned)((warps * 32 + threads - 1) / threads);
+  attention_simt_kernel<T><<<blocks, threads, 0, st>>>(q, kc, vc, o, B * S, S, start_pos, H, G, D, cache_seq,
+                                                       1.0f / sqrtf((float)D));
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ embedding ---
+// "The Evolving Transformer 04 · LLaMA", §01 Embeddings: x = wte(ids), no position table.
+template <typename T>
+__global__ void embed_kernel(const int32_t *__restrict__ tokens, const T *__restrict__ E, T *__restrict__ x,
+                             int ntok, int d, int vocab, int *status) {
+  constexpr int V = Vec16<T>::N;
+  const int nv = d / V;
+  const size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  if (idx >= (size_t)ntok * nv) return;
+  const int t = (int)(idx / nv), c = (int)(idx % nv) * V;
+  const int id = tokens[t];
+  Vec16<T> v;
+  if (id < 0 || id >= vocab) {
+    v.raw = make_uint4(0, 0, 0, 0);
+    if (c == 0) report_status(status, DEV_BAD_TOKEN);
+  } else {
+    v = load16(E + (size_t)id * d + c);
+  }
+  store16(x + (size_t)t * d + c, v);
+}
+
+template <typename T>
+cudaError_t launch_embed(const int32_t *tokens, const T *E, T *x, int ntok, int d, int vocab, int *status,
+                         cudaStream_t st) {
+  constexpr int V = Vec16<T>::N;
+  const size_t total = (size_t)ntok * (d / V);
+  if (total == 0) return cudaSuccess;
+  embed_kernel<T><<<(unsigned)((total + 255) / 256), 256, 0, st>>>(tokens, E, x, ntok, d, vocab, status);
+  return cudaGetLastError();
+}
+
+#define INSTANTIATE(T)                                                                                            \
+  template cudaError_t launch_rmsnorm<T>(const T *, const T *, T *, int, int, float, cudaStream_t);               \
+  template cudaError_t launch_gemm_simt<T>(const T *, const T *, const T *, const T *, void *, int, int, int, int, \
+                                           cudaStream_t);                                                         \
+  template cudaError_t launch_rope_kv<T>(const T *, T *, T *, T *, const float2 *, int, int, int, int, int, int,  \
+                                         int, cudaStream_t);                                                      \
+  template cudaError_t launch_attention_simt<T>(const T *, const T *, const T *, T *, int, int, int, int, int,    \
+                                                int, int, cudaStream_t);                                          \
+  template cudaError_t launch_embed<T>(const int32_t *, const T *, T *, int, int, int, int *, cudaStream_t);
+
+INSTANTIATE(float)
+INSTANTIATE(bf16)
+
+}  // namespace llama

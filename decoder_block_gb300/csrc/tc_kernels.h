@@ -1,0 +1,39 @@
+// Internal launch wrappers of the sm_103a tensor-core (tcgen05 / TMA) kernels
+// and the bf16 attention paths.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "common.cuh"
+
+namespace llama {
+
+// C[M,N] = epi(A[M,K] W[N,K]^T) on tcgen05 tensor cores, bf16 operands, fp32
+// accumulation in TMEM.  Epilogues (kernels.h Epilogue):
+//   EPI_STORE    C bf16 [M,N]
+//   EPI_RESIDUAL C bf16 [M,N] = R + acc (R bf16 [M,N]; C may equal R)
+//   EPI_SWIGLU   W holds gate/up rows interleaved in groups of 16 (see
+//                launch_interleave_rows); C bf16 [M, N/2] = SiLU(gate) * up
+//   EPI_F32OUT   C fp32 [M,N]
+// Requirements: K % 8 == 0 (16-byte TMA row pitch); EPI_SWIGLU needs N % 32 == 0.
+// status: device status word for bounded-wait expiry (may be null).
+cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C, int M, int N, int K, int epi,
+                           int *status, cudaStream_t st);
+
+// out[32j + i] = gate[16j + i], out[32j + 16 + i] = up[16j + i] (rows of width d), F % 16 == 0.
+cudaError_t launch_interleave_rows(const bf16 *gate, const bf16 *up, bf16 *out, int F, int d, cudaStream_t st);
+
+// Scratch of the split-KV decode attention (fp32 partial outputs and row stats).
+struct AttnScratch {
+  void *partial = nullptr;
+  size_t bytes = 0;
+};
+size_t attn_decode_scratch_bytes(int max_tokens, int H, int D, int max_seq);
+
+// Causal GQA attention over the bf16 cache; picks the prefill or decode kernel.
+cudaError_t launch_attention(const bf16 *q, const bf16 *kc, const bf16 *vc, bf16 *o, int B, int S, int start_pos,
+                             int H, int G, int D, int cache_seq, const AttnScratch &scratch, int *status,
+                             cudaStream_t st);
+
+}  // namespace llama

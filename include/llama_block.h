@@ -1,0 +1,165 @@
+/*
+ * llama_block.h -- C ABI of the GB300 (sm_103a) Llama pre-norm decoder block.
+ *
+ * Operation (one block, "Full Llama 3 transformer block", How it works):
+ *     h = x + Attn(RMSNorm_1(x)),   y = h + FFN(RMSNorm_2(h))
+ *   RMSNorm(x) = x / sqrt(mean(x^2) + norm_eps) * g        ("The Evolving Transformer 04 · LLaMA", §03)
+ *   Attn: q = u Wq^T, k = u Wk^T, v = u Wv^T (no bias); RoPE rotates interleaved
+ *         pairs (2i, 2i+1) of q and k by angle p * rope_theta^(-2i/d_head) at
+ *         absolute position p = start_pos + s (§02 RoPE; "Mini Llama 2
+ *         Implementation", Rotary positional embeddings); rotated k and raw v
+ *         are written into the KV cache at positions [start_pos, start_pos + S);
+ *         query head h attends to KV head h / (n_heads / n_kv_heads) over cache
+ *         positions j <= start_pos + s with softmax(q.k / sqrt(d_head)) (§05 GQA);
+ *         o is projected by Wo.
+ *   FFN:  W_down(SiLU(W_gate v) * (W_up v))                 (§04 SwiGLU; How it works: W1, W3, W2)
+ *
+ * Conventions for every entry point below:
+ *   - All tensor pointers are DEVICE pointers unless the name says _host.
+ *   - Weights use nn.Linear layout [out_features, in_features], row-major.
+ *   - Activations are token-major: x[b][s][d_model], row-major, contiguous.
+ *   - dtype LLAMA_BF16: bf16 storage, fp32 accumulation; LLAMA_F32: fp32 throughout.
+ *   - Functions that take a stream only ENQUEUE work on it (no host sync) and
+ *     return after validation; a non-OK status means nothing was enqueued.
+ *   - Every pointer must be 16-byte aligned (LLAMA_ERR_ALIGN otherwise).
+ *   - Errors are returned, never raised or aborted on; llama_status_string()
+ *     names them.  Kernels never trap: a device-side wait that exceeds its
+ *     budget, or an out-of-range token id, sets the handle's device status
+ *     word, read with llama_block_device_status() / llama_stack_device_status().
+ */
+#ifndef LLAMA_BLOCK_H
+#define LLAMA_BLOCK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (CUstream) handle; NULL means the legacy default stream. */
+typedef struct CUstream_st *llama_stream;
+
+typedef enum {
+    LLAMA_OK = 0,
+    LLAMA_ERR_INVALID_ARG = 1,   /* null pointer, bad enum, non-positive size */
+    LLAMA_ERR_SHAPE = 2,         /* d_model % n_heads, n_heads % n_kv_heads, odd d_head ... */
+    LLAMA_ERR_ALIGN = 3,         /* a pointer is not 16-byte aligned */
+    LLAMA_ERR_RANGE = 4,         /* start_pos + S beyond the cache / table, B beyond max_batch, T beyond max_tokens */
+    LLAMA_ERR_UNSUPPORTED = 5,   /* valid Llama shape this build has no kernel for */
+    LLAMA_ERR_OOM = 6,           /* device allocation failed in a create call */
+    LLAMA_ERR_CUDA = 7,          /* a CUDA runtime/driver call failed */
+    LLAMA_ERR_DEVICE_TIMEOUT = 8 /* a kernel's bounded wait ran out (see llama_get_device_status) */
+} llama_status;
+
+typedef enum { LLAMA_F32 = 0, LLAMA_BF16 = 1 } llama_dtype;
+
+/* Fields follow LlamaConfig / ModelArgs ("The Evolving Transformer 04 · LLaMA",
+ * §00 Config; "Full Llama 3 transformer block", How it works).  d_head is
+ * derived as d_model / n_heads.  max_seq_len bounds start_pos + S and sizes the
+ * RoPE table.  Requirements: d_model % n_heads == 0, n_heads % n_kv_heads == 0,
+ * d_head even and in {16, 32, 64, 128}, d_model and d_ff multiples of 8 (bf16)
+ * or 4 (fp32), norm_eps >= 0, rope_theta > 0. */
+typedef struct {
+    int32_t d_model;
+    int32_t n_heads;
+    int32_t n_kv_heads;
+    int32_t d_ff;
+    int32_t max_seq_len;
+    float norm_eps;
+    float rope_theta;
+    int32_t dtype; /* llama_dtype */
+} llama_config;
+
+/* Device pointers to one block's parameters, dtype = config.dtype.
+ * attn_norm, ffn_norm: [d_model]; wq: [n_heads*d_head, d_model];
+ * wk, wv: [n_kv_heads*d_head, d_model]; wo: [d_model, n_heads*d_head];
+ * w_gate, w_up: [d_ff, d_model]; w_down: [d_model, d_ff].  No biases. */
+typedef struct {
+    const void *attn_norm, *wq, *wk, *wv, *wo, *ffn_norm, *w_gate, *w_up, *w_down;
+} llama_block_weights;
+
+/* Caller-owned KV cache of one layer: k and v are each
+ * [max_batch][n_kv_heads][max_seq_len][d_head], dtype = config.dtype.  K is
+ * stored after RoPE, V as projected.  Sequence b of a call uses row b.  A
+ * forward call writes exactly positions [start_pos, start_pos + S) of rows
+ * [0, B) and leaves every other element bit-for-bit unchanged. */
+typedef struct {
+    void *k;
+    void *v;
+    int32_t max_batch;
+    int32_t max_seq_len;
+} llama_kv_cache;
+
+typedef struct llama_block llama_block;
+typedef struct llama_stack llama_stack;
+
+/* Validate cfg, copy/repack the weights into library-owned device memory (the
+ * caller may free its copies afterwards) and reserve workspace for up to
+ * max_tokens = B*S tokens per forward call.  Synchronous.  On error *out is
+ * NULL and nothing stays allocated. */
+llama_status llama_block_create(const llama_config *cfg, const llama_block_weights *w,
+                                int32_t max_tokens, llama_block **out);
+
+/* One block forward over x [B][S][d_model] -> y (same shape; y may alias x),
+ * positions start_pos .. start_pos + S - 1 of each sequence, reading and
+ * writing kv.  Requirements: 1 <= B <= kv->max_batch, S >= 1, B*S <= max_tokens,
+ * 0 <= start_pos, start_pos + S <= min(cfg.max_seq_len, kv->max_seq_len).
+ * Asynchronous on stream.  Calls on one llama_block must not overlap in time
+ * (they share its workspace). */
+llama_status llama_block_forward(llama_block *blk, const void *x, void *y, int32_t B, int32_t S,
+                                 int32_t start_pos, const llama_kv_cache *kv, llama_stream stream);
+
+/* Same as llama_block_forward but x_host / y_host are HOST buffers (pinned
+ * memory recommended): copies x in, runs the block, copies y out, all on
+ * stream; returns after enqueueing (synchronise the stream before reading
+ * y_host).  The KV cache stays on the device. */
+llama_status llama_block_forward_host(llama_block *blk, const void *x_host, void *y_host, int32_t B,
+                                      int32_t S, int32_t start_pos, const llama_kv_cache *kv,
+                                      llama_stream stream);
+
+void llama_block_destroy(llama_block *blk);
+
+/* Full stack ("The Evolving Transformer 04 · LLaMA", §01 Embeddings, §07
+ * Assemble): token embedding gather (no position table), n_layers blocks,
+ * final RMSNorm, untied LM head.  embed: [vocab][d_model]; layers: array of
+ * n_layers weight sets; final_norm: [d_model]; lm_head: [vocab][d_model]; all
+ * device pointers of cfg.dtype, copied at create. */
+llama_status llama_stack_create(const llama_config *cfg, int32_t n_layers, int32_t vocab,
+                                const void *embed, const llama_block_weights *layers,
+                                const void *final_norm, const void *lm_head, int32_t max_tokens,
+                                llama_stack **out);
+
+/* tokens: int32 [B][S] in [0, vocab) (device); kv: array of n_layers caches;
+ * logits: fp32 [B][S][vocab] (device).  Same range rules as the block. */
+llama_status llama_stack_forward(llama_stack *stk, const int32_t *tokens, int32_t B, int32_t S,
+                                 int32_t start_pos, const llama_kv_cache *kv, float *logits,
+                                 llama_stream stream);
+
+void llama_stack_destroy(llama_stack *stk);
+
+/* Bytes of one layer's K plus V cache for max_batch x max_seq_len positions:
+ * 2 * max_batch * n_kv_heads * max_seq_len * d_head * sizeof(dtype) ("Llama 4
+ * From Scratch", Worked example: 2 x KV heads x head width per token).
+ * Returns 0 for an invalid config. */
+size_t llama_kv_cache_bytes(const llama_config *cfg, int32_t max_batch, int32_t max_seq_len);
+
+/* SwiGLU inner width rule ("Full Llama 3 transformer block", How it works):
+ * 4*d_model -> floor(2/3) -> floor(x ffn_dim_multiplier) when the multiplier
+ * is > 0 -> round up to a multiple of multiple_of.  Returns -1 on bad input. */
+int32_t llama_ffn_hidden_dim(int32_t d_model, int32_t multiple_of, float ffn_dim_multiplier);
+
+const char *llama_status_string(llama_status s);
+
+/* Read and clear the handle's device status word.  Synchronises the device the
+ * handle lives on.  Returns LLAMA_OK when no kernel reported a problem since
+ * the last read, LLAMA_ERR_DEVICE_TIMEOUT when a bounded wait ran out,
+ * LLAMA_ERR_RANGE when a token id was outside [0, vocab) (its embedding row
+ * was written as zeros), LLAMA_ERR_CUDA when the read itself failed. */
+llama_status llama_block_device_status(llama_block *blk);
+llama_status llama_stack_device_status(llama_stack *stk);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LLAMA_BLOCK_H */

@@ -1,0 +1,59 @@
+/*
+ * llama_ops.h -- per-step entry points of the decoder block (same kernels the
+ * block forward launches), for unit-level parity checks and for callers that
+ * compose the steps themselves.  Conventions as in llama_block.h: device
+ * pointers, 16-byte alignment, row-major, asynchronous on `stream`, errors
+ * returned (nothing enqueued on error).  dtype is LLAMA_F32 or LLAMA_BF16.
+ * These entry points allocate nothing and report device-side wait expiry only
+ * through their return of later calls' CUDA errors (no status word).
+ */
+#ifndef LLAMA_OPS_H
+#define LLAMA_OPS_H
+
+#include "llama_block.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* RMSNorm of T rows of width d ("The Evolving Transformer 04 · LLaMA", §03):
+ * out[t] = x[t] / sqrt(mean(x[t]^2) + eps) * g.  x, out: [T][d]; g: [d].
+ * d must be a multiple of 8 (bf16) or 4 (fp32).  out may alias x. */
+llama_status llama_op_rmsnorm(int32_t dtype, const void *x, const void *g, void *out, int32_t T, int32_t d,
+                              float eps, llama_stream stream);
+
+/* Linear layer without bias ("The Evolving Transformer 04 · LLaMA", §05: nn.Linear(bias=False)):
+ *   epilogue 0: C = A W^T            C [M][N], dtype
+ *   epilogue 1: C = R + A W^T        R, C [M][N], dtype (C may alias R)
+ *   epilogue 2: C = A W^T            C [M][N], fp32
+ * A: [M][K]; W: [N][K].  K must be a multiple of 8.  bf16 runs on the tcgen05
+ * tensor cores with fp32 accumulation; fp32 runs on CUDA cores. */
+llama_status llama_op_linear(int32_t dtype, const void *A, const void *W, const void *R, void *C, int32_t M,
+                             int32_t N, int32_t K, int32_t epilogue, llama_stream stream);
+
+/* Causal grouped-query attention over a KV cache ("The Evolving Transformer 04
+ * · LLaMA", §05 GQA; "Full Llama 3 transformer block", How it works):
+ * o[b][s][h] = sum_{j <= start_pos + s} softmax_j(q[b][s][h] . K[b][h / (H/G)][j] / sqrt(D)) V[b][h / (H/G)][j].
+ * q, o: [B][S][H][D] (q already rotated); kv->k, kv->v: [max_batch][G][max_seq_len][D].
+ * Requirements as for llama_block_forward; D in {16, 32, 64, 128}. */
+llama_status llama_op_attention(int32_t dtype, const void *q, const llama_kv_cache *kv, void *o, int32_t B,
+                                int32_t S, int32_t start_pos, int32_t H, int32_t G, int32_t D, llama_stream stream);
+
+/* RoPE cos/sin table: table[p][i] = {cos(p f_i), sin(p f_i)}, f_i = theta^(-2i/D),
+ * p in [0, max_seq), i in [0, D/2), fp32 pairs computed in fp64 ("Mini Llama 2
+ * Implementation", Rotary positional embeddings).  table: float[max_seq][D/2][2]. */
+llama_status llama_op_rope_table(float *table, int32_t max_seq, int32_t D, float theta, llama_stream stream);
+
+/* RoPE + KV-cache write: qkv [B*S][(H + 2G) D] holds, per token, q (H heads),
+ * k (G heads), v (G heads).  Writes q rotated at position start_pos + s to
+ * q_out [B*S][H][D], k rotated to kv->k[b][g][start_pos + s], v unrotated to
+ * kv->v[b][g][start_pos + s]; nothing else in the cache changes.
+ * table from llama_op_rope_table with max_seq >= start_pos + S. */
+llama_status llama_op_rope_kv_write(int32_t dtype, const void *qkv, void *q_out, const llama_kv_cache *kv,
+                                    const float *table, int32_t table_max_seq, int32_t B, int32_t S,
+                                    int32_t start_pos, int32_t H, int32_t G, int32_t D, llama_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LLAMA_OPS_H */
