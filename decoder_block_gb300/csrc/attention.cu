@@ -1,8 +1,397 @@
-// bf16 attention dispatch: causal GQA over the KV cache.
+// Causal grouped-query attention over the bf16 KV cache on tcgen05 tensor cores
+// ("The Evolving Transformer 04 · LLaMA", §05 GQA; "Full Llama 3 transformer
+// block", How it works: cache read with the start_pos offset mask).
+//
+// Prefill kernel (one CTA per (sequence b, KV head g, block of 2*Mq query
+// positions), 320 threads):
+//   * A 128-row query tile packs the r = H/G query heads of group g: row
+//     hh*Mq + i is head g*r + hh at position q0 + i (Mq = 128 / r rounded to a
+//     power of two).  Each K/V tile that lands in shared memory therefore
+//     serves every query head of its group; the CTA holds two such tiles
+//     (t = 0, 1: consecutive position blocks) that ping-pong.
+//   * warp 0: TMA producer -- Q tiles once, then 128-key K and V tiles into a
+//     two-stage ring.  K/V tensor maps end at start_pos + S, so keys beyond
+//     the valid cache read as zeros.
+//   * warp 1: tcgen05.mma issuer -- S_t = Q_t K^T (fp32 in TMEM), then
+//     O_t += P_t V with P_t read from TMEM and V as an MN-major smem operand.
+//   * warps 2-5 / 6-9: softmax of tile 0 / 1, one thread per row: load the
+//     S row from TMEM, causal mask j <= start_pos + position, running max
+//     (rescaling O in TMEM only when the max grows by more than 2^8),
+//     p = 2^(s*log2e/sqrt(D) - m) on the MUFU unit, P written back to TMEM as
+//     bf16 over its own S columns; finally O / l stored as bf16.
+// Every wait is bounded; on expiry the kernel records a status code, drains,
+// frees TMEM and returns.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "kernels.h"
+#include "ptx.cuh"
 #include "tc_kernels.h"
 
 namespace llama {
+namespace {
+
+constexpr int ATT_THREADS = 320;
+constexpr int KV_TILE = 128;
+constexpr int KV_STAGES = 2;
+constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: rescale O when the running max grows by > 2^8
+
+template <int D>
+struct AttnLayout {
+  static constexpr int ATOM = 128 * 128;         // one 64-column (128-byte) swizzle atom of 128 rows
+  static constexpr int Q_TILE = (D / 64) * ATOM;  // 128 rows x D
+  static constexpr int KV_BYTES = (D / 64) * ATOM;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = 2 * Q_TILE;
+  static constexpr int OFF_V = OFF_K + KV_STAGES * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_V + KV_STAGES * KV_BYTES;
+  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done[2], fin
+  static constexpr int NBAR = 1 + 4 * KV_STAGES + 6 + 1;
+  // At least 116 KB so that a second CTA never shares the SM (both would need all 512 TMEM columns).
+  static constexpr int BYTES_MIN = 1024 + OFF_BAR + NBAR * 8 + 16;
+  static constexpr int BYTES = BYTES_MIN > 116 * 1024 ? BYTES_MIN : 116 * 1024;
+  static constexpr uint32_t TMEM_COLS = 512;  // S0, S1 (128 each), O0, O1 (D each)
+};
+
+struct AttnArgs {
+  bf16 *o;
+  int B, S, start_pos, H, G, r, Mq, kv_len, nqb;
+  float scale_log2;
+  int *status;
+};
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+template <int D>
+__global__ void __launch_bounds__(ATT_THREADS, 1)
+    attn_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, AttnArgs a) {
+  using L = AttnLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + L::NBAR);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const uint32_t s0 = ptx::smem_u32(smem);
+  const uint32_t bar0 = ptx::smem_u32(bars);
+  const uint32_t q_full = bar0;
+  auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto k_empty = [&](int s) { return bar0 + 8u * (1 + KV_STAGES + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * KV_STAGES + s); };
+  auto v_empty = [&](int s) { return bar0 + 8u * (1 + 3 * KV_STAGES + s); };
+  auto s_full = [&](int t) { return bar0 + 8u * (1 + 4 * KV_STAGES + t); };
+  auto p_full = [&](int t) { return bar0 + 8u * (3 + 4 * KV_STAGES + t); };
+  auto o_done = [&](int t) { return bar0 + 8u * (5 + 4 * KV_STAGES + t); };
+  const uint32_t fin = bar0 + 8u * (7 + 4 * KV_STAGES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bg_count = a.B * a.G;
+  const int qb = a.nqb - 1 - (int)(blockIdx.x / bg_count);  // longest query blocks first
+  const int bg = (int)(blockIdx.x % bg_count);
+  const int b = bg / a.G, g = bg % a.G;
+  const int q0 = qb * 2 * a.Mq;
+  const int kv_need = min(a.start_pos + q0 + 2 * a.Mq, a.kv_len);
+  const int n_kv = (kv_need + KV_TILE - 1) / KV_TILE;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(q_full, 1);
+    for (int s = 0; s < KV_STAGES; ++s) {
+      ptx::mbar_init(k_full(s), 1);
+      ptx::mbar_init(k_empty(s), 1);
+      ptx::mbar_init(v_full(s), 1);
+      ptx::mbar_init(v_empty(s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(s_full(t), 1);
+      ptx::mbar_init(p_full(t), 128);
+      ptx::mbar_init(o_done(t), 1);
+    }
+    ptx::mbar_init(fin, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  // Query-head slots beyond r (r not a power of two) are never loaded: zero them.
+  if (warp >= 2 && a.r * a.Mq < 128) {
+    const int first = a.r * a.Mq;
+    for (int t = 0; t < 2; ++t)
+      for (int at = 0; at < D / 64; ++at) {
+        uint4 *p = reinterpret_cast<uint4 *>(smem + L::OFF_Q + t * L::Q_TILE + at * L::ATOM + first * 128);
+        const int n16 = (128 - first) * 8;
+        for (int i = threadIdx.x - 64; i < n16; i += ATT_THREADS - 64) p[i] = make_uint4(0, 0, 0, 0);
+      }
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), L::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tmQ);
+      ptx::tma_prefetch_desc(&tmK);
+      ptx::tma_prefetch_desc(&tmV);
+      const uint32_t qbytes = 2u * a.r * (D / 64) * a.Mq * 128u;
+      ptx::mbar_arrive_expect_tx(q_full, qbytes);
+      for (int t = 0; t < 2; ++t)
+        for (int hh = 0; hh < a.r; ++hh)
+          for (int at = 0; at < D / 64; ++at)
+            ptx::tma_load_4d(s0 + L::OFF_Q + t * L::Q_TILE + at * L::ATOM + hh * a.Mq * 128, &tmQ, at * 64,
+                             g * a.r + hh, q0 + t * a.Mq, b, q_full);
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j % KV_STAGES;
+        const uint32_t ph = (j / KV_STAGES) & 1;
+        if (!ptx::mbar_wait(k_empty(st), ph ^ 1, abort_flag, a.status, DEV_TIMEOUT_PRODUCER)) break;
+        ptx::mbar_arrive_expect_tx(k_full(st), L::KV_BYTES);
+        for (int at = 0; at < D / 64; ++at)
+          ptx::tma_load_4d(s0 + L::OFF_K + st * L::KV_BYTES + at * L::ATOM, &tmK, at * 64, j * KV_TILE, g, b,
+                           k_full(st));
+        if (!ptx::mbar_wait(v_empty(st), ph ^ 1, abort_flag, a.status, DEV_TIMEOUT_PRODUCER)) {
+          issued = 2 * j + 1;
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(v_full(st), L::KV_BYTES);
+        for (int at = 0; at < D / 64; ++at)
+          ptx::tma_load_4d(s0 + L::OFF_V + st * L::KV_BYTES + at * L::ATOM, &tmV, at * 64, j * KV_TILE, g, b,
+                           v_full(st));
+        issued = 2 * j + 2;
+      }
+      // Drain: every issued copy must land before the CTA exits.
+      int dummy = 0;
+      ptx::mbar_wait(q_full, 0, &dummy, a.status, DEV_TIMEOUT_PRODUCER);
+      for (int j = max(0, issued / 2 - KV_STAGES); j < (issued + 1) / 2; ++j) {
+        const int st = j % KV_STAGES;
+        const uint32_t ph = (j / KV_STAGES) & 1;
+        ptx::mbar_wait(k_full(st), ph, &dummy, a.status, DEV_TIMEOUT_PRODUCER);
+        if (2 * j + 1 < issued) ptx::mbar_wait(v_full(st), ph, &dummy, a.status, DEV_TIMEOUT_PRODUCER);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, KV_TILE, false);
+      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, true);
+      bool ok = ptx::mbar_wait(q_full, 0, abort_flag, a.status, DEV_TIMEOUT_MMA);
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int st = j % KV_STAGES;
+        const uint32_t ph = (j / KV_STAGES) & 1;
+        if (!ptx::mbar_wait(k_full(st), ph, abort_flag, a.status, DEV_TIMEOUT_MMA)) break;
+        ptx::tc_fence_after();
+        const uint32_t kb = s0 + L::OFF_K + st * L::KV_BYTES;
+        for (int t = 0; t < 2; ++t) {
+          const uint32_t qbase = s0 + L::OFF_Q + t * L::Q_TILE;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * L::ATOM + (kk % 4) * 32;
+            ptx::mma_bf16_ss(tmem + t * 128, ptx::smem_desc_sw128(qbase + off), ptx::smem_desc_sw128(kb + off),
+                             idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(s_full(t));
+        }
+        ptx::mma_commit(k_empty(st));
+        if (!ptx::mbar_wait(v_full(st), ph, abort_flag, a.status, DEV_TIMEOUT_MMA)) break;
+        const uint32_t vb = s0 + L::OFF_V + st * L::KV_BYTES;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!ptx::mbar_wait(p_full(t), j & 1, abort_flag, a.status, DEV_TIMEOUT_MMA)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < KV_TILE / 16; ++kk) {
+            // 16 keys = two 8-row groups of the V tile; V rows hold 64 consecutive d values.
+            const uint64_t bdesc = ptx::smem_desc_sw128_mn(vb + kk * 16 * 128, L::ATOM, 1024);
+            ptx::mma_bf16_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, bdesc, idesc_pv,
+                             (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(o_done(t));
+        }
+        ptx::mma_commit(v_empty(st));
+      }
+      ptx::mma_commit(fin);
+      int dummy = 0;
+      ptx::mbar_wait(fin, 0, &dummy, a.status, DEV_TIMEOUT_MMA);
+    }
+  } else {
+    // ---------------------------------------------------------- softmax ---
+    const int t = (warp - 2) / 4;
+    const int qq = warp & 3;
+    const int row = qq * 32 + lane;
+    const int hh = row / a.Mq, i = row % a.Mq;
+    const int rel = q0 + t * a.Mq + i;
+    const bool valid = hh < a.r && rel < a.S;
+    const int pos = a.start_pos + rel;
+    const uint32_t lane_base = tmem + ((uint32_t)(qq * 32) << 16);
+    const uint32_t s_col = lane_base + t * 128;
+    const uint32_t o_col = lane_base + 256 + t * D;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      ok = ptx::mbar_wait(s_full(t), j & 1, abort_flag, a.status, DEV_TIMEOUT_ATTN);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      float s[KV_TILE];
+#pragma unroll
+      for (int c = 0; c < KV_TILE; c += 32) ptx::tmem_ld32(s_col + c, *reinterpret_cast<float(*)[32]>(s + c));
+      ptx::tmem_ld_wait();
+      const int key0 = j * KV_TILE;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < KV_TILE; ++k) {
+        if (key0 + k > pos) s[k] = -INFINITY;
+        mx = fmaxf(mx, s[k]);
+      }
+      const float m_tile = mx * a.scale_log2;
+      const bool need = m_tile > m_run + RESCALE_THRESHOLD;
+      float alpha = 1.f;
+      if (need) {
+        alpha = ptx::ex2_approx(m_run - m_tile);
+        m_run = m_tile;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        ok = ptx::mbar_wait(o_done(t), (j - 1) & 1, abort_flag, a.status, DEV_TIMEOUT_ATTN);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D; c += 16) {
+          float ov[16];
+          ptx::tmem_ld16(o_col + c, ov);
+          ptx::tmem_ld_wait();
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(ov[e] * alpha);
+          ptx::tmem_st16(o_col + c, w);
+        }
+      }
+      l_run *= alpha;
+      uint32_t pk[KV_TILE / 2];
+#pragma unroll
+      for (int k = 0; k < KV_TILE; k += 2) {
+        const float p0 = ptx::ex2_approx(fmaf(s[k], a.scale_log2, -m_run));
+        const float p1 = ptx::ex2_approx(fmaf(s[k + 1], a.scale_log2, -m_run));
+        l_run += p0 + p1;
+        pk[k / 2] = pack2(p0, p1);
+      }
+#pragma unroll
+      for (int c = 0; c < KV_TILE / 2; c += 16) ptx::tmem_st16(s_col + c, *reinterpret_cast<uint32_t(*)[16]>(pk + c));
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(p_full(t));
+    }
+    if (ok && n_kv > 0) {
+      ok = ptx::mbar_wait(o_done(t), (n_kv - 1) & 1, abort_flag, a.status, DEV_TIMEOUT_ATTN);
+      if (__all_sync(0xffffffffu, ok)) {
+        ptx::tc_fence_after();
+        const float inv = 1.f / l_run;
+        bf16 *dst = a.o + (((size_t)b * a.S + rel) * a.H + g * a.r + hh) * D;
+#pragma unroll
+        for (int c = 0; c < D; c += 16) {
+          float ov[16];
+          ptx::tmem_ld16(o_col + c, ov);
+          ptx::tmem_ld_wait();
+          if (valid) {
+            uint4 w0 = make_uint4(pack2(ov[0] * inv, ov[1] * inv), pack2(ov[2] * inv, ov[3] * inv),
+                                  pack2(ov[4] * inv, ov[5] * inv), pack2(ov[6] * inv, ov[7] * inv));
+            uint4 w1 = make_uint4(pack2(ov[8] * inv, ov[9] * inv), pack2(ov[10] * inv, ov[11] * inv),
+                                  pack2(ov[12] * inv, ov[13] * inv), pack2(ov[14] * inv, ov[15] * inv));
+            *reinterpret_cast<uint4 *>(dst + c) = w0;
+            *reinterpret_cast<uint4 *>(dst + c + 8) = w1;
+          }
+        }
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// 4-D bf16 map, dims/strides innermost first (strides in bytes for dims 1..3), box {64, b1, b2, 1}.
+bool make_map_4d(CUtensorMap *map, const void *ptr, const uint64_t dims[4], const uint64_t strides[3], uint32_t b1,
+                 uint32_t b2) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t gdim[4] = {dims[0], dims[1], dims[2], dims[3]};
+  cuuint64_t gstride[3] = {strides[0], strides[1], strides[2]};
+  cuuint32_t box[4] = {64, b1, b2, 1};
+  cuuint32_t estride[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), gdim, gstride, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_prefill(const bf16 *q, const bf16 *kc, const bf16 *vc, bf16 *o, int B, int S, int start_pos,
+                           int H, int G, int cache_seq, int *status, cudaStream_t st) {
+  using L = AttnLayout<D>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const int r = H / G;
+  int rp = 1;
+  while (rp < r) rp *= 2;
+  const int Mq = 128 / rp;
+  const int kv_len = start_pos + S;
+  CUtensorMap mq, mk, mv;
+  const uint64_t qd[4] = {(uint64_t)D, (uint64_t)H, (uint64_t)S, (uint64_t)B};
+  const uint64_t qs[3] = {(uint64_t)D * 2, (uint64_t)H * D * 2, (uint64_t)S * H * D * 2};
+  const uint64_t kd[4] = {(uint64_t)D, (uint64_t)kv_len, (uint64_t)G, (uint64_t)B};
+  const uint64_t ks[3] = {(uint64_t)D * 2, (uint64_t)cache_seq * D * 2, (uint64_t)G * cache_seq * D * 2};
+  if (!make_map_4d(&mq, q, qd, qs, 1, Mq) || !make_map_4d(&mk, kc, kd, ks, KV_TILE, 1) ||
+      !make_map_4d(&mv, vc, kd, ks, KV_TILE, 1))
+    return cudaErrorInvalidValue;
+  AttnArgs args;
+  args.o = o;
+  args.B = B;
+  args.S = S;
+  args.start_pos = start_pos;
+  args.H = H;
+  args.G = G;
+  args.r = r;
+  args.Mq = Mq;
+  args.kv_len = kv_len;
+  args.nqb = (S + 2 * Mq - 1) / (2 * Mq);
+  args.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
+  args.status = status;
+  const unsigned grid = (unsigned)(B * G * args.nqb);
+  attn_prefill_kernel<D><<<grid, ATT_THREADS, L::BYTES, st>>>(mq, mk, mv, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
 
 size_t attn_decode_scratch_bytes(int max_tokens, int H, int D, int max_seq) {
   (void)max_tokens;
@@ -16,7 +405,12 @@ cudaError_t launch_attention(const bf16 *q, const bf16 *kc, const bf16 *vc, bf16
                              int H, int G, int D, int cache_seq, const AttnScratch &scratch, int *status,
                              cudaStream_t st) {
   (void)scratch;
-  (void)status;
+  const int r = H / G;
+  const bool tc_ok = (D == 64 || D == 128) && r <= 8 && S > 1;
+  if (tc_ok) {
+    if (D == 128) return launch_prefill<128>(q, kc, vc, o, B, S, start_pos, H, G, cache_seq, status, st);
+    return launch_prefill<64>(q, kc, vc, o, B, S, start_pos, H, G, cache_seq, status, st);
+  }
   return launch_attention_simt<bf16>(q, kc, vc, o, B, S, start_pos, H, G, D, cache_seq, st);
 }
 

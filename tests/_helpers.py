@@ -58,6 +58,28 @@ def assert_parity(got, ref, dtype: str, what: str):
     return fro, mx
 
 
+def bf16_round(a: np.ndarray) -> np.ndarray:
+    """fp64 -> nearest bf16 (via fp32) -> fp64."""
+    return synth.as_f64(synth.f32_to_bf16_bits(np.asarray(a, dtype=np.float32)))
+
+
+def assert_branch_parity(y_got, y_ref, x, what):
+    """Parity of the summed branch outputs y - x of a bf16 block.
+
+    y is stored in bf16, so (y - x) carries y's own output rounding (and that of
+    the bf16 h stored between the branches) on top of the branch arithmetic.
+    Bar: ||err|| <= 5e-3 ||y_ref - x|| + 2 ||bf16(y_ref) - y_ref||, i.e. the bf16
+    relative-Frobenius bar on the branches plus twice the unavoidable rounding
+    of one bf16 store of y (measured on the reference itself)."""
+    y_got = np.asarray(y_got, dtype=np.float64)
+    ref_b = np.asarray(y_ref, dtype=np.float64) - x
+    err = float(np.linalg.norm((y_got - x) - ref_b))
+    round_err = float(np.linalg.norm(bf16_round(y_ref) - y_ref))
+    bar = BF16_FRO_REL * float(np.linalg.norm(ref_b)) + 2.0 * round_err
+    assert err <= bar, f"{what}: ||err|| {err:.4e} > bar {bar:.4e} (rounding part {2 * round_err:.4e})"
+    return err, bar
+
+
 def llama_dtype(shape):
     import decoder_block_gb300 as lb
     return lb.LLAMA_BF16 if shape["dtype"] == "bf16" else lb.LLAMA_F32

@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 import synth
-from _helpers import GpuBlock, assert_parity, f64_weights, to_dev, to_f64, torch
+from _helpers import GpuBlock, assert_branch_parity, assert_parity, f64_weights, to_dev, to_f64, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -43,7 +43,10 @@ def _check_full(shape, B, S, start_pos, L, fill_upto=0, tag="x"):
                                       synth.as_f64(vc))
     dt = shape["dtype"]
     assert_parity(y, yr, dt, "y")
-    assert_parity(y - synth.as_f64(x), yr - synth.as_f64(x), dt, "y - x (both branch outputs)")
+    if dt == "bf16":
+        assert_branch_parity(y, yr, synth.as_f64(x), "y - x (both branch outputs)")
+    else:
+        assert_parity(y - synth.as_f64(x), yr - synth.as_f64(x), dt, "y - x (both branch outputs)")
     sl = (slice(0, B), slice(None), slice(start_pos, start_pos + S))
     assert_parity(kg[sl], kr[sl], dt, "K cache slice")
     assert_parity(vg[sl], vr[sl], dt, "V cache slice")
@@ -96,7 +99,7 @@ def test_llama3_8b_prefill_full_size_sampled(name):
     ys = np.stack([y[b, t] for b, t in rows])
     xs = np.stack([synth.as_f64(x)[b, t] for b, t in rows])
     assert_parity(ys, yr, "bf16", "y (sampled rows)")
-    assert_parity(ys - xs, yr - xs, "bf16", "y - x (sampled rows)")
+    assert_branch_parity(ys, yr, xs, "y - x (sampled rows)")
     assert_parity(kg[:, :, :S], kr, "bf16", "K cache (all written positions)")
     assert_parity(vg[:, :, :S], vr, "bf16", "V cache (all written positions)")
 
@@ -112,7 +115,7 @@ def test_llama3_8b_decode_full_size():
     yr, kr, vr = oracle.block_forward_rows(s, f64_weights(w), synth.as_f64(x), sp, synth.as_f64(kc),
                                            synth.as_f64(vc), rows)
     assert_parity(y[:, 0], yr, "bf16", "y")
-    assert_parity(y[:, 0] - synth.as_f64(x)[:, 0], yr - synth.as_f64(x)[:, 0], "bf16", "y - x")
+    assert_branch_parity(y[:, 0], yr, synth.as_f64(x)[:, 0], "y - x")
     assert_parity(kg[:, :, sp:sp + 1], kr, "bf16", "K cache slice")
     assert_parity(vg[:, :, sp:sp + 1], vr, "bf16", "V cache slice")
     np.testing.assert_array_equal(kg[:, :, :sp], synth.as_f64(kc)[:, :, :sp])
