@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 Llama decoder block (C ABI, sm_103a kernels).
+
+Workload (one step = one llama_block_forward): the Llama-3-8B-shaped block
+prefill, B=1, S=8192, d_model=4096, 32 query / 8 KV heads of width 128,
+d_ff=14336, rope_theta=5e5, bf16 with fp32 accumulation, causal, start_pos=0,
+synthetic seeded inputs (x ~ N(0,1), weights ~ N(0,0.02), gains 1+N(0,0.1)).
+
+Prints one JSON line (rank 0).  value = whole-job tokens/s with inputs resident
+in HBM; e2e = the same through llama_block_forward_host with pinned host
+buffers (copies inside the timed region); roofline = the gate/up + SwiGLU GEMM
+(largest share of the step) timed with CUDA events inside the timed region;
+cpu_baseline = the fp64 oracle on the host cores on a bounded sample of the
+same workload.  `--impl reference` times that oracle as the reference arm.
+
+Multi-GPU (torchrun): replicas only -- every rank runs its own block on its own
+sequence; no collective on the data path; barrier + max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decoder-block tokens/s (prefill) & decode µs/step; % of bf16 TC / HBM roofline"
+WORKLOAD = "llama3_8b_block_prefill_b1s8192"
+SHAPE = dict(d_model=4096, n_heads=32, n_kv_heads=8, d_ff=14336, norm_eps=1e-5, rope_theta=5e5, dtype="bf16",
+             B=1, S=8192, start_pos=0, max_seq_len=8192)
+DECODE = dict(SHAPE, B=64, S=1, start_pos=4095, max_seq_len=4096)
+KERNELS_PER_PREFILL_FORWARD = 8  # rmsnorm, QKV GEMM, RoPE+KV, attention, O GEMM, rmsnorm, gate/up GEMM, down GEMM
+KERNELS_PER_DECODE_FORWARD = 9   # the same plus the split-KV combine
+
+
+def block_flops(s):
+    d, H, G, F = s["d_model"], s["n_heads"], s["n_kv_heads"], s["d_ff"]
+    D = d // H
+    T = s["B"] * s["S"]
+    linear = 2.0 * T * (d * (H + 2 * G) * D + H * D * d + d * 2 * F + F * d)
+    pairs = s["B"] * sum(s["start_pos"] + i + 1 for i in range(s["S"]))  # causal (query, key) pairs
+    attn = 4.0 * D * H * pairs
+    return linear, attn
+
+
+def gate_up_flops(s):
+    return 2.0 * s["B"] * s["S"] * s["d_model"] * 2 * s["d_ff"]
+
+
+def decode_attention_bytes(s):
+    D = s["d_model"] // s["n_heads"]
+    kv = 2.0 * s["B"] * s["n_kv_heads"] * (s["start_pos"] + 1) * D * 2
+    qo = 2.0 * s["B"] * s["n_heads"] * D * 2
+    return kv + qo
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            m = json.load(f)
+        return m, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_traffic(name):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        table = json.load(f)
+    ent = table.get(name)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, ent["source"])
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()
+    return ent["dram_bytes_per_launch"] if digest == ent["source_sha256"] else None
+
+
+# ----------------------------------------------------------- clock sampler ---
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names[1:], parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ cpu oracle ---
+
+def oracle_sample(tokens: int, seed_tag: str = "bench"):
+    """Inputs of a bounded sample of the workload: same weights, first `tokens` positions."""
+    import synth
+    s = dict(SHAPE, S=tokens, max_seq_len=tokens)
+    w = synth.block_weights(SHAPE)
+    wf = {k: synth.as_f64(v) for k, v in w.items()}
+    x = synth.as_f64(synth.block_activations(s, tag=seed_tag, B=1, S=tokens))
+    kc, vc = synth.kv_cache(s, max_batch=1, max_seq_len=tokens)
+    return s, wf, x, synth.as_f64(kc), synth.as_f64(vc)
+
+
+def time_oracle(tokens: int, reps: int = 1):
+    import oracle
+    s, wf, x, kc, vc = oracle_sample(tokens)
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.block_forward(s, wf, x, 0, kc, vc)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def cpu_info():
+    return {"cores": os.cpu_count()}
+
+
+# ------------------------------------------------------------------ main ---
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    tokens = args.ref_tokens
+    times = time_oracle(tokens, reps=args.warmup + args.steps)
+    timed = times[args.warmup:]
+    total = sum(timed)
+    value = tokens * len(timed) / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(timed),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": SHAPE["B"], "S": SHAPE["S"], "sample_tokens_per_step": tokens,
+                   "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"first {tokens} positions of the B=1 S=8192 prefill per step, same block weights"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-tokens", type=int, default=2048, help="oracle sample size for cpu_baseline")
+    ap.add_argument("--ref-tokens", type=int, default=512, help="oracle sample per step of --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--seq", type=int, default=8192,
+                    help="prefill length S (default 8192; smaller values are for profiler captures)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    global SHAPE, WORKLOAD
+    if args.seq != SHAPE["S"]:
+        SHAPE = dict(SHAPE, S=args.seq, max_seq_len=args.seq)
+        WORKLOAD = f"llama3_8b_block_prefill_b1s{args.seq}"
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import numpy as np
+    import torch
+
+    import decoder_block_gb300 as lb
+    import synth
+
+    lb.load()  # raises when the library has not been built: there is no fallback
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    # ---- inputs (seeded synthetic, the same recipe as the parity tests) ----
+    w_np = synth.block_weights(SHAPE)
+    w = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(dev) for k, v in w_np.items()}
+    B, S, d = SHAPE["B"], SHAPE["S"], SHAPE["d_model"]
+    G, D = SHAPE["n_kv_heads"], d // SHAPE["n_heads"]
+    x_np = synth.block_activations(SHAPE)
+    x = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).to(dev)
+    y = torch.empty_like(x)
+    kc = torch.zeros((B, G, SHAPE["max_seq_len"], D), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    cfg = lb.make_config(d, SHAPE["n_heads"], G, SHAPE["d_ff"], SHAPE["max_seq_len"], SHAPE["norm_eps"],
+                         SHAPE["rope_theta"], lb.LLAMA_BF16)
+    st, blk = lb.llama_block_create(cfg, lb.make_weights(w), B * S)
+    lb.check(st, "llama_block_create")
+    kv = lb.make_kv_cache(kc, vc, B, SHAPE["max_seq_len"])
+
+    def step():
+        lb.check(lb.llama_block_forward(blk, x, y, B, S, 0, kv, stream), "llama_block_forward")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    lb.check(lb.llama_block_device_status(blk), "device status")
+
+    # ---- timed region: K forwards, inputs resident in HBM ----
+    gpu_index = local
+    try:
+        gpu_index = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    lb.check(lb.llama_block_profile_enable(blk, args.steps), "profile enable")
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    elapsed_ms = ev0.elapsed_time(ev1)
+    st, launches, total_ms = lb.llama_block_profile_read(blk)
+    lb.check(st, "profile read")
+    lb.llama_block_profile_disable(blk)
+    clock_info = clocks.stop()
+    lb.check(lb.llama_block_device_status(blk), "device status")
+    max_ms = max_over_ranks(elapsed_ms, world)
+    ms_per_step = max_ms / args.steps
+    value = world * B * S * args.steps / (max_ms / 1e3)
+
+    # ---- end to end: host buffers through llama_block_forward_host ----
+    xh = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    for _ in range(2):
+        lb.check(lb.llama_block_forward_host(blk, xh, yh, B, S, 0, kv, stream), "forward_host")
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        lb.check(lb.llama_block_forward_host(blk, xh, yh, B, S, 0, kv, stream), "forward_host")
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    e2e_value = world * B * S * args.steps / (e2e_ms / 1e3)
+    io_bytes = B * S * d * 2
+
+    # ---- roofline of the dominant kernel (gate/up + SwiGLU GEMM) ----
+    peaks, peak_kind = measured_peaks()
+    gu = 6
+    gu_ms = total_ms[gu] / max(launches[gu], 1)
+    gu_tflops = gate_up_flops(SHAPE) / (gu_ms / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    traffic = kernel_traffic("gate_up_swiglu")
+    step_ms = {lb.llama_profile_step_name(i): total_ms[i] / max(launches[i], 1) for i in range(len(launches))}
+    lin, att = block_flops(SHAPE)
+
+    # ---- secondary: decode step (B=64 at start_pos 4095 over a filled cache) ----
+    decode = None
+    if not args.no_decode:
+        decode = bench_decode(lb, torch, w, dev, stream, args, peaks)
+
+    lb.llama_block_destroy(blk)
+    del kc, vc
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "S": S, "d_model": d, "n_heads": SHAPE["n_heads"],
+                   "n_kv_heads": G, "d_ff": SHAPE["d_ff"], "start_pos": 0, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (436 MB of weights read per step, plus activations and KV)",
+                   "block_tflops": (lin + att) / (ms_per_step / 1e3) / 1e12,
+                   "block_frac_of_bf16_peak": (lin + att) / (ms_per_step / 1e3) / 1e12 / peak},
+        "roofline": {"kernel": "gate_up_swiglu (tcgen05 GEMM, SiLU*up epilogue)", "bound": "tensor",
+                     "achieved": gu_tflops, "peak": peak, "unit": "TFLOP/s", "frac": gu_tflops / peak,
+                     "traffic": traffic, "peak_source": f"{peak_kind} bf16_tflops_sustained"},
+        "step_ms": step_ms,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
+                "d2h_bytes_per_step": io_bytes},
+        "gpu_launches": KERNELS_PER_PREFILL_FORWARD * args.steps,
+        "clocks": clock_info,
+    }
+    if decode is not None:
+        line["decode"] = decode
+    if rank == 0 and not args.no_cpu_baseline:
+        times = time_oracle(args.cpu_tokens)
+        line["cpu_baseline"] = {"value": args.cpu_tokens / times[0], "unit": "tokens/s", "cores": os.cpu_count(),
+                                "kind": "oracle",
+                                "sample": f"fp64 numpy oracle, first {args.cpu_tokens} positions of the B=1 S=8192 "
+                                          f"prefill with the same block weights ({times[0]:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def bench_decode(lb, torch, w, dev, stream, args, peaks):
+    s = DECODE
+    B, d, G = s["B"], s["d_model"], s["n_kv_heads"]
+    D = d // s["n_heads"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    kc = torch.randn((B, G, s["max_seq_len"], D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    vc = torch.randn((B, G, s["max_seq_len"], D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    x = torch.randn((B, 1, d), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    y = torch.empty_like(x)
+    cfg = lb.make_config(d, s["n_heads"], G, s["d_ff"], s["max_seq_len"], s["norm_eps"], s["rope_theta"],
+                         lb.LLAMA_BF16)
+    st, blk = lb.llama_block_create(cfg, lb.make_weights(w), B)
+    lb.check(st, "llama_block_create (decode)")
+    kv = lb.make_kv_cache(kc, vc, B, s["max_seq_len"])
+    sp = s["start_pos"]
+    for _ in range(args.warmup):
+        lb.check(lb.llama_block_forward(blk, x, y, B, 1, sp, kv, stream))
+    torch.cuda.synchronize()
+    steps = max(args.steps, 20)
+    lb.check(lb.llama_block_profile_enable(blk, steps))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        lb.check(lb.llama_block_forward(blk, x, y, B, 1, sp, kv, stream))
+    e1.record(stream)
+    torch.cuda.synchronize()
+    st, launches, total_ms = lb.llama_block_profile_read(blk)
+    lb.llama_block_profile_disable(blk)
+    lb.check(lb.llama_block_device_status(blk))
+    lb.llama_block_destroy(blk)
+    us = 1e3 * e0.elapsed_time(e1) / steps
+    att_ms = total_ms[3] / max(launches[3], 1)
+    gbs = decode_attention_bytes(s) / (att_ms / 1e3) / 1e9
+    hbm = float(peaks["hbm_gbs"])
+    weights_bytes = 2.0 * (d * (s["n_heads"] + 2 * G) * D + s["n_heads"] * D * d + 3 * d * s["d_ff"])
+    step_bytes = weights_bytes + decode_attention_bytes(s)
+    return {"workload": "llama3_8b_block_decode_b64_pos4095", "us_per_step": us,
+            "step_hbm_gbs": step_bytes / (us / 1e6) / 1e9, "step_hbm_frac": step_bytes / (us / 1e6) / 1e9 / hbm,
+            "attention_us": 1e3 * att_ms, "attention_gbs": gbs, "attention_hbm_frac": gbs / hbm,
+            "hbm_peak_gbs": hbm, "gpu_launches": KERNELS_PER_DECODE_FORWARD * steps,
+            "step_us": {lb.llama_profile_step_name(i): 1e3 * total_ms[i] / max(launches[i], 1)
+                        for i in range(len(launches))}}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

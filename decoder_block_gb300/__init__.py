@@ -83,13 +83,18 @@ def load() -> ctypes.CDLL:
         "llama_stack_destroy": (None, [c_void_p]),
         "llama_stack_device_status": (st, [c_void_p]),
         "llama_kv_cache_bytes": (c_size_t, [POINTER(llama_config), c_int32, c_int32]),
+        "llama_block_profile_enable": (st, [c_void_p, c_int32]),
+        "llama_block_profile_disable": (st, [c_void_p]),
+        "llama_block_profile_read": (st, [c_void_p, POINTER(c_int32), POINTER(c_float)]),
+        "llama_profile_step_name": (c_char_p, [c_int32]),
         "llama_ffn_hidden_dim": (c_int32, [c_int32, c_int32, c_float]),
         "llama_status_string": (c_char_p, [c_int32]),
         "llama_op_rmsnorm": (st, [c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_void_p]),
         "llama_op_linear": (st, [c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
                                  c_void_p]),
+        "llama_op_attention_workspace_bytes": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int32, c_int32]),
         "llama_op_attention": (st, [c_int32, c_void_p, POINTER(llama_kv_cache), c_void_p, c_int32, c_int32, c_int32,
-                                    c_int32, c_int32, c_int32, c_void_p]),
+                                    c_int32, c_int32, c_int32, c_void_p, c_size_t, c_void_p]),
         "llama_op_rope_table": (st, [c_void_p, c_int32, c_int32, c_float, c_void_p]),
         "llama_op_rope_kv_write": (st, [c_int32, c_void_p, c_void_p, POINTER(llama_kv_cache), c_void_p, c_int32,
                                         c_int32, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p]),
@@ -178,6 +183,29 @@ def llama_stack_device_status(stk) -> int:
     return load().llama_stack_device_status(stk)
 
 
+LLAMA_PROFILE_STEPS = 8
+
+
+def llama_block_profile_enable(blk, max_forwards) -> int:
+    return load().llama_block_profile_enable(blk, max_forwards)
+
+
+def llama_block_profile_disable(blk) -> int:
+    return load().llama_block_profile_disable(blk)
+
+
+def llama_block_profile_read(blk):
+    """Returns (status, launches[8], total_ms[8])."""
+    n = (c_int32 * LLAMA_PROFILE_STEPS)()
+    ms = (c_float * LLAMA_PROFILE_STEPS)()
+    s = load().llama_block_profile_read(blk, n, ms)
+    return s, list(n), list(ms)
+
+
+def llama_profile_step_name(step) -> str:
+    return load().llama_profile_step_name(step).decode()
+
+
 def llama_kv_cache_bytes(cfg: llama_config, max_batch, max_seq_len) -> int:
     return load().llama_kv_cache_bytes(byref(cfg), max_batch, max_seq_len)
 
@@ -198,8 +226,14 @@ def llama_op_linear(dtype, A, W, R, C, M, N, K, epilogue, stream=None) -> int:
     return load().llama_op_linear(dtype, _p(A), _p(W), _p(R), _p(C), M, N, K, epilogue, _stream(stream))
 
 
-def llama_op_attention(dtype, q, kv: llama_kv_cache, o, B, S, start_pos, H, G, D, stream=None) -> int:
-    return load().llama_op_attention(dtype, _p(q), byref(kv), _p(o), B, S, start_pos, H, G, D, _stream(stream))
+def llama_op_attention_workspace_bytes(dtype, B, S, start_pos, H, D) -> int:
+    return load().llama_op_attention_workspace_bytes(dtype, B, S, start_pos, H, D)
+
+
+def llama_op_attention(dtype, q, kv: llama_kv_cache, o, B, S, start_pos, H, G, D, workspace=None, workspace_bytes=0,
+                       stream=None) -> int:
+    return load().llama_op_attention(dtype, _p(q), byref(kv), _p(o), B, S, start_pos, H, G, D, _p(workspace),
+                                     workspace_bytes, _stream(stream))
 
 
 def llama_op_rope_table(table, max_seq, D, theta, stream=None) -> int:

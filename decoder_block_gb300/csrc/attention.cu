@@ -393,19 +393,12 @@ cudaError_t launch_prefill(const bf16 *q, const bf16 *kc, const bf16 *vc, bf16 *
 
 }  // namespace
 
-size_t attn_decode_scratch_bytes(int max_tokens, int H, int D, int max_seq) {
-  (void)max_tokens;
-  (void)H;
-  (void)D;
-  (void)max_seq;
-  return 16;
-}
-
 cudaError_t launch_attention(const bf16 *q, const bf16 *kc, const bf16 *vc, bf16 *o, int B, int S, int start_pos,
                              int H, int G, int D, int cache_seq, const AttnScratch &scratch, int *status,
                              cudaStream_t st) {
-  (void)scratch;
   const int r = H / G;
+  if (S == 1 && attn_decode_supported(H, G, D))
+    return launch_attn_decode(q, kc, vc, o, B, start_pos, H, G, D, cache_seq, scratch, status, st);
   const bool tc_ok = (D == 64 || D == 128) && r <= 8 && S > 1;
   if (tc_ok) {
     if (D == 128) return launch_prefill<128>(q, kc, vc, o, B, S, start_pos, H, G, cache_seq, status, st);

@@ -69,8 +69,16 @@ llama_status llama_op_linear(int32_t dtype, const void *A, const void *W, const 
       launch_gemm_simt<float>((const float *)A, (const float *)W, nullptr, (const float *)R, C, M, N, K, epilogue, st));
 }
 
+size_t llama_op_attention_workspace_bytes(int32_t dtype, int32_t B, int32_t S, int32_t start_pos, int32_t H,
+                                          int32_t D) {
+  if (dtype != LLAMA_BF16 || S != 1 || B <= 0 || H <= 0 || start_pos < 0 || !head_dim_ok(D)) return 0;
+  if (start_pos + 1 <= 256) return 0;  // a single chunk normalises in place
+  return attn_decode_scratch_bytes(B, H, D, start_pos + 1);
+}
+
 llama_status llama_op_attention(int32_t dtype, const void *q, const llama_kv_cache *kv, void *o, int32_t B,
-                                int32_t S, int32_t start_pos, int32_t H, int32_t G, int32_t D, llama_stream stream) {
+                                int32_t S, int32_t start_pos, int32_t H, int32_t G, int32_t D, void *workspace,
+                                size_t workspace_bytes, llama_stream stream) {
   if (dtype != LLAMA_F32 && dtype != LLAMA_BF16) return LLAMA_ERR_INVALID_ARG;
   if (kv == nullptr || B <= 0 || S <= 0 || start_pos < 0 || H <= 0 || G <= 0 || D <= 0)
     return LLAMA_ERR_INVALID_ARG;
@@ -83,11 +91,17 @@ llama_status llama_op_attention(int32_t dtype, const void *q, const llama_kv_cac
   }
   cudaStream_t st = (cudaStream_t)stream;
   if (dtype == LLAMA_BF16) {
-    AttnScratch none;
-    if ((size_t)B * S * H > 0 && S == 1 && attn_decode_scratch_bytes(B, H, D, start_pos + S) > 16)
-      return LLAMA_ERR_UNSUPPORTED;  // the split-KV decode path needs the block's workspace
+    const size_t need = llama_op_attention_workspace_bytes(dtype, B, S, start_pos, H, D);
+    if (need > 0) {
+      if (workspace_bytes < need) return LLAMA_ERR_RANGE;
+      llama_status s = check(workspace);
+      if (s != LLAMA_OK) return s;
+    }
+    AttnScratch ws;
+    ws.partial = need > 0 ? workspace : nullptr;
+    ws.bytes = need > 0 ? workspace_bytes : 0;
     return status_of(launch_attention((const bf16 *)q, (const bf16 *)kv->k, (const bf16 *)kv->v, (bf16 *)o, B, S,
-                                      start_pos, H, G, D, kv->max_seq_len, none, nullptr, st));
+                                      start_pos, H, G, D, kv->max_seq_len, ws, nullptr, st));
   }
   return status_of(launch_attention_simt<float>((const float *)q, (const float *)kv->k, (const float *)kv->v,
                                                 (float *)o, B, S, start_pos, H, G, D, kv->max_seq_len, st));

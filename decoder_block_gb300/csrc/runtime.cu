@@ -69,6 +69,28 @@ struct Workspace {
   AttnScratch attn;                      // split-KV partials of the decode path
 };
 
+// Optional per-step event timing of block forwards (llama_block_profile_*).
+struct Profiler {
+  bool on = false;
+  int max_forwards = 0, used = 0;
+  std::vector<cudaEvent_t> ev;  // [max_forwards][LLAMA_PROFILE_STEPS][2]
+  cudaEvent_t *slot = nullptr;  // events of the forward being enqueued (null: not recording)
+  void begin_forward() {
+    slot = (on && used < max_forwards) ? &ev[(size_t)used * LLAMA_PROFILE_STEPS * 2] : nullptr;
+    if (slot != nullptr) ++used;
+  }
+  void mark(int step, int edge, cudaStream_t st) {
+    if (slot != nullptr) cudaEventRecord(slot[step * 2 + edge], st);
+  }
+  void release() {
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    ev.clear();
+    on = false;
+    used = max_forwards = 0;
+    slot = nullptr;
+  }
+};
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool is_device_ptr(const void *p) {
@@ -210,28 +232,47 @@ llama_status forward_simt(const Dims &dm, const Weights &w, const Workspace &ws,
 }
 
 llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, const float2 *rope, const bf16 *x,
-                        bf16 *y, int B, int S, int start_pos, const llama_kv_cache *kv, int *status,
+                        bf16 *y, int B, int S, int start_pos, const llama_kv_cache *kv, int *status, Profiler *prof,
                         cudaStream_t st) {
   const int M = B * S;
   bf16 *xn = (bf16 *)ws.xn, *qkv = (bf16 *)ws.qkv, *q = (bf16 *)ws.q, *o = (bf16 *)ws.o, *h = (bf16 *)ws.h,
        *act = (bf16 *)ws.act, *hn = (bf16 *)ws.hn;
   bf16 *kc = (bf16 *)kv->k, *vc = (bf16 *)kv->v;
+  Profiler none;
+  Profiler &pf = prof != nullptr ? *prof : none;
+  pf.begin_forward();
+  pf.mark(0, 0, st);
   LAUNCH(launch_rmsnorm<bf16>(x, (const bf16 *)w.attn_norm, xn, M, dm.d, dm.eps, st));
+  pf.mark(0, 1, st);
+  pf.mark(1, 0, st);
   LAUNCH(launch_gemm_tc(xn, (const bf16 *)w.wqkv, nullptr, qkv, M, dm.QKV, dm.d, EPI_STORE, status, st));
+  pf.mark(1, 1, st);
+  pf.mark(2, 0, st);
   LAUNCH(launch_rope_kv<bf16>(qkv, q, kc, vc, rope, B, S, start_pos, dm.H, dm.G, dm.D, kv->max_seq_len, st));
+  pf.mark(2, 1, st);
+  pf.mark(3, 0, st);
   LAUNCH(launch_attention(q, kc, vc, o, B, S, start_pos, dm.H, dm.G, dm.D, kv->max_seq_len, ws.attn, status, st));
+  pf.mark(3, 1, st);
+  pf.mark(4, 0, st);
   LAUNCH(launch_gemm_tc(o, (const bf16 *)w.wo, x, h, M, dm.d, dm.H * dm.D, EPI_RESIDUAL, status, st));
+  pf.mark(4, 1, st);
+  pf.mark(5, 0, st);
   LAUNCH(launch_rmsnorm<bf16>(h, (const bf16 *)w.ffn_norm, hn, M, dm.d, dm.eps, st));
+  pf.mark(5, 1, st);
+  pf.mark(6, 0, st);
   LAUNCH(launch_gemm_tc(hn, (const bf16 *)w.w_gu, nullptr, act, M, 2 * dm.F, dm.d, EPI_SWIGLU, status, st));
+  pf.mark(6, 1, st);
+  pf.mark(7, 0, st);
   LAUNCH(launch_gemm_tc(act, (const bf16 *)w.w_down, h, y, M, dm.d, dm.F, EPI_RESIDUAL, status, st));
+  pf.mark(7, 1, st);
   return LLAMA_OK;
 }
 
 llama_status forward_any(const Dims &dm, const Weights &w, const Workspace &ws, const float2 *rope, const void *x,
                          void *y, int B, int S, int start_pos, const llama_kv_cache *kv, int *status,
-                         cudaStream_t st) {
+                         cudaStream_t st, Profiler *prof = nullptr) {
   if (dm.dtype == LLAMA_BF16)
-    return forward_tc(dm, w, ws, rope, (const bf16 *)x, (bf16 *)y, B, S, start_pos, kv, status, st);
+    return forward_tc(dm, w, ws, rope, (const bf16 *)x, (bf16 *)y, B, S, start_pos, kv, status, prof, st);
   return forward_simt<float>(dm, w, ws, rope, (const float *)x, (float *)y, B, S, start_pos, kv, st);
 }
 
@@ -271,6 +312,7 @@ struct llama_block {
   Workspace ws;
   float2 *rope = nullptr;
   int *status = nullptr;
+  Profiler prof;
 };
 
 struct llama_stack {
@@ -328,7 +370,7 @@ llama_status llama_block_forward(llama_block *blk, const void *x, void *y, int32
   if (s == LLAMA_OK) s = validate_call(blk->dm, blk->ws.max_tokens, B, S, start_pos, kv);
   if (s != LLAMA_OK) return s;
   return forward_any(blk->dm, blk->w, blk->ws, blk->rope, x, y, B, S, start_pos, kv, blk->status,
-                     (cudaStream_t)stream);
+                     (cudaStream_t)stream, &blk->prof);
 }
 
 llama_status llama_block_forward_host(llama_block *blk, const void *x_host, void *y_host, int32_t B, int32_t S,
@@ -340,7 +382,7 @@ llama_status llama_block_forward_host(llama_block *blk, const void *x_host, void
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemcpyAsync(blk->ws.xin, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return LLAMA_ERR_CUDA;
   s = forward_any(blk->dm, blk->w, blk->ws, blk->rope, blk->ws.xin, blk->ws.yout, B, S, start_pos, kv,
-                  blk->status, st);
+                  blk->status, st, &blk->prof);
   if (s != LLAMA_OK) return s;
   if (cudaMemcpyAsync(y_host, blk->ws.yout, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return LLAMA_ERR_CUDA;
   return LLAMA_OK;
@@ -352,9 +394,64 @@ void llama_block_destroy(llama_block *blk) {
   cudaGetDevice(&prev);
   cudaSetDevice(blk->device);
   cudaDeviceSynchronize();
+  blk->prof.release();
   blk->al.free_all();
   cudaSetDevice(prev);
   delete blk;
+}
+
+llama_status llama_block_profile_enable(llama_block *blk, int32_t max_forwards) {
+  if (blk == nullptr || max_forwards <= 0) return LLAMA_ERR_INVALID_ARG;
+  blk->prof.release();
+  blk->prof.ev.resize((size_t)max_forwards * LLAMA_PROFILE_STEPS * 2);
+  for (cudaEvent_t &e : blk->prof.ev) {
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      e = nullptr;
+      blk->prof.release();
+      return LLAMA_ERR_CUDA;
+    }
+  }
+  blk->prof.max_forwards = max_forwards;
+  blk->prof.used = 0;
+  blk->prof.on = true;
+  return LLAMA_OK;
+}
+
+llama_status llama_block_profile_disable(llama_block *blk) {
+  if (blk == nullptr) return LLAMA_ERR_INVALID_ARG;
+  cudaDeviceSynchronize();
+  blk->prof.release();
+  return LLAMA_OK;
+}
+
+llama_status llama_block_profile_read(llama_block *blk, int32_t *launches, float *total_ms) {
+  if (blk == nullptr || launches == nullptr || total_ms == nullptr) return LLAMA_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return LLAMA_ERR_CUDA;
+  for (int s = 0; s < LLAMA_PROFILE_STEPS; ++s) {
+    launches[s] = 0;
+    total_ms[s] = 0.f;
+  }
+  Profiler &p = blk->prof;
+  for (int f = 0; f < p.used; ++f)
+    for (int s = 0; s < LLAMA_PROFILE_STEPS; ++s) {
+      float ms = 0.f;
+      cudaEvent_t *e = &p.ev[((size_t)f * LLAMA_PROFILE_STEPS + s) * 2];
+      if (cudaEventElapsedTime(&ms, e[0], e[1]) == cudaSuccess) {
+        launches[s] += 1;
+        total_ms[s] += ms;
+      } else {
+        cudaGetLastError();
+      }
+    }
+  p.used = 0;
+  return LLAMA_OK;
+}
+
+const char *llama_profile_step_name(int32_t step) {
+  static const char *names[LLAMA_PROFILE_STEPS] = {"attention_norm", "qkv_projection", "rope_kv_write",
+                                                   "attention", "o_projection_residual", "ffn_norm",
+                                                   "gate_up_swiglu", "down_projection_residual"};
+  return (step >= 0 && step < LLAMA_PROFILE_STEPS) ? names[step] : "unknown";
 }
 
 llama_status llama_block_device_status(llama_block *blk) {

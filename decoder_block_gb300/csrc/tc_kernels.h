@@ -31,6 +31,12 @@ struct AttnScratch {
 };
 size_t attn_decode_scratch_bytes(int max_tokens, int H, int D, int max_seq);
 
+// Split-KV decode attention (S = 1) -- decode_attn.cu.
+bool attn_decode_supported(int H, int G, int D);
+cudaError_t launch_attn_decode(const bf16 *q, const bf16 *kc, const bf16 *vc, bf16 *o, int B, int start_pos, int H,
+                               int G, int D, int cache_seq, const AttnScratch &scratch, int *status,
+                               cudaStream_t st);
+
 // Causal GQA attention over the bf16 cache; picks the prefill or decode kernel.
 cudaError_t launch_attention(const bf16 *q, const bf16 *kc, const bf16 *vc, bf16 *o, int B, int S, int start_pos,
                              int H, int G, int D, int cache_seq, const AttnScratch &scratch, int *status,

@@ -151,6 +151,20 @@ int32_t llama_ffn_hidden_dim(int32_t d_model, int32_t multiple_of, float ffn_dim
 
 const char *llama_status_string(llama_status s);
 
+/* Per-step timing of llama_block_forward (tracing).  When enabled, every
+ * forward call records a CUDA event pair on its stream around each step's
+ * kernel launch, for up to max_forwards calls (events are created here;
+ * synchronous).  llama_block_profile_read synchronises the device, writes for
+ * each step s in [0, LLAMA_PROFILE_STEPS) the number of launches timed and
+ * their total milliseconds, then clears the record.  Steps: 0 attention_norm,
+ * 1 QKV projection, 2 RoPE + KV write, 3 attention, 4 O projection + residual,
+ * 5 ffn_norm, 6 gate/up + SwiGLU, 7 down projection + residual. */
+#define LLAMA_PROFILE_STEPS 8
+llama_status llama_block_profile_enable(llama_block *blk, int32_t max_forwards);
+llama_status llama_block_profile_disable(llama_block *blk);
+llama_status llama_block_profile_read(llama_block *blk, int32_t *launches, float *total_ms);
+const char *llama_profile_step_name(int32_t step);
+
 /* Read and clear the handle's device status word.  Synchronises the device the
  * handle lives on.  Returns LLAMA_OK when no kernel reported a problem since
  * the last read, LLAMA_ERR_DEVICE_TIMEOUT when a bounded wait ran out,

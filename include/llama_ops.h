@@ -35,9 +35,15 @@ llama_status llama_op_linear(int32_t dtype, const void *A, const void *W, const 
  * · LLaMA", §05 GQA; "Full Llama 3 transformer block", How it works):
  * o[b][s][h] = sum_{j <= start_pos + s} softmax_j(q[b][s][h] . K[b][h / (H/G)][j] / sqrt(D)) V[b][h / (H/G)][j].
  * q, o: [B][S][H][D] (q already rotated); kv->k, kv->v: [max_batch][G][max_seq_len][D].
- * Requirements as for llama_block_forward; D in {16, 32, 64, 128}. */
+ * Requirements as for llama_block_forward; D in {16, 32, 64, 128}.
+ * workspace: caller-owned device scratch of at least
+ * llama_op_attention_workspace_bytes(dtype, B, S, start_pos, H, D) bytes
+ * (the split-KV partials of the decode path); may be NULL when that is 0. */
+size_t llama_op_attention_workspace_bytes(int32_t dtype, int32_t B, int32_t S, int32_t start_pos, int32_t H,
+                                          int32_t D);
 llama_status llama_op_attention(int32_t dtype, const void *q, const llama_kv_cache *kv, void *o, int32_t B,
-                                int32_t S, int32_t start_pos, int32_t H, int32_t G, int32_t D, llama_stream stream);
+                                int32_t S, int32_t start_pos, int32_t H, int32_t G, int32_t D, void *workspace,
+                                size_t workspace_bytes, llama_stream stream);
 
 /* RoPE cos/sin table: table[p][i] = {cos(p f_i), sin(p f_i)}, f_i = theta^(-2i/D),
  * p in [0, max_seq), i in [0, D/2), fp32 pairs computed in fp64 ("Mini Llama 2

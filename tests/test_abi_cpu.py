@@ -95,3 +95,5 @@ def test_null_arguments_are_rejected(lib):
     assert lib.llama_op_linear(lib.LLAMA_BF16, None, None, None, None, 16, 16, 12, 0) == lib.LLAMA_ERR_UNSUPPORTED
     assert lib.llama_op_attention(lib.LLAMA_BF16, None, lib.make_kv_cache(None, None, 1, 8), None, 2, 1, 0,
                                   4, 2, 64) == lib.LLAMA_ERR_RANGE
+    assert lib.llama_op_attention_workspace_bytes(lib.LLAMA_BF16, 64, 1, 4095, 32, 128) == 64 * 32 * 16 * 130 * 4
+    assert lib.llama_op_attention_workspace_bytes(lib.LLAMA_BF16, 64, 8, 0, 32, 128) == 0

@@ -144,7 +144,11 @@ ATTN_CASES = [
     (3, 45, 7, 9, 3, 64, "bf16"),     # SmolLM2 grouping (n_rep 3), cache prefix
     (1, 200, 0, 8, 2, 128, "bf16"),   # n_rep 4, several key tiles
     (2, 130, 60, 4, 2, 128, "bf16"),  # prefix + ragged
-    (5, 1, 300, 8, 2, 128, "bf16"),   # decode step, S = 1
+    (5, 1, 300, 8, 2, 128, "bf16"),   # decode step, S = 1, two key chunks
+    (3, 1, 77, 9, 3, 64, "bf16"),     # decode, one chunk, n_rep 3
+    (2, 1, 1000, 32, 8, 128, "bf16"), # decode, ragged last chunk
+    (4, 1, 0, 4, 4, 64, "bf16"),      # decode of the first position (MHA)
+    (1, 1, 700, 16, 2, 128, "bf16"),  # decode, n_rep 8
     (2, 3, 0, 2, 1, 32, "bf16"),
 ]
 
@@ -161,9 +165,8 @@ def test_attention(lb, B, S, start_pos, H, G, D, dtype):
     qd, kd, vd = to_dev(q), to_dev(kc), to_dev(vc)
     o = t.empty_like(qd)
     dt = lb.LLAMA_BF16 if dtype == "bf16" else lb.LLAMA_F32
-    st = lb.llama_op_attention(dt, qd, lb.make_kv_cache(kd, vd, B, L), o, B, S, start_pos, H, G, D)
-    if st == lb.LLAMA_ERR_UNSUPPORTED:
-        pytest.skip("step served by the block's workspace-backed path")
-    lb.check(st)
+    nws = lb.llama_op_attention_workspace_bytes(dt, B, S, start_pos, H, D)
+    ws = t.empty(max(nws, 16), dtype=t.uint8, device="cuda")
+    lb.check(lb.llama_op_attention(dt, qd, lb.make_kv_cache(kd, vd, B, L), o, B, S, start_pos, H, G, D, ws, nws))
     t.cuda.synchronize()
     assert_parity(to_f64(o), ref, dtype, f"attention B={B} S={S} sp={start_pos} H={H} G={G} D={D}")
