@@ -96,6 +96,8 @@ def load() -> ctypes.CDLL:
         "llama_op_attention": (st, [c_int32, c_void_p, POINTER(llama_kv_cache), c_void_p, c_int32, c_int32, c_int32,
                                     c_int32, c_int32, c_int32, c_void_p, c_size_t, c_void_p]),
         "llama_op_rope_table": (st, [c_void_p, c_int32, c_int32, c_float, c_void_p]),
+        "llama_op_attention_decode_noalloc": (st, [c_void_p, POINTER(llama_kv_cache), c_void_p, c_int32, c_int32,
+                                                   c_int32, c_int32, c_int32, c_void_p]),
         "llama_op_rope_kv_write": (st, [c_int32, c_void_p, c_void_p, POINTER(llama_kv_cache), c_void_p, c_int32,
                                         c_int32, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p]),
     }
@@ -244,6 +246,14 @@ def llama_op_rope_kv_write(dtype, qkv, q_out, kv: llama_kv_cache, table, table_m
                            stream=None) -> int:
     return load().llama_op_rope_kv_write(dtype, _p(qkv), _p(q_out), byref(kv), _p(table), table_max_seq, B, S,
                                          start_pos, H, G, D, _stream(stream))
+
+
+LLAMA_NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def llama_op_attention_decode_noalloc(q, kv: llama_kv_cache, o, B, start_pos, H, G, D, stream=None) -> int:
+    """Decode attention using the library's built-in scratch array (no device allocation)."""
+    return load().llama_op_attention_decode_noalloc(_p(q), byref(kv), _p(o), B, start_pos, H, G, D, _stream(stream))
 
 
 def check(status: int, what: str = "llama call") -> None:

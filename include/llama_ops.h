@@ -59,6 +59,33 @@ llama_status llama_op_rope_kv_write(int32_t dtype, const void *qkv, void *q_out,
                                     const float *table, int32_t table_max_seq, int32_t B, int32_t S,
                                     int32_t start_pos, int32_t H, int32_t G, int32_t D, llama_stream stream);
 
+/* Decode-step attention that allocates nothing.  The method's pages have no
+ * counterpart: this entry point exists for callers that cannot allocate device
+ * memory when they run attention (a serving engine whose pool already owns
+ * the device memory, an embedded runtime with a fixed budget, code that must
+ * not synchronise the device the way cudaMalloc can).
+ *
+ * Computes the same as llama_op_attention with dtype LLAMA_BF16 and S = 1:
+ * q, o: [B][H][D] bf16, kv: bf16 [max_batch][G][max_seq_len][D], keys
+ * 0 .. start_pos visible.  The split-KV partial results live in one array of
+ * LLAMA_NOALLOC_SCRATCH_BYTES that is part of the library image on every GPU
+ * that loads it, held until the process exits; no cudaMalloc / cudaFree or
+ * allocating library routine is called.
+ *   - Limit: B * H * ceil((start_pos + 1) / 256) * (D + 2) * 4 bytes must not
+ *     exceed LLAMA_NOALLOC_SCRATCH_BYTES, else LLAMA_ERR_RANGE (nothing runs).
+ *     32 MiB covers, e.g., B = 64, H = 32, D = 128 up to 8192 cached positions.
+ *   - D in {64, 128}, n_heads / n_kv_heads <= 8 (LLAMA_ERR_UNSUPPORTED otherwise).
+ *   - The first call on a device looks up the array's device address (a
+ *     one-time set-up per device, done with that device current); make that
+ *     first call before any stream capture.
+ *   - All calls share the array and every call overwrites the partials it
+ *     reads, so nothing needs clearing; calls that may run at the same time on
+ *     the GPU (unordered streams) race on the array and must be avoided. */
+#define LLAMA_NOALLOC_SCRATCH_BYTES (32u << 20)
+llama_status llama_op_attention_decode_noalloc(const void *q, const llama_kv_cache *kv, void *o, int32_t B,
+                                               int32_t start_pos, int32_t H, int32_t G, int32_t D,
+                                               llama_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
