@@ -108,7 +108,7 @@ class ClockSampler:
         try:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -224,7 +224,7 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-tokens", type=int, default=2048, help="oracle sample size for cpu_baseline")
@@ -311,18 +311,19 @@ def main():
     # ---- end to end: host buffers through llama_block_forward_host ----
     xh = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).pin_memory()
     yh = torch.empty_like(xh).pin_memory()
+    e2e_steps = max(3, min(args.steps, 40))
     for _ in range(2):
         lb.check(lb.llama_block_forward_host(blk, xh, yh, B, S, 0, kv, stream), "forward_host")
     torch.cuda.synchronize()
     barrier(world)
     ev0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(e2e_steps):
         lb.check(lb.llama_block_forward_host(blk, xh, yh, B, S, 0, kv, stream), "forward_host")
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
-    e2e_value = world * B * S * args.steps / (e2e_ms / 1e3)
+    e2e_value = world * B * S * e2e_steps / (e2e_ms / 1e3)
     io_bytes = B * S * d * 2
 
     # ---- roofline of the dominant kernel (gate/up + SwiGLU GEMM) ----
@@ -357,7 +358,7 @@ def main():
                      "traffic": traffic, "peak_source": f"{peak_kind} bf16_tflops_sustained"},
         "step_ms": step_ms,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
-                "d2h_bytes_per_step": io_bytes},
+                "d2h_bytes_per_step": io_bytes, "steps": e2e_steps},
         "gpu_launches": KERNELS_PER_PREFILL_FORWARD * args.steps,
         "clocks": clock_info,
     }
@@ -396,7 +397,7 @@ def bench_decode(lb, torch, w, dev, stream, args, peaks):
     for _ in range(args.warmup):
         lb.check(lb.llama_block_forward(blk, x, y, B, 1, sp, kv, stream))
     torch.cuda.synchronize()
-    steps = max(args.steps, 20)
+    steps = max(min(args.steps, 200), 20)
     lb.check(lb.llama_block_profile_enable(blk, steps))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)

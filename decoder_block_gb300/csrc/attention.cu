@@ -397,6 +397,9 @@ cudaError_t launch_attention(const bf16 *q, const bf16 *kc, const bf16 *vc, bf16
                              int H, int G, int D, int cache_seq, const AttnScratch &scratch, int *status,
                              cudaStream_t st) {
   const int r = H / G;
+  if (S == 1 && attn_decode_tc_supported(H, G, D) &&
+      (start_pos + 1 <= 512 || scratch.bytes >= attn_decode_tc_scratch_bytes(B, H, start_pos + 1)))
+    return launch_attn_decode_tc(q, kc, vc, o, B, start_pos, H, G, cache_seq, scratch, status, st);
   if (S == 1 && attn_decode_supported(H, G, D))
     return launch_attn_decode(q, kc, vc, o, B, start_pos, H, G, D, cache_seq, scratch, status, st);
   const bool tc_ok = (D == 64 || D == 128) && r <= 8 && S > 1;

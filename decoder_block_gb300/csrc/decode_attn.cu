@@ -334,6 +334,17 @@ size_t attn_decode_scratch_bytes(int max_tokens, int H, int D, int max_seq) {
   return want < cap ? want : (one > cap ? one : cap);
 }
 
+cudaError_t launch_decode_combine(const float *part, bf16 *o, int BH, int D, int n_split, cudaStream_t st) {
+  if (D == 128) {
+    attn_decode_combine<128><<<BH, 128, 0, st>>>(part, o, 0, n_split);
+  } else if (D == 64) {
+    attn_decode_combine<64><<<BH, 64, 0, st>>>(part, o, 0, n_split);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
 bool attn_decode_supported(int H, int G, int D) {
   const int r = H / G;
   return (D == 64 || D == 128) && r <= 8;

@@ -8,8 +8,51 @@ namespace llama {
 
 // ---------------------------------------------------------------- RMSNorm ---
 // "The Evolving Transformer 04 · LLaMA", §03 RMSNorm: x * rsqrt(mean(x^2) + eps) * g.
-// One warp per row, 16-byte vectors, fp32 sum of squares; second pass re-reads
-// the row (L1/L2 resident) to normalise and scale.
+// One warp per row, 16-byte vectors, fp32 sum of squares.  Rows of up to
+// NV * 32 vectors are held in registers (one read of x, one write of out, all
+// of a lane's loads in flight together); longer rows take the two-pass loop.
+template <typename T, int NV>
+__global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const T *__restrict__ x, const T *__restrict__ g,
+                                                          T *__restrict__ out, int rows, int d, float eps) {
+  constexpr int V = Vec16<T>::N;
+  const int row = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const T *xr = x + (size_t)row * d;
+  T *orow = out + (size_t)row * d;
+  const int nv = d / V;
+  Vec16<T> v[NV];
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const int i = lane + 32 * j;
+    if (i < nv) v[j] = load16(xr + (size_t)i * V);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    if (lane + 32 * j < nv) {
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        const float f = v[j].get(k);
+        ss = fmaf(f, f, ss);
+      }
+    }
+  }
+  ss = warp_sum(ss);
+  const float r = rsqrtf(ss / (float)d + eps);
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const int i = lane + 32 * j;
+    if (i < nv) {
+      const Vec16<T> gv = load16(g + (size_t)i * V);
+      Vec16<T> o;
+#pragma unroll
+      for (int k = 0; k < V; ++k) o.set(k, v[j].get(k) * r * gv.get(k));
+      store16(orow + (size_t)i * V, o);
+    }
+  }
+}
+
 template <typename T>
 __global__ void rmsnorm_kernel(const T *__restrict__ x, const T *__restrict__ g, T *__restrict__ out, int rows,
                                int d, float eps) {
@@ -46,7 +89,19 @@ cudaError_t launch_rmsnorm(const T *x, const T *g, T *out, int rows, int d, floa
   if (rows <= 0) return cudaSuccess;
   const int threads = 256;
   const int blocks = (int)(((size_t)rows * 32 + threads - 1) / threads);
-  rmsnorm_kernel<T><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps);
+  const int nv = d / Vec16<T>::N;
+  const int per_lane = (nv + 31) / 32;
+  switch (per_lane) {
+    case 1: rmsnorm_reg_kernel<T, 1><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
+    case 2: rmsnorm_reg_kernel<T, 2><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
+    case 3: rmsnorm_reg_kernel<T, 3><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
+    case 4: rmsnorm_reg_kernel<T, 4><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
+    case 5: case 6: case 7: case 8:
+      rmsnorm_reg_kernel<T, 8><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
+    case 9: case 10: case 11: case 12: case 13: case 14: case 15: case 16:
+      rmsnorm_reg_kernel<T, 16><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
+    default: rmsnorm_kernel<T><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
+  }
   return cudaGetLastError();
 }
 

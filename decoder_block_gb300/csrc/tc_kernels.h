@@ -37,6 +37,16 @@ cudaError_t launch_attn_decode(const bf16 *q, const bf16 *kc, const bf16 *vc, bf
                                int G, int D, int cache_seq, const AttnScratch &scratch, int *status,
                                cudaStream_t st);
 
+// Merge split-KV partials [BH][n_split][D + 2] (o, m, l) into o [BH][D] bf16.
+cudaError_t launch_decode_combine(const float *part, bf16 *o, int BH, int D, int n_split, cudaStream_t st);
+
+// Tensor-core decode attention (D = 128) -- decode_tc.cu.
+bool attn_decode_tc_supported(int H, int G, int D);
+size_t attn_decode_tc_scratch_bytes(int B, int H, int kv_len);
+cudaError_t launch_attn_decode_tc(const bf16 *q, const bf16 *kc, const bf16 *vc, bf16 *o, int B, int start_pos,
+                                  int H, int G, int cache_seq, const AttnScratch &scratch, int *status,
+                                  cudaStream_t st);
+
 // Causal GQA attention over the bf16 cache; picks the prefill or decode kernel.
 cudaError_t launch_attention(const bf16 *q, const bf16 *kc, const bf16 *vc, bf16 *o, int B, int S, int start_pos,
                              int H, int G, int D, int cache_seq, const AttnScratch &scratch, int *status,

@@ -149,6 +149,10 @@ ATTN_CASES = [
     (2, 1, 1000, 32, 8, 128, "bf16"), # decode, ragged last chunk
     (4, 1, 0, 4, 4, 64, "bf16"),      # decode of the first position (MHA)
     (1, 1, 700, 16, 2, 128, "bf16"),  # decode, n_rep 8
+    (3, 1, 5, 8, 2, 128, "bf16"),     # decode over 6 cached positions (one partial tile)
+    (1, 1, 40, 8, 2, 128, "bf16"),    # decode with fewer query rows than one 16-row operand
+    (2, 1, 600, 4, 4, 128, "bf16"),   # decode, MHA, d_head 128
+    (2, 1, 2047, 32, 8, 128, "bf16"), # decode, chunk edge (2048 cached positions)
     (2, 3, 0, 2, 1, 32, "bf16"),
 ]
 
