@@ -231,6 +231,9 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=512, help="oracle sample per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the secondary block shapes (SmolLM2-shaped block, 8B prefill B=4 S=2048)")
+    ap.add_argument("--no-stack", action="store_true", help="skip the 32-layer stack measurement")
     ap.add_argument("--seq", type=int, default=8192,
                     help="prefill length S (default 8192; smaller values are for profiler captures)")
     args = ap.parse_args()
@@ -344,6 +347,19 @@ def main():
     lb.llama_block_destroy(blk)
     del kc, vc
 
+    secondary = {}
+    if not args.no_secondary:
+        secondary["smollm2_135m_block_b8s1024"] = bench_block_shape(
+            lb, torch, dev, stream, dict(d_model=576, n_heads=9, n_kv_heads=3, d_ff=1536, norm_eps=1e-5,
+                                         rope_theta=1e5, B=8, S=1024), args)
+        secondary["llama3_8b_block_prefill_b4s2048"] = bench_block_shape(
+            lb, torch, dev, stream, dict(SHAPE, B=4, S=2048), args, weights=w)
+    stack = None
+    if not args.no_stack:
+        del w
+        torch.cuda.empty_cache()
+        stack = bench_stack(lb, torch, dev, stream, args)
+
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -364,6 +380,10 @@ def main():
     }
     if decode is not None:
         line["decode"] = decode
+    if secondary:
+        line["secondary"] = secondary
+    if stack is not None:
+        line["stack"] = stack
     if rank == 0 and not args.no_cpu_baseline:
         times = time_oracle(args.cpu_tokens)
         line["cpu_baseline"] = {"value": args.cpu_tokens / times[0], "unit": "tokens/s", "cores": os.cpu_count(),
@@ -376,6 +396,94 @@ def main():
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def _rand_weights(torch, dev, s, seed):
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    d, H, G, F = s["d_model"], s["n_heads"], s["n_kv_heads"], s["d_ff"]
+    D = d // H
+
+    def rn(*shape, std=0.02, mean=0.0):
+        return (torch.randn(shape, generator=g, device=dev, dtype=torch.float32) * std + mean).to(torch.bfloat16)
+
+    return {"attn_norm": rn(d, std=0.1, mean=1.0), "wq": rn(H * D, d), "wk": rn(G * D, d), "wv": rn(G * D, d),
+            "wo": rn(d, H * D), "ffn_norm": rn(d, std=0.1, mean=1.0), "w_gate": rn(F, d), "w_up": rn(F, d),
+            "w_down": rn(d, F)}
+
+
+def bench_block_shape(lb, torch, dev, stream, s, args, weights=None):
+    """tokens/s of one block forward at another shape (device-generated inputs)."""
+    B, S, d, G = s["B"], s["S"], s["d_model"], s["n_kv_heads"]
+    D = d // s["n_heads"]
+    w = weights if weights is not None else _rand_weights(torch, dev, s, 2)
+    cfg = lb.make_config(d, s["n_heads"], G, s["d_ff"], S, s["norm_eps"], s["rope_theta"], lb.LLAMA_BF16)
+    st, blk = lb.llama_block_create(cfg, lb.make_weights(w), B * S)
+    lb.check(st, "llama_block_create (secondary)")
+    x = torch.randn((B, S, d), device=dev, dtype=torch.float32).to(torch.bfloat16)
+    y = torch.empty_like(x)
+    kc = torch.zeros((B, G, S, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    kv = lb.make_kv_cache(kc, vc, B, S)
+    for _ in range(args.warmup):
+        lb.check(lb.llama_block_forward(blk, x, y, B, S, 0, kv, stream))
+    steps = max(10, min(args.steps, 100))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        lb.check(lb.llama_block_forward(blk, x, y, B, S, 0, kv, stream))
+    e1.record(stream)
+    torch.cuda.synchronize()
+    lb.check(lb.llama_block_device_status(blk))
+    lb.llama_block_destroy(blk)
+    ms = e0.elapsed_time(e1) / steps
+    lin, att = block_flops(dict(s, start_pos=0))
+    return {"B": B, "S": S, "d_model": d, "ms_per_step": ms, "tokens_per_s": B * S / (ms / 1e3),
+            "tflops": (lin + att) / (ms / 1e3) / 1e12, "steps": steps, "gpu_launches": KERNELS_PER_PREFILL_FORWARD * steps}
+
+
+def bench_stack(lb, torch, dev, stream, args, n_layers=32, vocab=128256, S=8192):
+    """32-layer Llama-3-8B-shaped stack prefill, B=1, S=8192, untied LM head (device-generated weights)."""
+    s = SHAPE
+    d, G = s["d_model"], s["n_kv_heads"]
+    D = d // s["n_heads"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(3)
+    layers = [_rand_weights(torch, dev, s, 100 + l) for l in range(n_layers)]
+    embed = (torch.randn((vocab, d), generator=g, device=dev, dtype=torch.float32) * 0.02).to(torch.bfloat16)
+    head = (torch.randn((vocab, d), generator=g, device=dev, dtype=torch.float32) * 0.02).to(torch.bfloat16)
+    fnorm = (1.0 + 0.1 * torch.randn((d,), generator=g, device=dev, dtype=torch.float32)).to(torch.bfloat16)
+    cfg = lb.make_config(d, s["n_heads"], G, s["d_ff"], S, s["norm_eps"], s["rope_theta"], lb.LLAMA_BF16)
+    st, stk = lb.llama_stack_create(cfg, n_layers, vocab, embed, [lb.make_weights(w) for w in layers], fnorm, head, S)
+    lb.check(st, "llama_stack_create")
+    del layers, embed, head
+    torch.cuda.empty_cache()
+    caches = [(torch.zeros((1, G, S, D), dtype=torch.bfloat16, device=dev),
+               torch.zeros((1, G, S, D), dtype=torch.bfloat16, device=dev)) for _ in range(n_layers)]
+    kvs = [lb.make_kv_cache(k, v, 1, S) for k, v in caches]
+    tokens = torch.randint(0, vocab, (1, S), generator=g, device=dev, dtype=torch.int32)
+    logits = torch.empty((1, S, vocab), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        lb.check(lb.llama_stack_forward(stk, tokens, 1, S, 0, kvs, logits, stream))
+    steps = 5
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        lb.check(lb.llama_stack_forward(stk, tokens, 1, S, 0, kvs, logits, stream))
+    e1.record(stream)
+    torch.cuda.synchronize()
+    status = lb.llama_stack_device_status(stk)
+    lb.llama_stack_destroy(stk)
+    ok = bool(torch.isfinite(logits).all().item())
+    ms = e0.elapsed_time(e1) / steps
+    lin, att = block_flops(dict(s, S=S))
+    total = n_layers * (lin + att) + 2.0 * S * d * vocab
+    return {"workload": "llama3_8b_stack_32l_prefill_b1s8192_vocab128256", "ms_per_step": ms,
+            "tokens_per_s": S / (ms / 1e3), "tflops": total / (ms / 1e3) / 1e12, "steps": steps,
+            "logits_finite": ok, "device_status": status,
+            "gpu_launches": steps * (1 + n_layers * KERNELS_PER_PREFILL_FORWARD + 2)}
 
 
 def bench_decode(lb, torch, w, dev, stream, args, peaks):

@@ -81,22 +81,17 @@ def _counter_base(count: int) -> np.ndarray:
     return _BASE[:count]
 
 
-def normal(seed: int, tag: str, shape, std: float = 1.0, mean: float = 0.0) -> np.ndarray:
-    """fp32 array of N(mean, std^2) samples for the stream (seed, tag)."""
-    shape = tuple(int(s) for s in np.atleast_1d(shape)) if not isinstance(shape, tuple) else shape
-    total = int(np.prod(shape, dtype=np.int64))
-    key = stream_key(seed, tag)
-    out = np.empty(total, dtype=np.float32)
-    npairs = (total + 1) // 2
-    n = min(_CHUNK, max(npairs, 1))
+def _normal_chunks(key: int, out: np.ndarray, total: int, p_begin: int, p_end: int, std: float, mean: float):
+    """Fill out[2*p_begin : 2*p_end] (clipped to total) with the normals of pairs [p_begin, p_end)."""
+    n = min(_CHUNK, max(p_end - p_begin, 1))
     wbuf = np.empty(n, dtype=np.uint64)
     tbuf = np.empty(n, dtype=np.uint64)
     rad = np.empty(n, dtype=np.float64)
     ang = np.empty(n, dtype=np.float32)
     trig = np.empty(n, dtype=np.float32)
     z = np.empty((n, 2), dtype=np.float64)
-    for p0 in range(0, npairs, _CHUNK):
-        c = min(npairs, p0 + _CHUNK) - p0
+    for p0 in range(p_begin, p_end, _CHUNK):
+        c = min(p_end, p0 + _CHUNK) - p0
         w = _words(key, p0, c, wbuf, tbuf)
         r = rad[:c]
         np.right_shift(w, np.uint64(32), out=tbuf[:c])
@@ -123,6 +118,38 @@ def normal(seed: int, tag: str, shape, std: float = 1.0, mean: float = 0.0) -> n
         e0 = 2 * p0
         e1 = min(total, 2 * (p0 + c))
         out[e0:e1] = zc.reshape(-1)[: e1 - e0]
+
+
+_POOL = None
+
+
+def _pool():
+    global _POOL
+    if _POOL is None:
+        import concurrent.futures
+        import os
+        _POOL = concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1)))
+    return _POOL
+
+
+def normal(seed: int, tag: str, shape, std: float = 1.0, mean: float = 0.0) -> np.ndarray:
+    """fp32 array of N(mean, std^2) samples for the stream (seed, tag).
+
+    Large arrays are filled by several host threads; every element depends
+    only on (seed, tag, index), so the result does not depend on the split."""
+    shape = tuple(int(s) for s in np.atleast_1d(shape)) if not isinstance(shape, tuple) else shape
+    total = int(np.prod(shape, dtype=np.int64))
+    key = stream_key(seed, tag)
+    out = np.empty(total, dtype=np.float32)
+    npairs = (total + 1) // 2
+    if npairs <= 4 * _CHUNK:
+        _normal_chunks(key, out, total, 0, npairs, std, mean)
+    else:
+        step = 4 * _CHUNK
+        futs = [_pool().submit(_normal_chunks, key, out, total, p, min(npairs, p + step), std, mean)
+                for p in range(0, npairs, step)]
+        for f in futs:
+            f.result()
     return out.reshape(shape)
 
 

@@ -58,6 +58,22 @@ def assert_parity(got, ref, dtype: str, what: str):
     return fro, mx
 
 
+# Relative-Frobenius bar for the logits (and deep-layer caches) of a multi-layer
+# bf16 stack: storing every GEMM operand in bf16 already moves two
+# Llama-3-8B-shaped layers ~1.2 % from the exact result (derived and pinned in
+# test_stack_tolerance.py); the bar keeps a factor two above that.
+STACK_FRO_REL = 2.5e-2
+
+
+def assert_stack_parity(got, ref, what):
+    got = np.asarray(got, dtype=np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    fro, mx = parity_errors(got, ref)
+    assert fro <= STACK_FRO_REL and mx <= BF16_MAX_REL, (
+        f"{what}: rel-Frobenius {fro:.3e} (bar {STACK_FRO_REL}), max|err|/max|ref| {mx:.3e} (bar {BF16_MAX_REL})")
+    return fro, mx
+
+
 def bf16_round(a: np.ndarray) -> np.ndarray:
     """fp64 -> nearest bf16 (via fp32) -> fp64."""
     return synth.as_f64(synth.f32_to_bf16_bits(np.asarray(a, dtype=np.float32)))

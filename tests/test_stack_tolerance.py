@@ -1,0 +1,75 @@
+"""Derivation of the stack-logits tolerance (CPU).
+
+A bf16 tensor-core stack stores every GEMM operand (the RMSNorm outputs, the
+SwiGLU product, q/k/v, P, the residual stream) in bf16.  This test replays the
+oracle's exact arithmetic with a bf16 rounding at each of those storage points
+(a model of the storage precision, not of any kernel) and measures how far the
+logits land from the exact fp64 oracle.  For two Llama-3-8B-shaped layers that
+inherent error is about 1.2 % relative Frobenius -- above the 5e-3 bar that
+holds for a single block -- so the stack's logits are compared with
+STACK_LOGITS_FRO_REL = 2.5e-2, at least twice the emulated error; the max-error
+bar (3e-2 max|ref|) is unchanged.
+"""
+import math
+
+import numpy as np
+
+import oracle
+import synth
+
+STACK_LOGITS_FRO_REL = 2.5e-2
+
+
+def _bf(a):
+    return synth.as_f64(synth.f32_to_bf16_bits(np.asarray(a, dtype=np.float32)))
+
+
+def _rms(x, g, eps):
+    return x / np.sqrt(np.mean(x * x, -1, keepdims=True) + eps) * g
+
+
+def _block_bf16_storage(cfg, w, x):
+    """The block with every stored activation rounded to bf16 (start_pos = 0)."""
+    d, H, G = cfg["d_model"], cfg["n_heads"], cfg["n_kv_heads"]
+    D, r = d // H, H // G
+    B, S, _ = x.shape
+    u = _bf(_rms(x, w["attn_norm"], cfg["norm_eps"]))
+    q = _bf(u @ w["wq"].T).reshape(B, S, H, D)
+    k = _bf(u @ w["wk"].T).reshape(B, S, G, D)
+    v = _bf(u @ w["wv"].T).reshape(B, S, G, D)
+    pos = np.arange(S)
+    q = _bf(oracle.rope(q, pos, cfg["rope_theta"]))
+    k = _bf(oracle.rope(k, pos, cfg["rope_theta"]))
+    o = np.zeros((B, S, H, D))
+    vis = np.arange(S)[None, :] <= np.arange(S)[:, None]
+    for b in range(B):
+        for h in range(H):
+            sc = np.where(vis, q[b, :, h] @ k[b, :, h // r].T / math.sqrt(D), -np.inf)
+            p = np.exp(sc - sc.max(-1, keepdims=True))
+            o[b, :, h] = (_bf(p) @ v[b, :, h // r]) / p.sum(-1, keepdims=True)
+    hres = _bf(x + _bf(o.reshape(B, S, H * D)) @ w["wo"].T)
+    v2 = _bf(_rms(hres, w["ffn_norm"], cfg["norm_eps"]))
+    gt, up = v2 @ w["w_gate"].T, v2 @ w["w_up"].T
+    return _bf(hres + _bf(gt / (1 + np.exp(-gt)) * up) @ w["w_down"].T)
+
+
+def test_bf16_storage_error_of_a_two_layer_8b_stack_sets_the_logits_bar():
+    s = dict(synth.SHAPES["llama3_8b_prefill_b1s8192"], max_seq_len=40)
+    B, S, vocab, n = 1, 40, 2048, 2
+    layers = [{k: synth.as_f64(v) for k, v in synth.block_weights(s, layer=l).items()} for l in range(n)]
+    embed = _bf(synth.normal(0, "embed", (vocab, s["d_model"]), std=0.02))
+    head = _bf(synth.normal(0, "lm_head", (vocab, s["d_model"]), std=0.02))
+    fnorm = _bf(synth.normal(0, "final_norm", (s["d_model"],), std=0.1, mean=1.0))
+    tokens = synth.uniform_int(0, "tokens", (B, S), vocab)
+    kc = np.zeros((B, s["n_kv_heads"], S, s["d_model"] // s["n_heads"]))
+    ref, _ = oracle.stack_forward(s, layers, embed, fnorm, head, tokens, 0, [(kc, kc)] * n)
+    x = embed[tokens]
+    for w in layers:
+        x = _block_bf16_storage(s, w, x)
+    emu = _bf(_rms(x, fnorm, s["norm_eps"])) @ head.T
+    err = float(np.linalg.norm(emu - ref) / np.linalg.norm(ref))
+    # the storage precision alone exceeds the single-block bar ...
+    assert err > 5e-3
+    # ... and the stack bar leaves at least a factor two above it
+    assert 2.0 * err <= STACK_LOGITS_FRO_REL
+    assert float(np.max(np.abs(emu - ref)) / np.max(np.abs(ref))) < 3e-2
