@@ -37,7 +37,8 @@ EPI_F32OUT = 2
 class LlamaError(RuntimeError):
     def __init__(self, status: int, what: str = ""):
         self.status = status
-        super().__init__(f"{what}: {llama_status_string(status)} ({status})")
+        detail = f" [{llama_last_cuda_error()}]" if status == LLAMA_ERR_CUDA else ""
+        super().__init__(f"{what}: {llama_status_string(status)} ({status}){detail}")
 
 
 class llama_config(ctypes.Structure):
@@ -89,6 +90,7 @@ def load() -> ctypes.CDLL:
         "llama_profile_step_name": (c_char_p, [c_int32]),
         "llama_ffn_hidden_dim": (c_int32, [c_int32, c_int32, c_float]),
         "llama_status_string": (c_char_p, [c_int32]),
+        "llama_last_cuda_error": (c_char_p, []),
         "llama_op_rmsnorm": (st, [c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_void_p]),
         "llama_op_linear": (st, [c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
                                  c_void_p]),
@@ -218,6 +220,10 @@ def llama_ffn_hidden_dim(d_model, multiple_of, ffn_dim_multiplier) -> int:
 
 def llama_status_string(status) -> str:
     return load().llama_status_string(status).decode()
+
+
+def llama_last_cuda_error() -> str:
+    return load().llama_last_cuda_error().decode()
 
 
 def llama_op_rmsnorm(dtype, x, g, out, T, d, eps, stream=None) -> int:

@@ -181,41 +181,62 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, KV_TILE, false);
       constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, true);
       bool ok = ptx::mbar_wait(q_full, 0, abort_flag, a.status, DEV_TIMEOUT_MMA);
+      // S_t(j) = Q_t K(j)^T into TMEM columns t*128 (P_t later overwrites them as bf16).
+      auto issue_s = [&](int j, int t) {
+        const uint32_t kb = s0 + L::OFF_K + (j % KV_STAGES) * L::KV_BYTES;
+        const uint32_t qbase = s0 + L::OFF_Q + t * L::Q_TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * L::ATOM + (kk % 4) * 32;
+          ptx::mma_bf16_ss(tmem + t * 128, ptx::smem_desc_sw128(qbase + off), ptx::smem_desc_sw128(kb + off),
+                           idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(s_full(t));
+      };
+      // O_t += P_t(j) V(j), P_t read from TMEM, V as an MN-major operand.
+      auto issue_pv = [&](int j, int t) {
+        const uint32_t vb = s0 + L::OFF_V + (j % KV_STAGES) * L::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < KV_TILE / 16; ++kk) {
+          // 16 keys = two 8-row groups of the V tile; V rows hold 64 consecutive d values.
+          const uint64_t bdesc = ptx::smem_desc_sw128_mn(vb + kk * 16 * 128, L::ATOM, 1024);
+          ptx::mma_bf16_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, bdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(o_done(t));
+      };
+      // Staggered order: S_0(j+1) is issued right after PV_0(j), so the softmax of tile 0 for
+      // the next key tile overlaps the softmax of tile 1 and the tensor core alternates tiles.
+      if (ok && n_kv > 0) {
+        ok = ptx::mbar_wait(k_full(0), 0, abort_flag, a.status, DEV_TIMEOUT_MMA);
+        if (ok) {
+          ptx::tc_fence_after();
+          issue_s(0, 0);
+          issue_s(0, 1);
+          ptx::mma_commit(k_empty(0));
+        }
+      }
       for (int j = 0; j < n_kv && ok; ++j) {
         const int st = j % KV_STAGES;
         const uint32_t ph = (j / KV_STAGES) & 1;
-        if (!ptx::mbar_wait(k_full(st), ph, abort_flag, a.status, DEV_TIMEOUT_MMA)) break;
-        ptx::tc_fence_after();
-        const uint32_t kb = s0 + L::OFF_K + st * L::KV_BYTES;
-        for (int t = 0; t < 2; ++t) {
-          const uint32_t qbase = s0 + L::OFF_Q + t * L::Q_TILE;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * L::ATOM + (kk % 4) * 32;
-            ptx::mma_bf16_ss(tmem + t * 128, ptx::smem_desc_sw128(qbase + off), ptx::smem_desc_sw128(kb + off),
-                             idesc_qk, kk > 0 ? 1u : 0u);
-          }
-          ptx::mma_commit(s_full(t));
-        }
-        ptx::mma_commit(k_empty(st));
         if (!ptx::mbar_wait(v_full(st), ph, abort_flag, a.status, DEV_TIMEOUT_MMA)) break;
-        const uint32_t vb = s0 + L::OFF_V + st * L::KV_BYTES;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (!ptx::mbar_wait(p_full(t), j & 1, abort_flag, a.status, DEV_TIMEOUT_MMA)) {
-            ok = false;
-            break;
-          }
+        if (!ptx::mbar_wait(p_full(0), j & 1, abort_flag, a.status, DEV_TIMEOUT_MMA)) break;
+        ptx::tc_fence_after();
+        issue_pv(j, 0);
+        const bool more = j + 1 < n_kv;
+        if (more) {
+          const int st1 = (j + 1) % KV_STAGES;
+          if (!ptx::mbar_wait(k_full(st1), ((j + 1) / KV_STAGES) & 1, abort_flag, a.status, DEV_TIMEOUT_MMA)) break;
           ptx::tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < KV_TILE / 16; ++kk) {
-            // 16 keys = two 8-row groups of the V tile; V rows hold 64 consecutive d values.
-            const uint64_t bdesc = ptx::smem_desc_sw128_mn(vb + kk * 16 * 128, L::ATOM, 1024);
-            ptx::mma_bf16_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, bdesc, idesc_pv,
-                             (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          ptx::mma_commit(o_done(t));
+          issue_s(j + 1, 0);
         }
+        if (!ptx::mbar_wait(p_full(1), j & 1, abort_flag, a.status, DEV_TIMEOUT_MMA)) break;
+        ptx::tc_fence_after();
+        issue_pv(j, 1);
         ptx::mma_commit(v_empty(st));
+        if (more) {
+          issue_s(j + 1, 1);
+          ptx::mma_commit(k_empty((j + 1) % KV_STAGES));
+        }
       }
       ptx::mma_commit(fin);
       int dummy = 0;
@@ -242,16 +263,18 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         break;
       }
       ptx::tc_fence_after();
-      float s[KV_TILE];
-#pragma unroll
-      for (int c = 0; c < KV_TILE; c += 32) ptx::tmem_ld32(s_col + c, *reinterpret_cast<float(*)[32]>(s + c));
-      ptx::tmem_ld_wait();
+      // Pass 1: row max over the tile, 32 columns at a time (causal predicate only
+      // on tiles that reach past some row's position).
       const int key0 = j * KV_TILE;
+      const bool masked = __any_sync(0xffffffffu, key0 + KV_TILE - 1 > pos);
       float mx = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < KV_TILE; ++k) {
-        if (key0 + k > pos) s[k] = -INFINITY;
-        mx = fmaxf(mx, s[k]);
+      for (int c = 0; c < KV_TILE; c += 32) {
+        float sv[32];
+        ptx::tmem_ld32(s_col + c, sv);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) mx = fmaxf(mx, (masked && key0 + c + k > pos) ? -INFINITY : sv[k]);
       }
       const float m_tile = mx * a.scale_log2;
       const bool need = m_tile > m_run + RESCALE_THRESHOLD;
@@ -279,16 +302,27 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
       }
       l_run *= alpha;
-      uint32_t pk[KV_TILE / 2];
+      // Pass 2: p = 2^(s*scale - m), written back as bf16 pairs.  The P chunk of
+      // columns [c, c+32) lands in TMEM columns [c/2, c/2 + 16), which only hold S
+      // values already read (columns < c + 32).
 #pragma unroll
-      for (int k = 0; k < KV_TILE; k += 2) {
-        const float p0 = ptx::ex2_approx(fmaf(s[k], a.scale_log2, -m_run));
-        const float p1 = ptx::ex2_approx(fmaf(s[k + 1], a.scale_log2, -m_run));
-        l_run += p0 + p1;
-        pk[k / 2] = pack2(p0, p1);
+      for (int c = 0; c < KV_TILE; c += 32) {
+        float sv[32];
+        ptx::tmem_ld32(s_col + c, sv);
+        ptx::tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const float s0v = (masked && key0 + c + k > pos) ? -INFINITY : sv[k];
+          const float s1v = (masked && key0 + c + k + 1 > pos) ? -INFINITY : sv[k + 1];
+          const float p0 = ptx::ex2_approx(fmaf(s0v, a.scale_log2, -m_run));
+          const float p1 = ptx::ex2_approx(fmaf(s1v, a.scale_log2, -m_run));
+          l_run += p0 + p1;
+          pk[k / 2] = pack2(p0, p1);
+        }
+        // P of columns [c, c+32) -> TMEM columns [c/2, c/2 + 16): only S values already read
+        ptx::tmem_st16(s_col + c / 2, pk);
       }
-#pragma unroll
-      for (int c = 0; c < KV_TILE / 2; c += 16) ptx::tmem_st16(s_col + c, *reinterpret_cast<uint32_t(*)[16]>(pk + c));
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(p_full(t));

@@ -22,6 +22,10 @@ enum DeviceStatusCode : int {
   DEV_BAD_TOKEN = 16,
 };
 
+// Remembers the last CUDA error of a failing library call in this host thread
+// (read through llama_last_cuda_error()).
+void note_cuda_error(cudaError_t e);
+
 __device__ __forceinline__ void report_status(int *status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }

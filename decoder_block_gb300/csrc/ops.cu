@@ -24,7 +24,11 @@ llama_status check(const void *p) {
   return device_ptr(p) ? LLAMA_OK : LLAMA_ERR_INVALID_ARG;
 }
 
-llama_status status_of(cudaError_t e) { return e == cudaSuccess ? LLAMA_OK : LLAMA_ERR_CUDA; }
+llama_status status_of(cudaError_t e) {
+  if (e == cudaSuccess) return LLAMA_OK;
+  note_cuda_error(e);
+  return LLAMA_ERR_CUDA;
+}
 
 bool head_dim_ok(int D) { return D == 16 || D == 32 || D == 64 || D == 128; }
 

@@ -23,6 +23,14 @@
 using namespace llama;
 
 namespace {
+thread_local const char *t_last_cuda_error = "no error";
+}  // namespace
+
+namespace llama {
+void note_cuda_error(cudaError_t e) { t_last_cuda_error = cudaGetErrorString(e); }
+}  // namespace llama
+
+namespace {
 
 struct Dims {
   int d, H, G, D, F, QKV, max_seq;
@@ -208,7 +216,10 @@ llama_status alloc_workspace(const Dims &dm, int max_tokens, bool staging, Alloc
 #define LAUNCH(expr)                                 \
   do {                                               \
     cudaError_t _e = (expr);                         \
-    if (_e != cudaSuccess) return LLAMA_ERR_CUDA;    \
+    if (_e != cudaSuccess) {                         \
+      note_cuda_error(_e);                           \
+      return LLAMA_ERR_CUDA;                         \
+    }                                                \
   } while (0)
 
 template <typename T>
@@ -582,6 +593,8 @@ int32_t llama_ffn_hidden_dim(int32_t d_model, int32_t multiple_of, float ffn_dim
   h = (long long)multiple_of * ((h + multiple_of - 1) / multiple_of);
   return h > 0x7fffffffLL ? -1 : (int32_t)h;
 }
+
+const char *llama_last_cuda_error(void) { return t_last_cuda_error; }
 
 const char *llama_status_string(llama_status s) {
   switch (s) {

@@ -151,6 +151,11 @@ int32_t llama_ffn_hidden_dim(int32_t d_model, int32_t multiple_of, float ffn_dim
 
 const char *llama_status_string(llama_status s);
 
+/* Text of the last CUDA error a call of this library returned LLAMA_ERR_CUDA
+ * for, in the calling host thread ("no error" when none).  The pointer stays
+ * valid until the next failing call in the same thread. */
+const char *llama_last_cuda_error(void);
+
 /* Per-step timing of llama_block_forward (tracing).  When enabled, every
  * forward call records a CUDA event pair on its stream around each step's
  * kernel launch, for up to max_forwards calls (events are created here;
