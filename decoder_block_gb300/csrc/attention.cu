@@ -254,7 +254,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(qq * 32) << 16);
     const uint32_t s_col = lane_base + t * 128;
     const uint32_t o_col = lane_base + 256 + t * D;
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY;
+    uint64_t l2 = ptx::f2pack(0.f, 0.f);  // running row sum, two partial halves
+    const uint64_t scale2 = ptx::f2pack(a.scale_log2, a.scale_log2);
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       ok = ptx::mbar_wait(s_full(t), j & 1, abort_flag, a.status, DEV_TIMEOUT_ATTN);
@@ -268,13 +270,22 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const int key0 = j * KV_TILE;
       const bool masked = __any_sync(0xffffffffu, key0 + KV_TILE - 1 > pos);
       float mx = -INFINITY;
+      if (masked) {
 #pragma unroll
-      for (int c = 0; c < KV_TILE; c += 32) {
-        float sv[32];
-        ptx::tmem_ld32(s_col + c, sv);
-        ptx::tmem_ld_wait();
+        for (int c = 0; c < KV_TILE; c += 32) {
+          float sv[32];
+          ptx::tmem_ld32(s_col + c, sv);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) mx = fmaxf(mx, (masked && key0 + c + k > pos) ? -INFINITY : sv[k]);
+          for (int k = 0; k < 32; ++k) mx = fmaxf(mx, key0 + c + k > pos ? -INFINITY : sv[k]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < KV_TILE; c += 32) {
+          float sv[32];
+          ptx::tmem_ld32(s_col + c, sv);
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) mx = ptx::max3(mx, sv[k], sv[k + 1]);
+        }
       }
       const float m_tile = mx * a.scale_log2;
       const bool need = m_tile > m_run + RESCALE_THRESHOLD;
@@ -301,26 +312,32 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           ptx::tmem_st16(o_col + c, w);
         }
       }
-      l_run *= alpha;
+      l2 = ptx::fmul2(l2, ptx::f2pack(alpha, alpha));
+      const uint64_t negm2 = ptx::f2pack(-m_run, -m_run);
       // Pass 2: p = 2^(s*scale - m), written back as bf16 pairs.  The P chunk of
       // columns [c, c+32) lands in TMEM columns [c/2, c/2 + 16), which only hold S
       // values already read (columns < c + 32).
+      // p = 2^(s*scale - m) written back as bf16 pairs; the P chunk of columns
+      // [c, c+32) lands in TMEM columns [c/2, c/2 + 16): only S values already read.
 #pragma unroll
       for (int c = 0; c < KV_TILE; c += 32) {
         float sv[32];
         ptx::tmem_ld32(s_col + c, sv);
-        ptx::tmem_ld_wait();
+        if (masked) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (key0 + c + k > pos) sv[k] = -INFINITY;
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
-          const float s0v = (masked && key0 + c + k > pos) ? -INFINITY : sv[k];
-          const float s1v = (masked && key0 + c + k + 1 > pos) ? -INFINITY : sv[k + 1];
-          const float p0 = ptx::ex2_approx(fmaf(s0v, a.scale_log2, -m_run));
-          const float p1 = ptx::ex2_approx(fmaf(s1v, a.scale_log2, -m_run));
-          l_run += p0 + p1;
+          float x0, x1;
+          ptx::f2unpack(ptx::ffma2(ptx::f2pack(sv[k], sv[k + 1]), scale2, negm2), x0, x1);
+          const float p0 = ptx::ex2_approx(x0);
+          const float p1 = ptx::ex2_approx(x1);
+          l2 = ptx::fadd2(l2, ptx::f2pack(p0, p1));
           pk[k / 2] = pack2(p0, p1);
         }
-        // P of columns [c, c+32) -> TMEM columns [c/2, c/2 + 16): only S values already read
         ptx::tmem_st16(s_col + c / 2, pk);
       }
       ptx::tmem_st_wait();
@@ -331,7 +348,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       ok = ptx::mbar_wait(o_done(t), (n_kv - 1) & 1, abort_flag, a.status, DEV_TIMEOUT_ATTN);
       if (__all_sync(0xffffffffu, ok)) {
         ptx::tc_fence_after();
-        const float inv = 1.f / l_run;
+        float la, lb;
+        ptx::f2unpack(l2, la, lb);
+        const float inv = 1.f / (la + lb);
         bf16 *dst = a.o + (((size_t)b * a.S + rel) * a.H + g * a.r + hh) * D;
 #pragma unroll
         for (int c = 0; c < D; c += 16) {

@@ -236,10 +236,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int nout = args.N / 2;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
-          float g[16], u[16];
-          ptx::tmem_ld16(trow + c, g);
-          ptx::tmem_ld16(trow + c + 16, u);
-          ptx::tmem_ld_wait();
+          float gu[32];  // gate in columns c .. c+15, up in c+16 .. c+31
+          ptx::tmem_ld32(trow + c, gu);
+          const float *g = gu;
+          const float *u = gu + 16;
           const int f = (nt * BN + c) / 2;
           if (m < args.M && f < nout) {
             bf16 *dst = reinterpret_cast<bf16 *>(args.C) + (size_t)m * nout + f;
