@@ -29,8 +29,9 @@ def nvcc() -> str:
 
 
 def _flags():
+    extra = os.environ.get("LLAMA_NVCC_FLAGS", "").split()  # optional tuning defines, e.g. -DNAME=value
     return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
-                   "-I", CSRC, "-I", os.path.join(ROOT, "include")]
+                   "-I", CSRC, "-I", os.path.join(ROOT, "include")] + extra
 
 
 def _compile(src: str, verbose_ptxas: bool) -> str:

@@ -36,6 +36,14 @@ constexpr int ATT_THREADS = 320;
 constexpr int KV_TILE = 128;
 constexpr int KV_STAGES = 2;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: rescale O when the running max grows by > 2^8
+// Of every 32 exponentials of a row, this many run as a polynomial on the FMA
+// pipe and the rest on the MUFU unit.  Measured on GB300 at the 8B prefill
+// shape: 0 of 32 is fastest (the MUFU unit is not what paces the tile), so the
+// polynomial path is off by default; -DLLAMA_POLY_EXP2_PER_32=n turns it on.
+#ifndef LLAMA_POLY_EXP2_PER_32
+#define LLAMA_POLY_EXP2_PER_32 0
+#endif
+constexpr int POLY_EXP2_PER_32 = LLAMA_POLY_EXP2_PER_32;
 
 template <int D>
 struct AttnLayout {
@@ -331,10 +339,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
-          float x0, x1;
+          float x0, x1, p0, p1;
           ptx::f2unpack(ptx::ffma2(ptx::f2pack(sv[k], sv[k + 1]), scale2, negm2), x0, x1);
-          const float p0 = ptx::ex2_approx(x0);
-          const float p1 = ptx::ex2_approx(x1);
+          if (k < POLY_EXP2_PER_32) {
+            ptx::exp2_poly2(x0, x1, p0, p1);  // FMA pipe
+          } else {
+            p0 = ptx::ex2_approx(x0);         // MUFU
+            p1 = ptx::ex2_approx(x1);
+          }
           l2 = ptx::fadd2(l2, ptx::f2pack(p0, p1));
           pk[k / 2] = pack2(p0, p1);
         }
