@@ -506,6 +506,7 @@ def bench_decode(lb, torch, w, dev, stream, args, peaks):
         lb.check(lb.llama_block_forward(blk, x, y, B, 1, sp, kv, stream))
     torch.cuda.synchronize()
     steps = max(min(args.steps, 200), 20)
+    # per-step breakdown (events around each kernel), plain launches
     lb.check(lb.llama_block_profile_enable(blk, steps))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -515,6 +516,24 @@ def bench_decode(lb, torch, w, dev, stream, args, peaks):
     torch.cuda.synchronize()
     st, launches, total_ms = lb.llama_block_profile_read(blk)
     lb.llama_block_profile_disable(blk)
+    us_plain = 1e3 * e0.elapsed_time(e1) / steps
+    # the decode step as a CUDA graph (launch-bound inner loop): one captured forward, replayed
+    gstream = torch.cuda.Stream(device=dev)
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(gstream):
+        lb.check(lb.llama_block_forward(blk, x, y, B, 1, sp, kv, gstream))  # warm the capture stream
+        gstream.synchronize()
+        with torch.cuda.graph(graph, stream=gstream):
+            lb.check(lb.llama_block_forward(blk, x, y, B, 1, sp, kv, gstream))
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
     lb.check(lb.llama_block_device_status(blk))
     lb.llama_block_destroy(blk)
     us = 1e3 * e0.elapsed_time(e1) / steps
@@ -523,7 +542,8 @@ def bench_decode(lb, torch, w, dev, stream, args, peaks):
     hbm = float(peaks["hbm_gbs"])
     weights_bytes = 2.0 * (d * (s["n_heads"] + 2 * G) * D + s["n_heads"] * D * d + 3 * d * s["d_ff"])
     step_bytes = weights_bytes + decode_attention_bytes(s)
-    return {"workload": "llama3_8b_block_decode_b64_pos4095", "us_per_step": us,
+    return {"workload": "llama3_8b_block_decode_b64_pos4095", "us_per_step": us, "us_per_step_plain_launches": us_plain,
+            "timing": "CUDA graph of one llama_block_forward, replayed; step_us from per-kernel events in plain launches",
             "step_hbm_gbs": step_bytes / (us / 1e6) / 1e9, "step_hbm_frac": step_bytes / (us / 1e6) / 1e9 / hbm,
             "attention_us": 1e3 * att_ms, "attention_gbs": gbs, "attention_hbm_frac": gbs / hbm,
             "hbm_peak_gbs": hbm, "gpu_launches": KERNELS_PER_DECODE_FORWARD * steps,

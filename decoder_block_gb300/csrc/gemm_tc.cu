@@ -2,16 +2,24 @@
 // the block (QKV, O, gate/up, down) and the LM head:  C = epi(A W^T), with A
 // [M,K] activations and W [N,K] nn.Linear weights, both bf16 and K-major.
 //
-// Per CTA (one per SM, 192 threads):
-//   warp 0      TMA producer: 128x64 A box + 256x64 W box per stage, 128-byte
-//               swizzle, STAGES-deep ring of shared-memory buffers;
-//   warp 1      allocates 512 TMEM columns, issues tcgen05.mma (M=128, N=256,
-//               K=16) from one thread into one of two 256-column fp32
+// Per CTA (one per SM, 192 threads), output tiles of 128 x BN (BN = 256, 128
+// or 64, picked per shape on the host):
+//   warp 0      TMA producer: 128x64 A box + BNx64 W box per stage, 128-byte
+//               swizzle, a ring of STAGES shared-memory buffers (deeper for
+//               narrower tiles);
+//   warp 1      allocates 2*BN TMEM columns, issues tcgen05.mma (M=128, N=BN,
+//               K=16) from one thread into one of two BN-column fp32
 //               accumulators, commits stage releases and accumulator-ready;
 //   warps 2..5  epilogue: tcgen05.ld the accumulator rows of their TMEM lane
 //               quarter, apply the fused epilogue (store / + residual /
 //               SiLU(gate) * up / fp32 out) and store to global memory, then
 //               hand the accumulator back -- overlapping the next tile's K loop.
+// Split-K (for few output tiles, e.g. the decode step's M = 64 rows, so that
+// every SM streams a share of the weights): a work unit is (tile, K split);
+// each epilogue warp adds its 32-row fp32 partial into the tile's fp32
+// accumulator in the workspace (vector reductions at L2, cleared before the
+// launch), counts arrivals on a per-(tile, quarter) counter, and the last
+// arriving warp reads the sums back once and applies the epilogue.
 // Every mbarrier wait is bounded (clock budget); on expiry the kernel records a
 // status code, drains in-flight copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -25,21 +33,31 @@
 namespace llama {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 5;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+constexpr int BM = 128, BK = 64;
 constexpr int NUM_THREADS = 192;
-constexpr uint32_t TMEM_COLS = 512;
 constexpr int GROUP_M = 16;
+
+template <int BN_>
+struct GemmCfg {
+  static constexpr int BN = BN_;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators (128, 256 or 512: powers of two)
+};
 
 struct GemmArgs {
   const bf16 *R;
   void *C;
   int M, N, K;
   int *status;
+  int splits;        // K splits per output tile (1: no split)
+  int ksteps_split;  // BK steps per split
+  float *part;       // split-K accumulators [tiles][BM][BN] fp32 (zero at launch)
+  int *counters;     // split-K arrivals [tiles][4]
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int &mt, int &nt) {
@@ -57,9 +75,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Columns n .. n+15 of row m (EPI_STORE / EPI_RESIDUAL / EPI_F32OUT).
 template <int EPI>
-__device__ __forceinline__ void epilogue_chunk16(const float (&v)[16], const GemmArgs &a, int m, int n) {
-  // v holds columns n .. n+15 of row m (EPI_STORE / EPI_RESIDUAL / EPI_F32OUT).
+__device__ __forceinline__ void epilogue_chunk16(const float *v, const GemmArgs &a, int m, int n) {
   if (m >= a.M || n >= a.N) return;
   const size_t base = (size_t)m * a.N + n;
   if constexpr (EPI == EPI_F32OUT) {
@@ -108,13 +126,37 @@ __device__ __forceinline__ void epilogue_chunk16(const float (&v)[16], const Gem
   }
 }
 
+// Accumulator columns n .. n+31 of row m through the fused epilogue.  For
+// SwiGLU the 32 columns are 16 gate then 16 up rows of the interleaved weight.
 template <int EPI>
+__device__ __forceinline__ void epilogue_chunk32(const float (&v)[32], const GemmArgs &a, int m, int n) {
+  if constexpr (EPI == EPI_SWIGLU) {
+    const int nout = a.N / 2;
+    const int f = n / 2;
+    if (m < a.M && f < nout) {
+      bf16 *dst = reinterpret_cast<bf16 *>(a.C) + (size_t)m * nout + f;
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        w[i] = pack_bf16(silu_f32(v[2 * i]) * v[16 + 2 * i], silu_f32(v[2 * i + 1]) * v[16 + 2 * i + 1]);
+      *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4 *>(dst + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+  } else {
+    epilogue_chunk16<EPI>(v, a, m, n);
+    epilogue_chunk16<EPI>(v + 16, a, m, n + 16);
+  }
+}
+
+template <int EPI, int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs args) {
+  using G = GemmCfg<BN>;
+  constexpr int STAGES = G::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * G::STAGE_BYTES);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + G::NUM_BARS);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const uint32_t smem0 = ptx::smem_u32(smem);
@@ -128,7 +170,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tiles = (args.M + BM - 1) / BM, n_tiles = (args.N + BN - 1) / BN;
   const int num_tiles = m_tiles * n_tiles;
+  const int num_units = num_tiles * args.splits;
   const int k_steps = (args.K + BK - 1) / BK;
+  // unit -> (tile, K range in BK steps)
+  auto unit_coords = [&](int u, int &mt, int &nt, int &k0, int &k1) {
+    const int tile = u / args.splits, sp = u % args.splits;
+    tile_coords(tile, m_tiles, n_tiles, mt, nt);
+    k0 = sp * args.ksteps_split;
+    k1 = min(k_steps, k0 + args.ksteps_split);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -144,7 +194,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), G::TMEM_COLS);
     ptx::tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -160,18 +210,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        int mt, nt;
-        tile_coords(tile, m_tiles, n_tiles, mt, nt);
-        for (int k = 0; k < k_steps; ++k) {
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        int mt, nt, k0, k1;
+        unit_coords(u, mt, nt, k0, k1);
+        for (int k = k0; k < k1; ++k) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!ptx::mbar_wait(empty_bar(s), ph ^ 1, abort_flag, args.status, DEV_TIMEOUT_PRODUCER)) {
             ok = false;
             break;
           }
-          const uint32_t sa = smem0 + s * STAGE_BYTES, sb = sa + A_BYTES;
-          ptx::mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
+          const uint32_t sa = smem0 + s * G::STAGE_BYTES, sb = sa + G::A_BYTES;
+          ptx::mbar_arrive_expect_tx(full_bar(s), G::STAGE_BYTES);
           ptx::tma_load_2d(sa, &tmA, k * BK, mt * BM, full_bar(s));
           ptx::tma_load_2d(sb, &tmB, k * BK, nt * BN, full_bar(s));
           ++it;
@@ -188,13 +238,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
       int it = 0, tcount = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tcount) {
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++tcount) {
+        int mt, nt, k0, k1;
+        unit_coords(u, mt, nt, k0, k1);
         const int acc = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
         if (!ptx::mbar_wait(tempty_bar(acc), aph ^ 1, abort_flag, args.status, DEV_TIMEOUT_MMA)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int k = 0; k < k_steps; ++k) {
+        for (int k = k0; k < k1; ++k) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!ptx::mbar_wait(full_bar(s), ph, abort_flag, args.status, DEV_TIMEOUT_MMA)) {
@@ -202,12 +254,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sa = smem0 + s * STAGE_BYTES, sb = sa + A_BYTES;
+          const uint32_t sa = smem0 + s * G::STAGE_BYTES, sb = sa + G::A_BYTES;
           const uint64_t adesc = ptx::smem_desc_sw128(sa), bdesc = ptx::smem_desc_sw128(sb);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             ptx::mma_bf16_ss(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
-                             (k | kk) != 0 ? 1u : 0u);
+                             (k > k0 || kk != 0) ? 1u : 0u);
           ptx::mma_commit(empty_bar(s));
           ++it;
         }
@@ -222,9 +274,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     int tcount = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tcount) {
-      int mt, nt;
-      tile_coords(tile, m_tiles, n_tiles, mt, nt);
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++tcount) {
+      int mt, nt, k0, k1;
+      unit_coords(u, mt, nt, k0, k1);
       const int acc = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
       bool ok = ptx::mbar_wait(tfull_bar(acc), aph, abort_flag, args.status, DEV_TIMEOUT_EPILOGUE);
@@ -232,43 +284,68 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::tc_fence_after();
       const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       const int m = mt * BM + row;
-      if constexpr (EPI == EPI_SWIGLU) {
-        const int nout = args.N / 2;
+      if (args.splits == 1) {
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
-          float gu[32];  // gate in columns c .. c+15, up in c+16 .. c+31
-          ptx::tmem_ld32(trow + c, gu);
-          const float *g = gu;
-          const float *u = gu + 16;
-          const int f = (nt * BN + c) / 2;
-          if (m < args.M && f < nout) {
-            bf16 *dst = reinterpret_cast<bf16 *>(args.C) + (size_t)m * nout + f;
-            uint32_t w[8];
+          float v[32];
+          ptx::tmem_ld32(trow + c, v);
+          epilogue_chunk32<EPI>(v, args, m, nt * BN + c);
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(tempty_bar(acc));
+      } else {
+        // split-K: add this warp's 32 x BN fp32 partial into the tile's accumulator,
+        // release TMEM, count arrivals; the last split's warp finishes the tile
+        const int tile = u / args.splits;
+        const bool rows_live = mt * BM + q * 32 < args.M;
+        float *acc_row = args.part + ((size_t)tile * BM + row) * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          ptx::tmem_ld32(trow + c, v);
+          if (m < args.M) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              w[i] = pack_bf16(silu_f32(g[2 * i]) * u[2 * i], silu_f32(g[2 * i + 1]) * u[2 * i + 1]);
-            *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-            *reinterpret_cast<uint4 *>(dst + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+            for (int i = 0; i < 32; i += 4) ptx::red_add_v4(acc_row + c + i, v[i], v[i + 1], v[i + 2], v[i + 3]);
           }
         }
-      } else {
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(tempty_bar(acc));
+        if (rows_live) {
+          __threadfence();
+          __syncwarp();
+          int prev = 0;
+          if (lane == 0) prev = atomicAdd(args.counters + tile * 4 + q, 1);
+          prev = __shfl_sync(0xffffffffu, prev, 0);
+          if (prev == args.splits - 1) {  // every split has added its partial: finish the tile
+            __threadfence();
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 16) {
-          float v[16];
-          ptx::tmem_ld16(trow + c, v);
-          ptx::tmem_ld_wait();
-          epilogue_chunk16<EPI>(v, args, m, nt * BN + c);
+            for (int c = 0; c < BN; c += 32) {
+              float v[32];
+              if (m < args.M) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                  const float4 p4 = __ldcg(reinterpret_cast<const float4 *>(acc_row + c + i));
+                  v[i] = p4.x;
+                  v[i + 1] = p4.y;
+                  v[i + 2] = p4.z;
+                  v[i + 3] = p4.w;
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+              }
+              epilogue_chunk32<EPI>(v, args, m, nt * BN + c);
+            }
+          }
         }
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(tempty_bar(acc));
     }
   }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    ptx::tmem_dealloc(tmem_base, G::TMEM_COLS);
   }
 }
 
@@ -304,18 +381,40 @@ int sm_count() {
   return n > 0 ? n : 1;
 }
 
-template <int EPI>
-cudaError_t launch_epi(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &args, cudaStream_t st) {
+template <int EPI, int BN>
+cudaError_t launch_cfg(const bf16 *A, const bf16 *W, GemmArgs args, cudaStream_t st) {
+  using G = GemmCfg<BN>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    G::SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
+  CUtensorMap ma, mb;
+  if (!make_map_2d(&ma, A, (uint64_t)args.M, (uint64_t)args.K, BM) ||
+      !make_map_2d(&mb, W, (uint64_t)args.N, (uint64_t)args.K, BN))
+    return cudaErrorInvalidValue;
   const int tiles = ((args.M + BM - 1) / BM) * ((args.N + BN - 1) / BN);
-  const int grid = tiles < sm_count() ? tiles : sm_count();
-  gemm_tc_kernel<EPI><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ma, mb, args);
+  const int units = tiles * args.splits;
+  if (args.splits > 1) {
+    cudaError_t e = cudaMemsetAsync(args.counters, 0, (size_t)tiles * 4 * sizeof(int), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(args.part, 0, (size_t)tiles * BM * BN * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+  }
+  const int grid = units < sm_count() ? units : sm_count();
+  gemm_tc_kernel<EPI, BN><<<grid, NUM_THREADS, G::SMEM_BYTES, st>>>(ma, mb, args);
   return cudaGetLastError();
+}
+
+template <int EPI>
+cudaError_t launch_epi(const bf16 *A, const bf16 *W, GemmArgs args, int bn, cudaStream_t st) {
+  switch (bn) {
+    case 256: return launch_cfg<EPI, 256>(A, W, args, st);
+    case 128: return launch_cfg<EPI, 128>(A, W, args, st);
+    case 64: return launch_cfg<EPI, 64>(A, W, args, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 __global__ void interleave_rows_kernel(const uint4 *__restrict__ gate, const uint4 *__restrict__ up,
@@ -332,20 +431,88 @@ __global__ void interleave_rows_kernel(const uint4 *__restrict__ gate, const uin
 
 }  // namespace
 
+GemmPlan plan_gemm(int M, int N, int K, size_t ws_part_bytes, int ws_counter_slots) {
+  const int sms = sm_count();
+  const int m_tiles = (M + BM - 1) / BM;
+  const int k_steps = (K + BK - 1) / BK;
+  GemmPlan p;
+  auto tiles_for = [&](int bn) { return m_tiles * ((N + bn - 1) / bn); };
+  if (tiles_for(256) >= sms) {
+    // Compute-bound regime: fewest waves, weighted by the narrower tiles' lower
+    // per-flop efficiency (shared-memory operand traffic per MMA).
+    const int bns[3] = {256, 128, 64};
+    const double eff[3] = {1.0, 1.12, 1.45};
+    double best = 1e30;
+    for (int i = 0; i < 3; ++i) {
+      const int waves = (tiles_for(bns[i]) + sms - 1) / sms;
+      const double cost = waves * bns[i] * eff[i];
+      if (cost < best - 1e-9) {
+        best = cost;
+        p.bn = bns[i];
+      }
+    }
+    return p;
+  }
+  // Few output tiles (decode: weight streaming): pick the tile width and K split
+  // that minimise the per-SM load, rounds x (K steps per unit) x (shared-memory
+  // fill per K step: 16 KB of A plus BN x 128 B of weights); ties go to more
+  // units (more SMs streaming weights at once).
+  double best = 1e30;
+  int best_units = 0;
+  const int bns[3] = {256, 128, 64};
+  for (int i = 0; i < 3; ++i) {
+    const int bn = bns[i];
+    const int tiles = tiles_for(bn);
+    for (int want = 1; want <= 16 && want <= k_steps; ++want) {
+      const int kss = (k_steps + want - 1) / want;
+      const int splits = (k_steps + kss - 1) / kss;
+      const int units = tiles * splits;
+      if (splits > 1 && ((size_t)tiles * BM * bn * sizeof(float) > ws_part_bytes || tiles * 4 > ws_counter_slots))
+        continue;
+      const int rounds = (units + sms - 1) / sms;
+      // + 12 K steps of fixed per-unit cost (pipeline fill, epilogue; measured on the
+      // decode shapes); split reductions add the partial rows once more
+      const double cost = (double)rounds * (kss + 12) * (16.0 + bn / 8.0) + (splits > 1 ? bn / 8.0 : 0.0);
+      if (cost < best - 1e-9 || (cost <= best + 1e-9 && units > best_units && units <= sms)) {
+        best = cost;
+        best_units = units;
+        p.bn = bn;
+        p.splits = splits;
+        p.ksteps_split = kss;
+      }
+    }
+  }
+  if (p.splits == 1) p.ksteps_split = 0;
+  return p;
+}
+
+size_t gemm_splitk_part_bytes() {
+  // Split plans arise only when fewer than one wave of 128x256 tiles exists,
+  // i.e. fewer than 2 x SMs 128-wide or 4 x SMs 64-wide tiles: one fp32
+  // accumulator tile each.
+  return (size_t)sm_count() * BM * 256 * sizeof(float);
+}
+
+int gemm_splitk_counter_slots() { return 4 * sm_count() * 4; }
+
 cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C, int M, int N, int K, int epi,
-                           int *status, cudaStream_t st) {
+                           int *status, cudaStream_t st, const GemmWorkspace *ws) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   if (K <= 0 || (K & 7) != 0) return cudaErrorInvalidValue;
   if (epi == EPI_SWIGLU && (N & 31) != 0) return cudaErrorInvalidValue;
-  CUtensorMap ma, mb;
-  if (!make_map_2d(&ma, A, (uint64_t)M, (uint64_t)K, BM) || !make_map_2d(&mb, W, (uint64_t)N, (uint64_t)K, BN))
-    return cudaErrorInvalidValue;
-  GemmArgs args{R, C, M, N, K, status};
+  const GemmPlan plan = plan_gemm(M, N, K, ws != nullptr ? ws->part_bytes : 0, ws != nullptr ? ws->counter_slots : 0);
+  GemmArgs args{R, C, M, N, K, status, 1, (K + BK - 1) / BK, nullptr, nullptr};
+  if (plan.splits > 1) {
+    args.splits = plan.splits;
+    args.ksteps_split = plan.ksteps_split;
+    args.part = ws->part;
+    args.counters = ws->counters;
+  }
   switch (epi) {
-    case EPI_STORE: return launch_epi<EPI_STORE>(ma, mb, args, st);
-    case EPI_RESIDUAL: return launch_epi<EPI_RESIDUAL>(ma, mb, args, st);
-    case EPI_F32OUT: return launch_epi<EPI_F32OUT>(ma, mb, args, st);
-    case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(ma, mb, args, st);
+    case EPI_STORE: return launch_epi<EPI_STORE>(A, W, args, plan.bn, st);
+    case EPI_RESIDUAL: return launch_epi<EPI_RESIDUAL>(A, W, args, plan.bn, st);
+    case EPI_F32OUT: return launch_epi<EPI_F32OUT>(A, W, args, plan.bn, st);
+    case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(A, W, args, plan.bn, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -114,6 +114,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Vector fp32 atomic add to global memory, no return value (performed at L2).
+__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
 // Three-input maximum (one instruction).
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;

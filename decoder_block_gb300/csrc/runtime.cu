@@ -75,6 +75,7 @@ struct Workspace {
   void *xn = nullptr, *qkv = nullptr, *q = nullptr, *o = nullptr, *h = nullptr, *act = nullptr, *hn = nullptr;
   void *xin = nullptr, *yout = nullptr;  // staging for the host-buffer entry point
   AttnScratch attn;                      // split-KV partials of the decode path
+  GemmWorkspace gemm;                    // split-K partials of few-row GEMMs (decode)
 };
 
 // Optional per-step event timing of block forwards (llama_block_profile_*).
@@ -209,6 +210,10 @@ llama_status alloc_workspace(const Dims &dm, int max_tokens, bool staging, Alloc
     const size_t bytes = attn_decode_scratch_bytes(max_tokens, dm.H, dm.D, dm.max_seq);
     ws->attn.partial = al.alloc(bytes);
     ws->attn.bytes = bytes;
+    ws->gemm.part_bytes = gemm_splitk_part_bytes();
+    ws->gemm.part = (float *)al.alloc(ws->gemm.part_bytes);
+    ws->gemm.counter_slots = gemm_splitk_counter_slots();
+    ws->gemm.counters = (int *)al.alloc((size_t)ws->gemm.counter_slots * sizeof(int));
   }
   return al.failed ? LLAMA_ERR_OOM : LLAMA_OK;
 }
@@ -256,7 +261,7 @@ llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, c
   LAUNCH(launch_rmsnorm<bf16>(x, (const bf16 *)w.attn_norm, xn, M, dm.d, dm.eps, st));
   pf.mark(0, 1, st);
   pf.mark(1, 0, st);
-  LAUNCH(launch_gemm_tc(xn, (const bf16 *)w.wqkv, nullptr, qkv, M, dm.QKV, dm.d, EPI_STORE, status, st));
+  LAUNCH(launch_gemm_tc(xn, (const bf16 *)w.wqkv, nullptr, qkv, M, dm.QKV, dm.d, EPI_STORE, status, st, &ws.gemm));
   pf.mark(1, 1, st);
   pf.mark(2, 0, st);
   LAUNCH(launch_rope_kv<bf16>(qkv, q, kc, vc, rope, B, S, start_pos, dm.H, dm.G, dm.D, kv->max_seq_len, st));
@@ -265,16 +270,17 @@ llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, c
   LAUNCH(launch_attention(q, kc, vc, o, B, S, start_pos, dm.H, dm.G, dm.D, kv->max_seq_len, ws.attn, status, st));
   pf.mark(3, 1, st);
   pf.mark(4, 0, st);
-  LAUNCH(launch_gemm_tc(o, (const bf16 *)w.wo, x, h, M, dm.d, dm.H * dm.D, EPI_RESIDUAL, status, st));
+  LAUNCH(launch_gemm_tc(o, (const bf16 *)w.wo, x, h, M, dm.d, dm.H * dm.D, EPI_RESIDUAL, status, st, &ws.gemm));
   pf.mark(4, 1, st);
   pf.mark(5, 0, st);
   LAUNCH(launch_rmsnorm<bf16>(h, (const bf16 *)w.ffn_norm, hn, M, dm.d, dm.eps, st));
   pf.mark(5, 1, st);
   pf.mark(6, 0, st);
-  LAUNCH(launch_gemm_tc(hn, (const bf16 *)w.w_gu, nullptr, act, M, 2 * dm.F, dm.d, EPI_SWIGLU, status, st));
+  LAUNCH(launch_gemm_tc(hn, (const bf16 *)w.w_gu, nullptr, act, M, 2 * dm.F, dm.d, EPI_SWIGLU, status, st,
+                        &ws.gemm));
   pf.mark(6, 1, st);
   pf.mark(7, 0, st);
-  LAUNCH(launch_gemm_tc(act, (const bf16 *)w.w_down, h, y, M, dm.d, dm.F, EPI_RESIDUAL, status, st));
+  LAUNCH(launch_gemm_tc(act, (const bf16 *)w.w_down, h, y, M, dm.d, dm.F, EPI_RESIDUAL, status, st, &ws.gemm));
   pf.mark(7, 1, st);
   return LLAMA_OK;
 }
@@ -553,7 +559,7 @@ llama_status llama_stack_forward(llama_stack *stk, const int32_t *tokens, int32_
   if (dm.dtype == LLAMA_BF16) {
     LAUNCH(launch_rmsnorm<bf16>((const bf16 *)cur, (const bf16 *)stk->final_norm, (bf16 *)stk->xn, M, dm.d, dm.eps, st));
     LAUNCH(launch_gemm_tc((const bf16 *)stk->xn, (const bf16 *)stk->lm_head, nullptr, logits, M, stk->vocab, dm.d,
-                          EPI_F32OUT, stk->status, st));
+                          EPI_F32OUT, stk->status, st, &stk->ws.gemm));
   } else {
     LAUNCH(launch_rmsnorm<float>((const float *)cur, (const float *)stk->final_norm, (float *)stk->xn, M, dm.d, dm.eps,
                                  st));

@@ -17,9 +17,28 @@ namespace llama {
 //                launch_interleave_rows); C bf16 [M, N/2] = SiLU(gate) * up
 //   EPI_F32OUT   C fp32 [M,N]
 // Requirements: K % 8 == 0 (16-byte TMA row pitch); EPI_SWIGLU needs N % 32 == 0.
+// Split-K scratch of the GEMM (fp32 partial tiles and arrival counters).
+struct GemmWorkspace {
+  float *part = nullptr;
+  size_t part_bytes = 0;
+  int *counters = nullptr;
+  int counter_slots = 0;
+};
+size_t gemm_splitk_part_bytes();
+int gemm_splitk_counter_slots();
+
+// Tile width and K split chosen for a shape (split-K only when ws can hold it).
+struct GemmPlan {
+  int bn = 256;
+  int splits = 1;
+  int ksteps_split = 0;
+};
+GemmPlan plan_gemm(int M, int N, int K, size_t ws_part_bytes, int ws_counter_slots);
+
 // status: device status word for bounded-wait expiry (may be null).
+// ws: split-K scratch (null: never split).
 cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C, int M, int N, int K, int epi,
-                           int *status, cudaStream_t st);
+                           int *status, cudaStream_t st, const GemmWorkspace *ws = nullptr);
 
 // out[32j + i] = gate[16j + i], out[32j + 16 + i] = up[16j + i] (rows of width d), F % 16 == 0.
 cudaError_t launch_interleave_rows(const bf16 *gate, const bf16 *up, bf16 *out, int F, int d, cudaStream_t st);
