@@ -58,6 +58,9 @@ struct GemmArgs {
   int ksteps_split;  // BK steps per split
   float *part;       // split-K accumulators [tiles][BM][BN] fp32 (zero at launch)
   int *counters;     // split-K arrivals [tiles][4]
+  const float *ss_in;  // ROWSCALE epilogues: per-row sum of squares of A's rows
+  float *ss_out;       // EPI_RESIDUAL_SQSUM: per-row sum of squares of C (accumulated)
+  float inv_d, eps;    // RMSNorm: scale = rsqrt(ss * inv_d + eps)
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int &mt, int &nt) {
@@ -75,11 +78,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Columns n .. n+15 of row m (EPI_STORE / EPI_RESIDUAL / EPI_F32OUT).
-template <int EPI>
-__device__ __forceinline__ void epilogue_chunk16(const float *v, const GemmArgs &a, int m, int n) {
-  if (m >= a.M || n >= a.N) return;
+// Columns n .. n+15 of row m (EPI_STORE / EPI_RESIDUAL / EPI_F32OUT).  With
+// SQSUM, returns the sum of squares of the bf16 values stored.
+template <int EPI, bool SQSUM = false>
+__device__ __forceinline__ float epilogue_chunk16(const float *v, const GemmArgs &a, int m, int n) {
+  if (m >= a.M || n >= a.N) return 0.f;
   const size_t base = (size_t)m * a.N + n;
+  float sq = 0.f;
   if constexpr (EPI == EPI_F32OUT) {
     float *c = reinterpret_cast<float *>(a.C) + base;
     if (n + 16 <= a.N && (a.N & 3) == 0) {
@@ -112,6 +117,13 @@ __device__ __forceinline__ void epilogue_chunk16(const float *v, const GemmArgs 
           if (n + i < a.N) w[i] += __bfloat162float(r[i]);
       }
     }
+    if constexpr (SQSUM) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float q = __bfloat162float(__float2bfloat16_rn(w[i]));
+        if (vec || n + i < a.N) sq = fmaf(q, q, sq);
+      }
+    }
     if (vec) {
       uint4 o0 = make_uint4(pack_bf16(w[0], w[1]), pack_bf16(w[2], w[3]), pack_bf16(w[4], w[5]), pack_bf16(w[6], w[7]));
       uint4 o1 = make_uint4(pack_bf16(w[8], w[9]), pack_bf16(w[10], w[11]), pack_bf16(w[12], w[13]),
@@ -124,13 +136,21 @@ __device__ __forceinline__ void epilogue_chunk16(const float *v, const GemmArgs 
         if (n + i < a.N) c[i] = __float2bfloat16_rn(w[i]);
     }
   }
+  return sq;
 }
 
 // Accumulator columns n .. n+31 of row m through the fused epilogue.  For
 // SwiGLU the 32 columns are 16 gate then 16 up rows of the interleaved weight.
+// Returns the row's sum-of-squares contribution (EPI_RESIDUAL_SQSUM), else 0.
 template <int EPI>
-__device__ __forceinline__ void epilogue_chunk32(const float (&v)[32], const GemmArgs &a, int m, int n) {
-  if constexpr (EPI == EPI_SWIGLU) {
+__device__ __forceinline__ float epilogue_chunk32(float (&v)[32], const GemmArgs &a, int m, int n) {
+  if constexpr (EPI == EPI_STORE_ROWSCALE || EPI == EPI_SWIGLU_ROWSCALE) {
+    // RMSNorm of A's row m, applied to the GEMM result (the gain is folded into W)
+    const float r = m < a.M ? rsqrtf(a.ss_in[m] * a.inv_d + a.eps) : 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= r;
+  }
+  if constexpr (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_ROWSCALE) {
     const int nout = a.N / 2;
     const int f = n / 2;
     if (m < a.M && f < nout) {
@@ -142,9 +162,17 @@ __device__ __forceinline__ void epilogue_chunk32(const float (&v)[32], const Gem
       *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
       *reinterpret_cast<uint4 *>(dst + 8) = make_uint4(w[4], w[5], w[6], w[7]);
     }
+    return 0.f;
+  } else if constexpr (EPI == EPI_STORE_ROWSCALE) {
+    epilogue_chunk16<EPI_STORE>(v, a, m, n);
+    epilogue_chunk16<EPI_STORE>(v + 16, a, m, n + 16);
+    return 0.f;
+  } else if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
+    return epilogue_chunk16<EPI_RESIDUAL, true>(v, a, m, n) + epilogue_chunk16<EPI_RESIDUAL, true>(v + 16, a, m, n + 16);
   } else {
     epilogue_chunk16<EPI>(v, a, m, n);
     epilogue_chunk16<EPI>(v + 16, a, m, n + 16);
+    return 0.f;
   }
 }
 
@@ -285,14 +313,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       const int m = mt * BM + row;
       if (args.splits == 1) {
+        float sq = 0.f;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           float v[32];
           ptx::tmem_ld32(trow + c, v);
-          epilogue_chunk32<EPI>(v, args, m, nt * BN + c);
+          sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + c);
         }
         ptx::tc_fence_before();
         ptx::mbar_arrive(tempty_bar(acc));
+        if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
+          if (m < args.M) atomicAdd(args.ss_out + m, sq);
+        }
       } else {
         // split-K: add this warp's 32 x BN fp32 partial into the tile's accumulator,
         // release TMEM, count arrivals; the last split's warp finishes the tile
@@ -318,6 +350,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           prev = __shfl_sync(0xffffffffu, prev, 0);
           if (prev == args.splits - 1) {  // every split has added its partial: finish the tile
             __threadfence();
+            float sq = 0.f;
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
               float v[32];
@@ -334,7 +367,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = 0.f;
               }
-              epilogue_chunk32<EPI>(v, args, m, nt * BN + c);
+              sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + c);
+            }
+            if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
+              if (m < args.M) atomicAdd(args.ss_out + m, sq);
             }
           }
         }
@@ -496,12 +532,20 @@ size_t gemm_splitk_part_bytes() {
 int gemm_splitk_counter_slots() { return 4 * sm_count() * 4; }
 
 cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C, int M, int N, int K, int epi,
-                           int *status, cudaStream_t st, const GemmWorkspace *ws) {
+                           int *status, cudaStream_t st, const GemmWorkspace *ws, const RowNorm *norm) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   if (K <= 0 || (K & 7) != 0) return cudaErrorInvalidValue;
-  if (epi == EPI_SWIGLU && (N & 31) != 0) return cudaErrorInvalidValue;
+  if ((epi == EPI_SWIGLU || epi == EPI_SWIGLU_ROWSCALE) && (N & 31) != 0) return cudaErrorInvalidValue;
+  const bool needs_norm = epi == EPI_STORE_ROWSCALE || epi == EPI_SWIGLU_ROWSCALE || epi == EPI_RESIDUAL_SQSUM;
+  if (needs_norm && norm == nullptr) return cudaErrorInvalidValue;
   const GemmPlan plan = plan_gemm(M, N, K, ws != nullptr ? ws->part_bytes : 0, ws != nullptr ? ws->counter_slots : 0);
-  GemmArgs args{R, C, M, N, K, status, 1, (K + BK - 1) / BK, nullptr, nullptr};
+  GemmArgs args{R, C, M, N, K, status, 1, (K + BK - 1) / BK, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f};
+  if (norm != nullptr) {
+    args.ss_in = norm->ss_in;
+    args.ss_out = norm->ss_out;
+    args.inv_d = 1.0f / (float)norm->d;
+    args.eps = norm->eps;
+  }
   if (plan.splits > 1) {
     args.splits = plan.splits;
     args.ksteps_split = plan.ksteps_split;
@@ -513,6 +557,9 @@ cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C,
     case EPI_RESIDUAL: return launch_epi<EPI_RESIDUAL>(A, W, args, plan.bn, st);
     case EPI_F32OUT: return launch_epi<EPI_F32OUT>(A, W, args, plan.bn, st);
     case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(A, W, args, plan.bn, st);
+    case EPI_STORE_ROWSCALE: return launch_epi<EPI_STORE_ROWSCALE>(A, W, args, plan.bn, st);
+    case EPI_SWIGLU_ROWSCALE: return launch_epi<EPI_SWIGLU_ROWSCALE>(A, W, args, plan.bn, st);
+    case EPI_RESIDUAL_SQSUM: return launch_epi<EPI_RESIDUAL_SQSUM>(A, W, args, plan.bn, st);
   }
   return cudaErrorInvalidValue;
 }

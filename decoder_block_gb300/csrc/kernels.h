@@ -13,7 +13,19 @@ enum Epilogue : int {
   EPI_RESIDUAL = 1,  // C = R + A W^T             (R, C in the input dtype)
   EPI_F32OUT = 2,    // C = A W^T, C fp32
   EPI_SWIGLU = 3,    // C = SiLU(A W1^T) * (A W3^T)
+  // RMSNorm fused into the consuming GEMM (gain folded into W at create time):
+  // row m of the accumulator is scaled by rsqrt(ss[m] / d + eps).
+  EPI_STORE_ROWSCALE = 4,   // C = r_m (A W^T)
+  EPI_SWIGLU_ROWSCALE = 5,  // C = SiLU(r_m A W1^T) * (r_m A W3^T)
+  // residual add that also accumulates ss_out[m] += sum_n C[m,n]^2 of the stored bf16 C
+  EPI_RESIDUAL_SQSUM = 6,
 };
+
+// ss[t] = sum_j x[t][j]^2 (fp32) for rows of width d.
+cudaError_t launch_row_sqsum(const bf16 *x, float *ss, int rows, int d, cudaStream_t st);
+
+// W[n][k] <- bf16(W[n][k] * g[k]) in place (fold an RMSNorm gain into a weight).
+cudaError_t launch_scale_columns(bf16 *W, const bf16 *g, int rows, int cols, cudaStream_t st);
 
 // RMSNorm of `rows` rows of width d (d % (16 / sizeof(T)) == 0).
 template <typename T>

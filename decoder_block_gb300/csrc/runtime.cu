@@ -11,6 +11,11 @@
 //   6. v2  = RMSNorm(h; ffn_norm)
 //   7. a   = SiLU(v2 W_gate^T) * (v2 W_up^T)  (SwiGLU in the epilogue)
 //   8. y   = h + a W_down^T                   (residual in the epilogue)
+// bf16 tensor-core path: both RMSNorms are fused -- their gains are folded into
+// [Wq; Wk; Wv] and [W_gate; W_up] at create time, a row-statistics pass (step 1)
+// and the O-projection epilogue (step 5) produce sum(x^2) and sum(h^2) per row,
+// and the QKV and gate/up epilogues scale each row by rsqrt(mean + eps).  The
+// fp32 path keeps the standalone steps.
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -76,6 +81,7 @@ struct Workspace {
   void *xin = nullptr, *yout = nullptr;  // staging for the host-buffer entry point
   AttnScratch attn;                      // split-KV partials of the decode path
   GemmWorkspace gemm;                    // split-K partials of few-row GEMMs (decode)
+  float *ss_x = nullptr, *ss_h = nullptr;  // per-row sums of squares (fused RMSNorm statistics)
 };
 
 // Optional per-step event timing of block forwards (llama_block_profile_*).
@@ -184,6 +190,12 @@ llama_status copy_weights(const Dims &dm, const llama_block_weights *w, Allocs &
     if (err == cudaSuccess)
       err = launch_interleave_rows((const bf16 *)w->w_gate, (const bf16 *)w->w_up, (bf16 *)out->w_gu, dm.F, dm.d,
                                    nullptr);
+    // RMSNorm gains folded into the consuming projections: (x g) W^T = x (W diag g)^T,
+    // so the GEMMs read the raw activations and scale rows by rsqrt(mean(x^2) + eps).
+    if (err == cudaSuccess)
+      err = launch_scale_columns((bf16 *)out->wqkv, (const bf16 *)w->attn_norm, dm.QKV, dm.d, nullptr);
+    if (err == cudaSuccess)
+      err = launch_scale_columns((bf16 *)out->w_gu, (const bf16 *)w->ffn_norm, 2 * dm.F, dm.d, nullptr);
     if (err == cudaSuccess) err = cudaDeviceSynchronize();
   } else {
     cp(out->w_gate, w->w_gate, (size_t)dm.F * dm.d * e);
@@ -195,13 +207,15 @@ llama_status copy_weights(const Dims &dm, const llama_block_weights *w, Allocs &
 llama_status alloc_workspace(const Dims &dm, int max_tokens, bool staging, Allocs &al, Workspace *ws) {
   const size_t e = dm.esize, T = (size_t)max_tokens;
   ws->max_tokens = max_tokens;
-  ws->xn = al.alloc(T * dm.d * e);
+  if (dm.dtype != LLAMA_BF16) {  // standalone RMSNorm outputs (the bf16 path fuses both norms)
+    ws->xn = al.alloc(T * dm.d * e);
+    ws->hn = al.alloc(T * dm.d * e);
+  }
   ws->qkv = al.alloc(T * dm.QKV * e);
   ws->q = al.alloc(T * dm.H * dm.D * e);
   ws->o = al.alloc(T * dm.H * dm.D * e);
   ws->h = al.alloc(T * dm.d * e);
   ws->act = al.alloc(T * dm.F * e);
-  ws->hn = al.alloc(T * dm.d * e);
   if (staging) {
     ws->xin = al.alloc(T * dm.d * e);
     ws->yout = al.alloc(T * dm.d * e);
@@ -214,6 +228,8 @@ llama_status alloc_workspace(const Dims &dm, int max_tokens, bool staging, Alloc
     ws->gemm.part = (float *)al.alloc(ws->gemm.part_bytes);
     ws->gemm.counter_slots = gemm_splitk_counter_slots();
     ws->gemm.counters = (int *)al.alloc((size_t)ws->gemm.counter_slots * sizeof(int));
+    ws->ss_x = (float *)al.alloc(T * sizeof(float));
+    ws->ss_h = (float *)al.alloc(T * sizeof(float));
   }
   return al.failed ? LLAMA_ERR_OOM : LLAMA_OK;
 }
@@ -251,17 +267,23 @@ llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, c
                         bf16 *y, int B, int S, int start_pos, const llama_kv_cache *kv, int *status, Profiler *prof,
                         cudaStream_t st) {
   const int M = B * S;
-  bf16 *xn = (bf16 *)ws.xn, *qkv = (bf16 *)ws.qkv, *q = (bf16 *)ws.q, *o = (bf16 *)ws.o, *h = (bf16 *)ws.h,
-       *act = (bf16 *)ws.act, *hn = (bf16 *)ws.hn;
+  bf16 *qkv = (bf16 *)ws.qkv, *q = (bf16 *)ws.q, *o = (bf16 *)ws.o, *h = (bf16 *)ws.h, *act = (bf16 *)ws.act;
   bf16 *kc = (bf16 *)kv->k, *vc = (bf16 *)kv->v;
   Profiler none;
   Profiler &pf = prof != nullptr ? *prof : none;
   pf.begin_forward();
+  // attention_norm statistics; the normalisation itself happens in the QKV GEMM
   pf.mark(0, 0, st);
-  LAUNCH(launch_rmsnorm<bf16>(x, (const bf16 *)w.attn_norm, xn, M, dm.d, dm.eps, st));
+  LAUNCH(launch_row_sqsum(x, ws.ss_x, M, dm.d, st));
+  if (cudaMemsetAsync(ws.ss_h, 0, (size_t)M * sizeof(float), st) != cudaSuccess) return LLAMA_ERR_CUDA;
   pf.mark(0, 1, st);
+  RowNorm norm_x;
+  norm_x.ss_in = ws.ss_x;
+  norm_x.eps = dm.eps;
+  norm_x.d = dm.d;
   pf.mark(1, 0, st);
-  LAUNCH(launch_gemm_tc(xn, (const bf16 *)w.wqkv, nullptr, qkv, M, dm.QKV, dm.d, EPI_STORE, status, st, &ws.gemm));
+  LAUNCH(launch_gemm_tc(x, (const bf16 *)w.wqkv, nullptr, qkv, M, dm.QKV, dm.d, EPI_STORE_ROWSCALE, status, st,
+                        &ws.gemm, &norm_x));
   pf.mark(1, 1, st);
   pf.mark(2, 0, st);
   LAUNCH(launch_rope_kv<bf16>(qkv, q, kc, vc, rope, B, S, start_pos, dm.H, dm.G, dm.D, kv->max_seq_len, st));
@@ -269,15 +291,21 @@ llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, c
   pf.mark(3, 0, st);
   LAUNCH(launch_attention(q, kc, vc, o, B, S, start_pos, dm.H, dm.G, dm.D, kv->max_seq_len, ws.attn, status, st));
   pf.mark(3, 1, st);
+  // h = x + o Wo^T; the epilogue also accumulates the ffn_norm statistics of h
+  RowNorm norm_h;
+  norm_h.ss_in = ws.ss_h;
+  norm_h.ss_out = ws.ss_h;
+  norm_h.eps = dm.eps;
+  norm_h.d = dm.d;
   pf.mark(4, 0, st);
-  LAUNCH(launch_gemm_tc(o, (const bf16 *)w.wo, x, h, M, dm.d, dm.H * dm.D, EPI_RESIDUAL, status, st, &ws.gemm));
+  LAUNCH(launch_gemm_tc(o, (const bf16 *)w.wo, x, h, M, dm.d, dm.H * dm.D, EPI_RESIDUAL_SQSUM, status, st, &ws.gemm,
+                        &norm_h));
   pf.mark(4, 1, st);
-  pf.mark(5, 0, st);
-  LAUNCH(launch_rmsnorm<bf16>(h, (const bf16 *)w.ffn_norm, hn, M, dm.d, dm.eps, st));
+  pf.mark(5, 0, st);  // ffn_norm: fused into the O and gate/up GEMM epilogues
   pf.mark(5, 1, st);
   pf.mark(6, 0, st);
-  LAUNCH(launch_gemm_tc(hn, (const bf16 *)w.w_gu, nullptr, act, M, 2 * dm.F, dm.d, EPI_SWIGLU, status, st,
-                        &ws.gemm));
+  LAUNCH(launch_gemm_tc(h, (const bf16 *)w.w_gu, nullptr, act, M, 2 * dm.F, dm.d, EPI_SWIGLU_ROWSCALE, status, st,
+                        &ws.gemm, &norm_h));
   pf.mark(6, 1, st);
   pf.mark(7, 0, st);
   LAUNCH(launch_gemm_tc(act, (const bf16 *)w.w_down, h, y, M, dm.d, dm.F, EPI_RESIDUAL, status, st, &ws.gemm));

@@ -105,6 +105,49 @@ cudaError_t launch_rmsnorm(const T *x, const T *g, T *out, int rows, int d, floa
   return cudaGetLastError();
 }
 
+// Sum of squares per row (the RMSNorm statistic of rows the next GEMM normalises
+// in its epilogue): one warp per row, 16-byte loads, fp32 accumulation.
+__global__ void __launch_bounds__(256) row_sqsum_kernel(const bf16 *__restrict__ x, float *__restrict__ ss, int rows,
+                                                        int d) {
+  const int row = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const bf16 *xr = x + (size_t)row * d;
+  const int nv = d / 8;
+  float acc = 0.f;
+#pragma unroll 4
+  for (int i = lane; i < nv; i += 32) {
+    Vec16<bf16> v = load16(xr + (size_t)i * 8);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float f = v.get(k);
+      acc = fmaf(f, f, acc);
+    }
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) ss[row] = acc;
+}
+
+cudaError_t launch_row_sqsum(const bf16 *x, float *ss, int rows, int d, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  row_sqsum_kernel<<<(unsigned)(((size_t)rows * 32 + 255) / 256), 256, 0, st>>>(x, ss, rows, d);
+  return cudaGetLastError();
+}
+
+__global__ void scale_columns_kernel(bf16 *__restrict__ W, const bf16 *__restrict__ g, int rows, int cols) {
+  const size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  if (idx >= (size_t)rows * cols) return;
+  const int k = (int)(idx % cols);
+  W[idx] = __float2bfloat16_rn(__bfloat162float(W[idx]) * __bfloat162float(g[k]));
+}
+
+cudaError_t launch_scale_columns(bf16 *W, const bf16 *g, int rows, int cols, cudaStream_t st) {
+  const size_t n = (size_t)rows * cols;
+  if (n == 0) return cudaSuccess;
+  scale_columns_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(W, g, rows, cols);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------ SIMT GEMM ---
 // C[M,N] = A[M,K] W[N,K]^T (nn.Linear, no bias), fp32 accumulation.
 // 64x64 output tile per 256-thread CTA, 4x4 per thread, K step 16.

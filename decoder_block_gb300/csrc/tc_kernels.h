@@ -35,10 +35,21 @@ struct GemmPlan {
 };
 GemmPlan plan_gemm(int M, int N, int K, size_t ws_part_bytes, int ws_counter_slots);
 
+// RMSNorm statistics for the fused epilogues: ss_in (ROWSCALE modes) holds
+// sum_j A[m][j]^2 over the d normalised columns; ss_out (EPI_RESIDUAL_SQSUM)
+// receives sum_n C[m][n]^2 (must be zero before the launch).
+struct RowNorm {
+  const float *ss_in = nullptr;
+  float *ss_out = nullptr;
+  float eps = 0.f;
+  int d = 1;
+};
+
 // status: device status word for bounded-wait expiry (may be null).
-// ws: split-K scratch (null: never split).
+// ws: split-K scratch (null: never split).  norm: required by the ROWSCALE and SQSUM epilogues.
 cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C, int M, int N, int K, int epi,
-                           int *status, cudaStream_t st, const GemmWorkspace *ws = nullptr);
+                           int *status, cudaStream_t st, const GemmWorkspace *ws = nullptr,
+                           const RowNorm *norm = nullptr);
 
 // out[32j + i] = gate[16j + i], out[32j + 16 + i] = up[16j + i] (rows of width d), F % 16 == 0.
 cudaError_t launch_interleave_rows(const bf16 *gate, const bf16 *up, bf16 *out, int F, int d, cudaStream_t st);
