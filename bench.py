@@ -37,8 +37,6 @@ WORKLOAD = "llama3_8b_block_prefill_b1s8192"
 SHAPE = dict(d_model=4096, n_heads=32, n_kv_heads=8, d_ff=14336, norm_eps=1e-5, rope_theta=5e5, dtype="bf16",
              B=1, S=8192, start_pos=0, max_seq_len=8192)
 DECODE = dict(SHAPE, B=64, S=1, start_pos=4095, max_seq_len=4096)
-KERNELS_PER_PREFILL_FORWARD = 8  # rmsnorm, QKV GEMM, RoPE+KV, attention, O GEMM, rmsnorm, gate/up GEMM, down GEMM
-KERNELS_PER_DECODE_FORWARD = 9   # the same plus the split-KV combine
 
 
 def block_flops(s):
@@ -295,10 +293,12 @@ def main():
     barrier(world)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = lb.llama_kernel_launch_count()
     ev0.record(stream)
     for _ in range(args.steps):
         step()
     ev1.record(stream)
+    launches_timed = lb.llama_kernel_launch_count() - launches0
     torch.cuda.synchronize()
     barrier(world)
     elapsed_ms = ev0.elapsed_time(ev1)
@@ -375,7 +375,7 @@ def main():
         "step_ms": step_ms,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
                 "d2h_bytes_per_step": io_bytes, "steps": e2e_steps},
-        "gpu_launches": KERNELS_PER_PREFILL_FORWARD * args.steps,
+        "gpu_launches": launches_timed,
         "clocks": clock_info,
     }
     if decode is not None:
@@ -430,17 +430,39 @@ def bench_block_shape(lb, torch, dev, stream, s, args, weights=None):
     steps = max(10, min(args.steps, 100))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    n0 = lb.llama_kernel_launch_count()
     e0.record(stream)
     for _ in range(steps):
         lb.check(lb.llama_block_forward(blk, x, y, B, S, 0, kv, stream))
     e1.record(stream)
+    per_forward = (lb.llama_kernel_launch_count() - n0) // steps
     torch.cuda.synchronize()
+    ms_plain = e0.elapsed_time(e1) / steps
+    # the same step captured once in a CUDA graph and replayed (no per-kernel launch gaps)
+    gstream = torch.cuda.Stream(device=dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(gstream):
+        lb.check(lb.llama_block_forward(blk, x, y, B, S, 0, kv, gstream))
+        gstream.synchronize()
+        with torch.cuda.graph(graph, stream=gstream):
+            lb.check(lb.llama_block_forward(blk, x, y, B, S, 0, kv, gstream))
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_graph = e0.elapsed_time(e1) / steps
     lb.check(lb.llama_block_device_status(blk))
     lb.llama_block_destroy(blk)
-    ms = e0.elapsed_time(e1) / steps
+    ms = min(ms_plain, ms_graph)
     lin, att = block_flops(dict(s, start_pos=0))
-    return {"B": B, "S": S, "d_model": d, "ms_per_step": ms, "tokens_per_s": B * S / (ms / 1e3),
-            "tflops": (lin + att) / (ms / 1e3) / 1e12, "steps": steps, "gpu_launches": KERNELS_PER_PREFILL_FORWARD * steps}
+    return {"B": B, "S": S, "d_model": d, "ms_per_step": ms, "ms_per_step_plain_launches": ms_plain,
+            "ms_per_step_cuda_graph": ms_graph, "tokens_per_s": B * S / (ms / 1e3),
+            "tflops": (lin + att) / (ms / 1e3) / 1e12, "steps": steps, "kernels_per_step": per_forward,
+            "gpu_launches": per_forward * steps}
 
 
 def bench_stack(lb, torch, dev, stream, args, n_layers=32, vocab=128256, S=8192):
@@ -469,10 +491,12 @@ def bench_stack(lb, torch, dev, stream, args, n_layers=32, vocab=128256, S=8192)
     steps = 5
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    n0 = lb.llama_kernel_launch_count()
     e0.record(stream)
     for _ in range(steps):
         lb.check(lb.llama_stack_forward(stk, tokens, 1, S, 0, kvs, logits, stream))
     e1.record(stream)
+    n_launched = lb.llama_kernel_launch_count() - n0
     torch.cuda.synchronize()
     status = lb.llama_stack_device_status(stk)
     lb.llama_stack_destroy(stk)
@@ -483,7 +507,7 @@ def bench_stack(lb, torch, dev, stream, args, n_layers=32, vocab=128256, S=8192)
     return {"workload": "llama3_8b_stack_32l_prefill_b1s8192_vocab128256", "ms_per_step": ms,
             "tokens_per_s": S / (ms / 1e3), "tflops": total / (ms / 1e3) / 1e12, "steps": steps,
             "logits_finite": ok, "device_status": status,
-            "gpu_launches": steps * (1 + n_layers * KERNELS_PER_PREFILL_FORWARD + 2)}
+            "gpu_launches": n_launched}
 
 
 def bench_decode(lb, torch, w, dev, stream, args, peaks):
@@ -509,10 +533,12 @@ def bench_decode(lb, torch, w, dev, stream, args, peaks):
     # per-step breakdown (events around each kernel), plain launches
     lb.check(lb.llama_block_profile_enable(blk, steps))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = lb.llama_kernel_launch_count()
     e0.record(stream)
     for _ in range(steps):
         lb.check(lb.llama_block_forward(blk, x, y, B, 1, sp, kv, stream))
     e1.record(stream)
+    per_forward = (lb.llama_kernel_launch_count() - n0) // steps
     torch.cuda.synchronize()
     st, launches, total_ms = lb.llama_block_profile_read(blk)
     lb.llama_block_profile_disable(blk)
@@ -546,7 +572,7 @@ def bench_decode(lb, torch, w, dev, stream, args, peaks):
             "timing": "CUDA graph of one llama_block_forward, replayed; step_us from per-kernel events in plain launches",
             "step_hbm_gbs": step_bytes / (us / 1e6) / 1e9, "step_hbm_frac": step_bytes / (us / 1e6) / 1e9 / hbm,
             "attention_us": 1e3 * att_ms, "attention_gbs": gbs, "attention_hbm_frac": gbs / hbm,
-            "hbm_peak_gbs": hbm, "gpu_launches": KERNELS_PER_DECODE_FORWARD * steps,
+            "hbm_peak_gbs": hbm, "kernels_per_step": per_forward, "gpu_launches": per_forward * steps,
             "step_us": {lb.llama_profile_step_name(i): 1e3 * total_ms[i] / max(launches[i], 1)
                         for i in range(len(launches))}}
 

@@ -91,6 +91,7 @@ def load() -> ctypes.CDLL:
         "llama_ffn_hidden_dim": (c_int32, [c_int32, c_int32, c_float]),
         "llama_status_string": (c_char_p, [c_int32]),
         "llama_last_cuda_error": (c_char_p, []),
+        "llama_kernel_launch_count": (ctypes.c_ulonglong, []),
         "llama_op_rmsnorm": (st, [c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_void_p]),
         "llama_op_linear": (st, [c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
                                  c_void_p]),
@@ -224,6 +225,10 @@ def llama_status_string(status) -> str:
 
 def llama_last_cuda_error() -> str:
     return load().llama_last_cuda_error().decode()
+
+
+def llama_kernel_launch_count() -> int:
+    return int(load().llama_kernel_launch_count())
 
 
 def llama_op_rmsnorm(dtype, x, g, out, T, d, eps, stream=None) -> int:

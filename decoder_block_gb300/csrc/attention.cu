@@ -452,6 +452,7 @@ cudaError_t launch_prefill(const bf16 *q, const bf16 *kc, const bf16 *vc, bf16 *
   args.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   args.status = status;
   const unsigned grid = (unsigned)(B * G * args.nqb);
+  count_launch();
   attn_prefill_kernel<D><<<grid, ATT_THREADS, L::BYTES, st>>>(mq, mk, mv, args);
   return cudaGetLastError();
 }

@@ -25,6 +25,8 @@ enum DeviceStatusCode : int {
 // Remembers the last CUDA error of a failing library call in this host thread
 // (read through llama_last_cuda_error()).
 void note_cuda_error(cudaError_t e);
+// Counts one kernel launch (library-wide total, read by llama_kernel_launch_count).
+void count_launch();
 
 __device__ __forceinline__ void report_status(int *status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);

@@ -301,10 +301,12 @@ cudaError_t launch_dec(const DecArgs &base, int B, const AttnScratch &scratch, c
     a.vc = base.vc + (size_t)b0 * base.G * base.cache_seq * D;
     a.o = base.o + (size_t)b0 * base.H * D;
     dim3 grid(base.n_split, base.G, nb);
+    count_launch();
     attn_decode_kernel<D, RP><<<grid, DEC_THREADS, L::BYTES, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (base.n_split > 1) {
+      count_launch();
       attn_decode_combine<D><<<nb * base.H, D, 0, st>>>(a.part, a.o, base.H, base.n_split);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
@@ -336,8 +338,10 @@ size_t attn_decode_scratch_bytes(int max_tokens, int H, int D, int max_seq) {
 
 cudaError_t launch_decode_combine(const float *part, bf16 *o, int BH, int D, int n_split, cudaStream_t st) {
   if (D == 128) {
+    count_launch();
     attn_decode_combine<128><<<BH, 128, 0, st>>>(part, o, 0, n_split);
   } else if (D == 64) {
+    count_launch();
     attn_decode_combine<64><<<BH, 64, 0, st>>>(part, o, 0, n_split);
   } else {
     return cudaErrorInvalidValue;

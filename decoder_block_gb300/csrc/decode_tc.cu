@@ -472,6 +472,7 @@ cudaError_t launch_attn_decode_tc(const bf16 *q, const bf16 *kc, const bf16 *vc,
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = a.n_items < sms ? a.n_items : sms;
+  count_launch();
   attn_decode_tc_kernel<<<grid, DT_THREADS, DtLayout::BYTES, st>>>(mq, mk, mv, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.n_split == 1) return e;

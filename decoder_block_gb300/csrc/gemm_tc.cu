@@ -12,7 +12,8 @@
 //               accumulators, commits stage releases and accumulator-ready;
 //   warps 2..5  epilogue: tcgen05.ld the accumulator rows of their TMEM lane
 //               quarter, apply the fused epilogue (store / + residual /
-//               SiLU(gate) * up / fp32 out) and store to global memory, then
+//               SiLU(gate) * up / fp32 out / RMSNorm row scale / RoPE and
+//               KV-cache scatter) and store to global memory, then
 //               hand the accumulator back -- overlapping the next tile's K loop.
 // Split-K (for few output tiles, e.g. the decode step's M = 64 rows, so that
 // every SM streams a share of the weights): a work unit is (tile, K split);
@@ -61,6 +62,7 @@ struct GemmArgs {
   const float *ss_in;  // ROWSCALE epilogues: per-row sum of squares of A's rows
   float *ss_out;       // EPI_RESIDUAL_SQSUM: per-row sum of squares of C (accumulated)
   float inv_d, eps;    // RMSNorm: scale = rsqrt(ss * inv_d + eps)
+  QkvScatter qkv;      // EPI_QKV_ROPE destinations
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int &mt, int &nt) {
@@ -142,9 +144,44 @@ __device__ __forceinline__ float epilogue_chunk16(const float *v, const GemmArgs
 // Accumulator columns n .. n+31 of row m through the fused epilogue.  For
 // SwiGLU the 32 columns are 16 gate then 16 up rows of the interleaved weight.
 // Returns the row's sum-of-squares contribution (EPI_RESIDUAL_SQSUM), else 0.
+// EPI_QKV_ROPE: 32 consecutive columns of one head (D % 32 == 0), already row
+// scaled.  Interleaved pairs (2i, 2i+1) sit in adjacent registers.
+__device__ __forceinline__ void qkv_rope_chunk32(const float (&v)[32], const GemmArgs &a, int m, int n) {
+  const QkvScatter &r = a.qkv;
+  if (m >= a.M || n >= a.N) return;
+  const int head = n / r.D, e = n % r.D;
+  const int b = m / r.S, p = r.start_pos + m % r.S;
+  uint32_t w[16];
+  if (head < r.H + r.G) {
+    // "The Evolving Transformer 04 · LLaMA", §02 RoPE: (a cos - b sin, a sin + b cos)
+    const float4 *cs = reinterpret_cast<const float4 *>(r.table + (size_t)p * (r.D / 2) + e / 2);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float4 c = __ldg(cs + k);  // {cos_i, sin_i, cos_i+1, sin_i+1}
+      const float a0 = v[4 * k], b0 = v[4 * k + 1], a1 = v[4 * k + 2], b1 = v[4 * k + 3];
+      w[2 * k] = pack_bf16(a0 * c.x - b0 * c.y, a0 * c.y + b0 * c.x);
+      w[2 * k + 1] = pack_bf16(a1 * c.z - b1 * c.w, a1 * c.w + b1 * c.z);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) w[k] = pack_bf16(v[2 * k], v[2 * k + 1]);
+  }
+  bf16 *dst;
+  if (head < r.H) {
+    dst = r.q + (size_t)m * r.H * r.D + n;
+  } else {
+    const bool is_k = head < r.H + r.G;
+    const int g = head - r.H - (is_k ? 0 : r.G);
+    dst = (is_k ? r.kc : r.vc) + (((size_t)b * r.G + g) * r.cache_seq + p) * r.D + e;
+  }
+  uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) d4[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+}
+
 template <int EPI>
 __device__ __forceinline__ float epilogue_chunk32(float (&v)[32], const GemmArgs &a, int m, int n) {
-  if constexpr (EPI == EPI_STORE_ROWSCALE || EPI == EPI_SWIGLU_ROWSCALE) {
+  if constexpr (EPI == EPI_STORE_ROWSCALE || EPI == EPI_SWIGLU_ROWSCALE || EPI == EPI_QKV_ROPE) {
     // RMSNorm of A's row m, applied to the GEMM result (the gain is folded into W)
     const float r = m < a.M ? rsqrtf(a.ss_in[m] * a.inv_d + a.eps) : 0.f;
 #pragma unroll
@@ -162,6 +199,9 @@ __device__ __forceinline__ float epilogue_chunk32(float (&v)[32], const GemmArgs
       *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
       *reinterpret_cast<uint4 *>(dst + 8) = make_uint4(w[4], w[5], w[6], w[7]);
     }
+    return 0.f;
+  } else if constexpr (EPI == EPI_QKV_ROPE) {
+    qkv_rope_chunk32(v, a, m, n);
     return 0.f;
   } else if constexpr (EPI == EPI_STORE_ROWSCALE) {
     epilogue_chunk16<EPI_STORE>(v, a, m, n);
@@ -439,6 +479,7 @@ cudaError_t launch_cfg(const bf16 *A, const bf16 *W, GemmArgs args, cudaStream_t
     if (e != cudaSuccess) return e;
   }
   const int grid = units < sm_count() ? units : sm_count();
+  count_launch();
   gemm_tc_kernel<EPI, BN><<<grid, NUM_THREADS, G::SMEM_BYTES, st>>>(ma, mb, args);
   return cudaGetLastError();
 }
@@ -532,14 +573,22 @@ size_t gemm_splitk_part_bytes() {
 int gemm_splitk_counter_slots() { return 4 * sm_count() * 4; }
 
 cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C, int M, int N, int K, int epi,
-                           int *status, cudaStream_t st, const GemmWorkspace *ws, const RowNorm *norm) {
+                           int *status, cudaStream_t st, const GemmWorkspace *ws, const RowNorm *norm,
+                           const QkvScatter *scatter) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   if (K <= 0 || (K & 7) != 0) return cudaErrorInvalidValue;
   if ((epi == EPI_SWIGLU || epi == EPI_SWIGLU_ROWSCALE) && (N & 31) != 0) return cudaErrorInvalidValue;
-  const bool needs_norm = epi == EPI_STORE_ROWSCALE || epi == EPI_SWIGLU_ROWSCALE || epi == EPI_RESIDUAL_SQSUM;
+  const bool needs_norm = epi == EPI_STORE_ROWSCALE || epi == EPI_SWIGLU_ROWSCALE || epi == EPI_RESIDUAL_SQSUM ||
+                          epi == EPI_QKV_ROPE;
   if (needs_norm && norm == nullptr) return cudaErrorInvalidValue;
+  if (epi == EPI_QKV_ROPE) {
+    if (scatter == nullptr || scatter->D <= 0 || (scatter->D & 31) != 0 || scatter->S <= 0 ||
+        N != (scatter->H + 2 * scatter->G) * scatter->D || M % scatter->S != 0)
+      return cudaErrorInvalidValue;
+  }
   const GemmPlan plan = plan_gemm(M, N, K, ws != nullptr ? ws->part_bytes : 0, ws != nullptr ? ws->counter_slots : 0);
-  GemmArgs args{R, C, M, N, K, status, 1, (K + BK - 1) / BK, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f};
+  GemmArgs args{R, C, M, N, K, status, 1, (K + BK - 1) / BK, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f, {}};
+  if (scatter != nullptr) args.qkv = *scatter;
   if (norm != nullptr) {
     args.ss_in = norm->ss_in;
     args.ss_out = norm->ss_out;
@@ -560,6 +609,7 @@ cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C,
     case EPI_STORE_ROWSCALE: return launch_epi<EPI_STORE_ROWSCALE>(A, W, args, plan.bn, st);
     case EPI_SWIGLU_ROWSCALE: return launch_epi<EPI_SWIGLU_ROWSCALE>(A, W, args, plan.bn, st);
     case EPI_RESIDUAL_SQSUM: return launch_epi<EPI_RESIDUAL_SQSUM>(A, W, args, plan.bn, st);
+    case EPI_QKV_ROPE: return launch_epi<EPI_QKV_ROPE>(A, W, args, plan.bn, st);
   }
   return cudaErrorInvalidValue;
 }
@@ -568,6 +618,7 @@ cudaError_t launch_interleave_rows(const bf16 *gate, const bf16 *up, bf16 *out, 
   if ((F & 15) != 0 || (d & 7) != 0) return cudaErrorInvalidValue;
   const int vpr = d / 8;
   const size_t total = (size_t)2 * F * vpr;
+  count_launch();
   interleave_rows_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(
       reinterpret_cast<const uint4 *>(gate), reinterpret_cast<const uint4 *>(up), reinterpret_cast<uint4 *>(out), F,
       vpr);

@@ -19,6 +19,9 @@ enum Epilogue : int {
   EPI_SWIGLU_ROWSCALE = 5,  // C = SiLU(r_m A W1^T) * (r_m A W3^T)
   // residual add that also accumulates ss_out[m] += sum_n C[m,n]^2 of the stored bf16 C
   EPI_RESIDUAL_SQSUM = 6,
+  // QKV projection with the attention RMSNorm row scale, RoPE on the q and k
+  // columns and the scatter of rotated q into q_out and of k / v into the cache
+  EPI_QKV_ROPE = 7,
 };
 
 // ss[t] = sum_j x[t][j]^2 (fp32) for rows of width d.

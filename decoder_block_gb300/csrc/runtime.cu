@@ -15,7 +15,10 @@
 // [Wq; Wk; Wv] and [W_gate; W_up] at create time, a row-statistics pass (step 1)
 // and the O-projection epilogue (step 5) produce sum(x^2) and sum(h^2) per row,
 // and the QKV and gate/up epilogues scale each row by rsqrt(mean + eps).  The
-// fp32 path keeps the standalone steps.
+// QKV epilogue also applies RoPE and writes k and v into the cache (step 3 in
+// the same kernel as step 2, for d_head % 32 == 0).  The fp32 path keeps the
+// standalone steps.
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -33,6 +36,9 @@ thread_local const char *t_last_cuda_error = "no error";
 
 namespace llama {
 void note_cuda_error(cudaError_t e) { t_last_cuda_error = cudaGetErrorString(e); }
+
+std::atomic<unsigned long long> g_kernel_launches{0};
+void count_launch() { g_kernel_launches.fetch_add(1, std::memory_order_relaxed); }
 }  // namespace llama
 
 namespace {
@@ -211,7 +217,8 @@ llama_status alloc_workspace(const Dims &dm, int max_tokens, bool staging, Alloc
     ws->xn = al.alloc(T * dm.d * e);
     ws->hn = al.alloc(T * dm.d * e);
   }
-  ws->qkv = al.alloc(T * dm.QKV * e);
+  if (dm.dtype != LLAMA_BF16 || dm.D % 32 != 0)  // unrotated qkv (the bf16 path rotates in the GEMM epilogue)
+    ws->qkv = al.alloc(T * dm.QKV * e);
   ws->q = al.alloc(T * dm.H * dm.D * e);
   ws->o = al.alloc(T * dm.H * dm.D * e);
   ws->h = al.alloc(T * dm.d * e);
@@ -281,13 +288,34 @@ llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, c
   norm_x.ss_in = ws.ss_x;
   norm_x.eps = dm.eps;
   norm_x.d = dm.d;
-  pf.mark(1, 0, st);
-  LAUNCH(launch_gemm_tc(x, (const bf16 *)w.wqkv, nullptr, qkv, M, dm.QKV, dm.d, EPI_STORE_ROWSCALE, status, st,
-                        &ws.gemm, &norm_x));
-  pf.mark(1, 1, st);
-  pf.mark(2, 0, st);
-  LAUNCH(launch_rope_kv<bf16>(qkv, q, kc, vc, rope, B, S, start_pos, dm.H, dm.G, dm.D, kv->max_seq_len, st));
-  pf.mark(2, 1, st);
+  if (dm.D % 32 == 0) {
+    // QKV projection, RoPE and the cache write in one GEMM epilogue
+    QkvScatter sc;
+    sc.table = rope;
+    sc.q = q;
+    sc.kc = kc;
+    sc.vc = vc;
+    sc.S = S;
+    sc.start_pos = start_pos;
+    sc.H = dm.H;
+    sc.G = dm.G;
+    sc.D = dm.D;
+    sc.cache_seq = kv->max_seq_len;
+    pf.mark(1, 0, st);
+    LAUNCH(launch_gemm_tc(x, (const bf16 *)w.wqkv, nullptr, nullptr, M, dm.QKV, dm.d, EPI_QKV_ROPE, status, st,
+                          &ws.gemm, &norm_x, &sc));
+    pf.mark(1, 1, st);
+    pf.mark(2, 0, st);  // RoPE + KV write: fused into the QKV epilogue
+    pf.mark(2, 1, st);
+  } else {
+    pf.mark(1, 0, st);
+    LAUNCH(launch_gemm_tc(x, (const bf16 *)w.wqkv, nullptr, qkv, M, dm.QKV, dm.d, EPI_STORE_ROWSCALE, status, st,
+                          &ws.gemm, &norm_x));
+    pf.mark(1, 1, st);
+    pf.mark(2, 0, st);
+    LAUNCH(launch_rope_kv<bf16>(qkv, q, kc, vc, rope, B, S, start_pos, dm.H, dm.G, dm.D, kv->max_seq_len, st));
+    pf.mark(2, 1, st);
+  }
   pf.mark(3, 0, st);
   LAUNCH(launch_attention(q, kc, vc, o, B, S, start_pos, dm.H, dm.G, dm.D, kv->max_seq_len, ws.attn, status, st));
   pf.mark(3, 1, st);
@@ -629,6 +657,10 @@ int32_t llama_ffn_hidden_dim(int32_t d_model, int32_t multiple_of, float ffn_dim
 }
 
 const char *llama_last_cuda_error(void) { return t_last_cuda_error; }
+
+unsigned long long llama_kernel_launch_count(void) {
+  return llama::g_kernel_launches.load(std::memory_order_relaxed);
+}
 
 const char *llama_status_string(llama_status s) {
   switch (s) {

@@ -91,6 +91,7 @@ cudaError_t launch_rmsnorm(const T *x, const T *g, T *out, int rows, int d, floa
   const int blocks = (int)(((size_t)rows * 32 + threads - 1) / threads);
   const int nv = d / Vec16<T>::N;
   const int per_lane = (nv + 31) / 32;
+  count_launch();
   switch (per_lane) {
     case 1: rmsnorm_reg_kernel<T, 1><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
     case 2: rmsnorm_reg_kernel<T, 2><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
@@ -130,6 +131,7 @@ __global__ void __launch_bounds__(256) row_sqsum_kernel(const bf16 *__restrict__
 
 cudaError_t launch_row_sqsum(const bf16 *x, float *ss, int rows, int d, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
+  count_launch();
   row_sqsum_kernel<<<(unsigned)(((size_t)rows * 32 + 255) / 256), 256, 0, st>>>(x, ss, rows, d);
   return cudaGetLastError();
 }
@@ -144,6 +146,7 @@ __global__ void scale_columns_kernel(bf16 *__restrict__ W, const bf16 *__restric
 cudaError_t launch_scale_columns(bf16 *W, const bf16 *g, int rows, int cols, cudaStream_t st) {
   const size_t n = (size_t)rows * cols;
   if (n == 0) return cudaSuccess;
+  count_launch();
   scale_columns_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(W, g, rows, cols);
   return cudaGetLastError();
 }
@@ -225,6 +228,7 @@ cudaError_t launch_gemm_simt(const T *A, const T *W, const T *W3, const T *R, vo
                              int epi, cudaStream_t st) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   dim3 grid((N + SG_BN - 1) / SG_BN, (M + SG_BM - 1) / SG_BM);
+  count_launch();
   switch (epi) {
     case EPI_STORE: gemm_simt_kernel<T, EPI_STORE><<<grid, 256, 0, st>>>(A, W, W3, R, C, M, N, K); break;
     case EPI_RESIDUAL: gemm_simt_kernel<T, EPI_RESIDUAL><<<grid, 256, 0, st>>>(A, W, W3, R, C, M, N, K); break;
@@ -253,6 +257,7 @@ __global__ void rope_table_kernel(float2 *table, int max_seq, int D, double thet
 cudaError_t launch_rope_table(float2 *table, int max_seq, int D, double theta, cudaStream_t st) {
   const size_t n = (size_t)max_seq * (D / 2);
   const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  count_launch();
   rope_table_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(table, max_seq, D, theta);
   return cudaGetLastError();
 }
@@ -306,6 +311,7 @@ cudaError_t launch_rope_kv(const T *qkv, T *q_out, T *kc, T *vc, const float2 *t
   const size_t total = (size_t)B * S * ((H + 2 * G) * D / V);
   if (total == 0) return cudaSuccess;
   const int threads = 256;
+  count_launch();
   rope_kv_kernel<T><<<(unsigned)((total + threads - 1) / threads), threads, 0, st>>>(
       qkv, q_out, kc, vc, table, B * S, S, start_pos, H, G, D, cache_seq);
   return cudaGetLastError();
@@ -371,6 +377,7 @@ cudaError_t launch_attention_simt(const T *q, const T *kc, const T *vc, T *o, in
   if (warps == 0) return cudaSuccess;
   const int threads = 256;
   const unsigned blocks = (unsigned)((warps * 32 + threads - 1) / threads);
+  count_launch();
   attention_simt_kernel<T><<<blocks, threads, 0, st>>>(q, kc, vc, o, B * S, S, start_pos, H, G, D, cache_seq,
                                                        1.0f / sqrtf((float)D));
   return cudaGetLastError();
@@ -403,6 +410,7 @@ cudaError_t launch_embed(const int32_t *tokens, const T *E, T *x, int ntok, int 
   constexpr int V = Vec16<T>::N;
   const size_t total = (size_t)ntok * (d / V);
   if (total == 0) return cudaSuccess;
+  count_launch();
   embed_kernel<T><<<(unsigned)((total + 255) / 256), 256, 0, st>>>(tokens, E, x, ntok, d, vocab, status);
   return cudaGetLastError();
 }

@@ -45,11 +45,23 @@ struct RowNorm {
   int d = 1;
 };
 
+// EPI_QKV_ROPE destinations: GEMM row m is token (b, s) = (m / S, m % S) at
+// position p = start_pos + s; output columns [0, H D) are q, [H D, (H+G) D) k
+// and [(H+G) D, (H+2G) D) v.  q and k pairs (2i, 2i+1) of each head are
+// rotated by table[p][i] = {cos, sin}; rotated q goes to q [T][H D], rotated k
+// and v to kc / vc [batch][G][cache_seq][D].  Needs D % 32 == 0.
+struct QkvScatter {
+  const float2 *table = nullptr;
+  bf16 *q = nullptr, *kc = nullptr, *vc = nullptr;
+  int S = 1, start_pos = 0, H = 0, G = 0, D = 0, cache_seq = 0;
+};
+
 // status: device status word for bounded-wait expiry (may be null).
-// ws: split-K scratch (null: never split).  norm: required by the ROWSCALE and SQSUM epilogues.
+// ws: split-K scratch (null: never split).  norm: required by the ROWSCALE, SQSUM
+// and QKV_ROPE epilogues; scatter: required by EPI_QKV_ROPE (C unused there).
 cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C, int M, int N, int K, int epi,
                            int *status, cudaStream_t st, const GemmWorkspace *ws = nullptr,
-                           const RowNorm *norm = nullptr);
+                           const RowNorm *norm = nullptr, const QkvScatter *scatter = nullptr);
 
 // out[32j + i] = gate[16j + i], out[32j + 16 + i] = up[16j + i] (rows of width d), F % 16 == 0.
 cudaError_t launch_interleave_rows(const bf16 *gate, const bf16 *up, bf16 *out, int F, int d, cudaStream_t st);

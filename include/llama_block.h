@@ -156,6 +156,12 @@ const char *llama_status_string(llama_status s);
  * valid until the next failing call in the same thread. */
 const char *llama_last_cuda_error(void);
 
+/* Number of CUDA kernels this library has launched since it was loaded, all
+ * threads and handles together (tracing).  A launch captured into a CUDA graph
+ * counts once, at capture; graph replays do not count.  Memsets are not kernels
+ * of this library and are not counted. */
+unsigned long long llama_kernel_launch_count(void);
+
 /* Per-step timing of llama_block_forward (tracing).  When enabled, every
  * forward call records a CUDA event pair on its stream around each step's
  * kernel launch, for up to max_forwards calls (events are created here;

@@ -188,3 +188,23 @@ def test_forward_rejects_bad_calls_on_device(lb):
         assert blk.forward(xh, y, 1, 8, 0, kc, vc) == lb.LLAMA_ERR_INVALID_ARG
         t.cuda.synchronize()
         assert lb.llama_block_device_status(blk.h) == lb.LLAMA_OK
+
+
+def test_kernel_launch_count_per_forward(lb):
+    """The bf16 path runs six kernels per prefill forward (row statistics, QKV+RoPE+cache, attention, O, gate/up,
+    down) and seven per D=128 decode forward (the split-KV combine); the counter sees every one."""
+    t = torch()
+    for shape, B, S, start_pos, L, want in [
+            (dict(synth.SHAPES["smollm2_135m"], max_seq_len=64), 2, 64, 0, 64, 6),
+            (dict(synth.SHAPES["llama3_8b_decode_b64"], max_seq_len=600), 4, 1, 520, 600, 7)]:
+        w = synth.block_weights(shape)
+        with GpuBlock(shape, w, B * S, max_seq_len=L) as blk:
+            G, D = shape["n_kv_heads"], shape["d_model"] // shape["n_heads"]
+            kc = t.zeros((B, G, L, D), dtype=t.bfloat16, device="cuda")
+            vc = t.zeros_like(kc)
+            x = t.zeros((B, S, shape["d_model"]), dtype=t.bfloat16, device="cuda")
+            y = t.empty_like(x)
+            n0 = lb.llama_kernel_launch_count()
+            lb.check(blk.forward(x, y, B, S, start_pos, kc, vc))
+            assert lb.llama_kernel_launch_count() - n0 == want
+            t.cuda.synchronize()
