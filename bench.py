@@ -232,6 +232,8 @@ def main():
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the secondary block shapes (SmolLM2-shaped block, 8B prefill B=4 S=2048)")
     ap.add_argument("--no-stack", action="store_true", help="skip the 32-layer stack measurement")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time only the decode step (B=64 at start_pos 4095); for profiler captures")
     ap.add_argument("--seq", type=int, default=8192,
                     help="prefill length S (default 8192; smaller values are for profiler captures)")
     args = ap.parse_args()
@@ -262,6 +264,14 @@ def main():
     w = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(dev) for k, v in w_np.items()}
     B, S, d = SHAPE["B"], SHAPE["S"], SHAPE["d_model"]
     G, D = SHAPE["n_kv_heads"], d // SHAPE["n_heads"]
+    if args.decode_only:
+        decode = bench_decode(lb, torch, w, dev, stream, args, measured_peaks()[0])
+        if rank == 0:
+            print(json.dumps({"metric": "decode block step µs (B=64 at start_pos 4095)", "value": decode["us_per_step"],
+                              "unit": "us/step", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                              "higher_is_better": False, "dtype": "bf16", "data": "synthetic",
+                              "config": {"workload": decode["workload"]}, "decode": decode}), flush=True)
+        return 0
     x_np = synth.block_activations(SHAPE)
     x = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).to(dev)
     y = torch.empty_like(x)
@@ -499,15 +509,49 @@ def bench_stack(lb, torch, dev, stream, args, n_layers=32, vocab=128256, S=8192)
     n_launched = lb.llama_kernel_launch_count() - n0
     torch.cuda.synchronize()
     status = lb.llama_stack_device_status(stk)
-    lb.llama_stack_destroy(stk)
     ok = bool(torch.isfinite(logits).all().item())
     ms = e0.elapsed_time(e1) / steps
     lin, att = block_flops(dict(s, S=S))
     total = n_layers * (lin + att) + 2.0 * S * d * vocab
+    del caches, kvs, logits
+    torch.cuda.empty_cache()
+    gen = bench_generate(lb, torch, dev, stream, stk, n_layers, vocab, g)
+    lb.llama_stack_destroy(stk)
     return {"workload": "llama3_8b_stack_32l_prefill_b1s8192_vocab128256", "ms_per_step": ms,
             "tokens_per_s": S / (ms / 1e3), "tflops": total / (ms / 1e3) / 1e12, "steps": steps,
             "logits_finite": ok, "device_status": status,
-            "gpu_launches": n_launched}
+            "gpu_launches": n_launched, "generate": gen}
+
+
+def bench_generate(lb, torch, dev, stream, stk, n_layers, vocab, g, B=64, start_pos=4064, n_new=32, L=4096):
+    """Greedy decoding through the 32-layer stack: B sequences, a one-token prompt at start_pos over caches
+    pre-filled with N(0,1) values, n_new tokens chosen on the device (no host round trip per token)."""
+    s = SHAPE
+    G, D = s["n_kv_heads"], s["d_model"] // s["n_heads"]
+    caches = [(torch.randn((B, G, L, D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16),
+               torch.randn((B, G, L, D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16))
+              for _ in range(n_layers)]
+    kvs = [lb.make_kv_cache(k, v, B, L) for k, v in caches]
+    prompt = torch.randint(0, vocab, (B, 1), generator=g, device=dev, dtype=torch.int32)
+    out = torch.empty((B, n_new), dtype=torch.int32, device=dev)
+    logits = torch.empty((B, vocab), dtype=torch.float32, device=dev)
+    lb.check(lb.llama_stack_generate(stk, prompt, B, 1, start_pos, n_new, kvs, out, logits, stream))
+    torch.cuda.synchronize()
+    steps = 3
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = lb.llama_kernel_launch_count()
+    e0.record(stream)
+    for _ in range(steps):
+        lb.check(lb.llama_stack_generate(stk, prompt, B, 1, start_pos, n_new, kvs, out, logits, stream))
+    e1.record(stream)
+    n_launched = lb.llama_kernel_launch_count() - n0
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    ids = out.cpu()
+    return {"workload": f"llama3_8b_stack_32l_greedy_b{B}_pos{start_pos}_new{n_new}_vocab{vocab}",
+            "ms_per_call": ms, "ms_per_token_step": ms / n_new, "tokens_per_s": B * n_new / (ms / 1e3),
+            "ids_in_range": bool(((ids >= 0) & (ids < vocab)).all().item()), "steps": steps,
+            "device_status": lb.llama_stack_device_status(stk), "gpu_launches": n_launched}
 
 
 def bench_decode(lb, torch, w, dev, stream, args, peaks):

@@ -79,6 +79,8 @@ def load() -> ctypes.CDLL:
         "llama_block_device_status": (st, [c_void_p]),
         "llama_stack_create": (st, [POINTER(llama_config), c_int32, c_int32, c_void_p, POINTER(llama_block_weights),
                                     c_void_p, c_void_p, c_int32, POINTER(c_void_p)]),
+        "llama_stack_generate": (st, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
+                                      POINTER(llama_kv_cache), c_void_p, c_void_p, c_void_p]),
         "llama_stack_forward": (st, [c_void_p, c_void_p, c_int32, c_int32, c_int32, POINTER(llama_kv_cache),
                                      c_void_p, c_void_p]),
         "llama_stack_destroy": (None, [c_void_p]),
@@ -178,6 +180,13 @@ def llama_stack_create(cfg: llama_config, n_layers, vocab, embed, layers, final_
 def llama_stack_forward(stk, tokens, B, S, start_pos, kv_list, logits, stream=None) -> int:
     arr = (llama_kv_cache * max(len(kv_list), 1))(*kv_list)
     return load().llama_stack_forward(stk, _p(tokens), B, S, start_pos, arr, _p(logits), _stream(stream))
+
+
+def llama_stack_generate(stk, prompt, B, S_prompt, start_pos, n_new, kv_list, out_tokens, logits,
+                         stream=None) -> int:
+    arr = (llama_kv_cache * max(len(kv_list), 1))(*kv_list)
+    return load().llama_stack_generate(stk, _p(prompt), B, S_prompt, start_pos, n_new, arr, _p(out_tokens),
+                                       _p(logits), _stream(stream))
 
 
 def llama_stack_destroy(stk) -> None:

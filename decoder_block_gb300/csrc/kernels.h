@@ -59,4 +59,13 @@ template <typename T>
 cudaError_t launch_embed(const int32_t *tokens, const T *E, T *x, int ntok, int d, int vocab, int *status,
                          cudaStream_t st);
 
+// Greedy pick: out[r * out_stride] (and next[r], when not null) = arg-max of
+// logits row r [rows][vocab] fp32, lowest id among equal maxima.
+cudaError_t launch_argmax_rows(const float *logits, int rows, int vocab, int32_t *out, int out_stride, int32_t *next,
+                               cudaStream_t st);
+
+// out[b] = x[b][S - 1] (rows of width d; d % (16 / sizeof(T)) == 0).
+template <typename T>
+cudaError_t launch_gather_last_rows(const T *x, T *out, int B, int S, int d, cudaStream_t st);
+
 }  // namespace llama

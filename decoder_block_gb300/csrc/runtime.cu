@@ -398,6 +398,7 @@ struct llama_stack {
   int *status = nullptr;
   void *embed = nullptr, *final_norm = nullptr, *lm_head = nullptr;
   void *x0 = nullptr, *x1 = nullptr, *xn = nullptr;
+  int32_t *next_tok = nullptr;  // greedy decoding: the ids fed to the next step [max_tokens]
 };
 
 extern "C" {
@@ -563,6 +564,7 @@ llama_status llama_stack_create(const llama_config *cfg, int32_t n_layers, int32
     k->x0 = k->al.alloc((size_t)max_tokens * dm.d * e);
     k->x1 = k->al.alloc((size_t)max_tokens * dm.d * e);
     k->xn = k->al.alloc((size_t)max_tokens * dm.d * e);
+    k->next_tok = (int32_t *)k->al.alloc((size_t)max_tokens * sizeof(int32_t));
     k->rope = (float2 *)k->al.alloc((size_t)dm.max_seq * (dm.D / 2) * sizeof(float2));
     k->status = (int *)k->al.alloc(sizeof(int));
     if (k->al.failed) s = LLAMA_ERR_OOM;
@@ -585,6 +587,54 @@ llama_status llama_stack_create(const llama_config *cfg, int32_t n_layers, int32
   return LLAMA_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Embedding gather and the N blocks; returns the buffer holding the last
+// block's output [B*S][d] in *hidden.
+llama_status stack_layers(llama_stack *stk, const int32_t *tokens, int B, int S, int start_pos,
+                          const llama_kv_cache *kv, cudaStream_t st, void **hidden) {
+  const Dims &dm = stk->dm;
+  const int M = B * S;
+  void *cur = stk->x0, *nxt = stk->x1;
+  if (dm.dtype == LLAMA_BF16)
+    LAUNCH(launch_embed<bf16>(tokens, (const bf16 *)stk->embed, (bf16 *)cur, M, dm.d, stk->vocab, stk->status, st));
+  else
+    LAUNCH(launch_embed<float>(tokens, (const float *)stk->embed, (float *)cur, M, dm.d, stk->vocab, stk->status, st));
+  for (int l = 0; l < stk->n_layers; ++l) {
+    llama_status s =
+        forward_any(dm, stk->layers[l], stk->ws, stk->rope, cur, nxt, B, S, start_pos, &kv[l], stk->status, st);
+    if (s != LLAMA_OK) return s;
+    void *t = cur;
+    cur = nxt;
+    nxt = t;
+  }
+  *hidden = cur;
+  return LLAMA_OK;
+}
+
+// Final RMSNorm and the LM head over `rows` rows of `hidden`: logits [rows][vocab] fp32.
+llama_status stack_head(llama_stack *stk, const void *hidden, int rows, float *logits, cudaStream_t st) {
+  const Dims &dm = stk->dm;
+  if (dm.dtype == LLAMA_BF16) {
+    LAUNCH(launch_rmsnorm<bf16>((const bf16 *)hidden, (const bf16 *)stk->final_norm, (bf16 *)stk->xn, rows, dm.d,
+                                dm.eps, st));
+    LAUNCH(launch_gemm_tc((const bf16 *)stk->xn, (const bf16 *)stk->lm_head, nullptr, logits, rows, stk->vocab, dm.d,
+                          EPI_F32OUT, stk->status, st, &stk->ws.gemm));
+  } else {
+    LAUNCH(launch_rmsnorm<float>((const float *)hidden, (const float *)stk->final_norm, (float *)stk->xn, rows, dm.d,
+                                 dm.eps, st));
+    LAUNCH(launch_gemm_simt<float>((const float *)stk->xn, (const float *)stk->lm_head, nullptr, nullptr, logits,
+                                   rows, stk->vocab, dm.d, EPI_F32OUT, st));
+  }
+  return LLAMA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 llama_status llama_stack_forward(llama_stack *stk, const int32_t *tokens, int32_t B, int32_t S, int32_t start_pos,
                                  const llama_kv_cache *kv, float *logits, llama_stream stream) {
   if (stk == nullptr || (kv == nullptr && stk->n_layers > 0)) return LLAMA_ERR_INVALID_ARG;
@@ -597,30 +647,51 @@ llama_status llama_stack_forward(llama_stack *stk, const int32_t *tokens, int32_
     s = validate_call(stk->dm, stk->ws.max_tokens, B, S, start_pos, &kv[l]);
     if (s != LLAMA_OK) return s;
   }
+  cudaStream_t st = (cudaStream_t)stream;
+  void *hidden = nullptr;
+  s = stack_layers(stk, tokens, B, S, start_pos, kv, st, &hidden);
+  if (s != LLAMA_OK) return s;
+  return stack_head(stk, hidden, B * S, logits, st);
+}
+
+llama_status llama_stack_generate(llama_stack *stk, const int32_t *prompt, int32_t B, int32_t S_prompt,
+                                  int32_t start_pos, int32_t n_new, const llama_kv_cache *kv, int32_t *out_tokens,
+                                  float *logits, llama_stream stream) {
+  if (stk == nullptr || (kv == nullptr && stk->n_layers > 0)) return LLAMA_ERR_INVALID_ARG;
+  llama_status s = check_ptr(prompt);
+  if (s == LLAMA_OK) s = check_ptr(out_tokens);
+  if (s == LLAMA_OK) s = check_ptr(logits);
+  if (s != LLAMA_OK) return s;
+  if (B <= 0 || S_prompt <= 0 || start_pos < 0 || n_new <= 0) return LLAMA_ERR_INVALID_ARG;
+  // positions start_pos .. start_pos + S_prompt + n_new - 2 are run (the last pick is not fed back)
+  const long long last_pos = (long long)start_pos + S_prompt + n_new - 2;
+  if ((long long)B * S_prompt > stk->ws.max_tokens || last_pos + 1 > stk->dm.max_seq) return LLAMA_ERR_RANGE;
+  for (int l = 0; l < stk->n_layers; ++l) {
+    s = validate_call(stk->dm, stk->ws.max_tokens, B, S_prompt, start_pos, &kv[l]);
+    if (s == LLAMA_OK && last_pos + 1 > kv[l].max_seq_len) s = LLAMA_ERR_RANGE;
+    if (s != LLAMA_OK) return s;
+  }
   const Dims &dm = stk->dm;
   cudaStream_t st = (cudaStream_t)stream;
-  const int M = B * S;
-  void *cur = stk->x0, *nxt = stk->x1;
-  if (dm.dtype == LLAMA_BF16)
-    LAUNCH(launch_embed<bf16>(tokens, (const bf16 *)stk->embed, (bf16 *)cur, M, dm.d, stk->vocab, stk->status, st));
-  else
-    LAUNCH(launch_embed<float>(tokens, (const float *)stk->embed, (float *)cur, M, dm.d, stk->vocab, stk->status, st));
-  for (int l = 0; l < stk->n_layers; ++l) {
-    s = forward_any(dm, stk->layers[l], stk->ws, stk->rope, cur, nxt, B, S, start_pos, &kv[l], stk->status, st);
+  int pos = start_pos;
+  for (int i = 0; i < n_new; ++i) {
+    const int S = i == 0 ? S_prompt : 1;
+    void *hidden = nullptr;
+    s = stack_layers(stk, i == 0 ? prompt : stk->next_tok, B, S, pos, kv, st, &hidden);
     if (s != LLAMA_OK) return s;
-    void *t = cur;
-    cur = nxt;
-    nxt = t;
-  }
-  if (dm.dtype == LLAMA_BF16) {
-    LAUNCH(launch_rmsnorm<bf16>((const bf16 *)cur, (const bf16 *)stk->final_norm, (bf16 *)stk->xn, M, dm.d, dm.eps, st));
-    LAUNCH(launch_gemm_tc((const bf16 *)stk->xn, (const bf16 *)stk->lm_head, nullptr, logits, M, stk->vocab, dm.d,
-                          EPI_F32OUT, stk->status, st, &stk->ws.gemm));
-  } else {
-    LAUNCH(launch_rmsnorm<float>((const float *)cur, (const float *)stk->final_norm, (float *)stk->xn, M, dm.d, dm.eps,
-                                 st));
-    LAUNCH(launch_gemm_simt<float>((const float *)stk->xn, (const float *)stk->lm_head, nullptr, nullptr, logits, M,
-                                   stk->vocab, dm.d, EPI_F32OUT, st));
+    const void *last = hidden;
+    if (S > 1) {  // the last position of each sequence, into the free ping-pong buffer
+      void *dst = hidden == stk->x0 ? stk->x1 : stk->x0;
+      if (dm.dtype == LLAMA_BF16)
+        LAUNCH(launch_gather_last_rows<bf16>((const bf16 *)hidden, (bf16 *)dst, B, S, dm.d, st));
+      else
+        LAUNCH(launch_gather_last_rows<float>((const float *)hidden, (float *)dst, B, S, dm.d, st));
+      last = dst;
+    }
+    s = stack_head(stk, last, B, logits, st);
+    if (s != LLAMA_OK) return s;
+    LAUNCH(launch_argmax_rows(logits, B, stk->vocab, out_tokens + i, n_new, stk->next_tok, st));
+    pos += S;
   }
   return LLAMA_OK;
 }

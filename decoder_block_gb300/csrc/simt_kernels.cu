@@ -415,6 +415,82 @@ cudaError_t launch_embed(const int32_t *tokens, const T *E, T *x, int ntok, int 
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------- greedy decoding ---
+// Row r of the logits picks the id of its maximum; among equal maxima the
+// lowest id wins, and NaN is never picked (a row of NaN gives id 0).
+__device__ __forceinline__ void argmax_merge(float &v, int &i, float ov, int oi) {
+  if (ov > v || (ov == v && oi < i)) {
+    v = ov;
+    i = oi;
+  }
+}
+
+__global__ void argmax_rows_kernel(const float *__restrict__ logits, int vocab, int32_t *__restrict__ out,
+                                   int out_stride, int32_t *__restrict__ next) {
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  const float *l = logits + (size_t)blockIdx.x * vocab;
+  float best = -INFINITY;
+  int bi = INT_MAX;
+  for (int j = threadIdx.x; j < vocab; j += blockDim.x) argmax_merge(best, bi, __ldcs(l + j), j);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    argmax_merge(best, bi, ov, oi);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  if (lane == 0) {
+    sv[warp] = best;
+    si[warp] = bi;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    best = lane < nwarps ? sv[lane] : -INFINITY;
+    bi = lane < nwarps ? si[lane] : INT_MAX;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      argmax_merge(best, bi, ov, oi);
+    }
+    if (lane == 0) {
+      const int id = bi == INT_MAX ? 0 : bi;
+      out[(size_t)blockIdx.x * out_stride] = id;
+      if (next != nullptr) next[blockIdx.x] = id;
+    }
+  }
+}
+
+cudaError_t launch_argmax_rows(const float *logits, int rows, int vocab, int32_t *out, int out_stride, int32_t *next,
+                               cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  count_launch();
+  argmax_rows_kernel<<<rows, 1024, 0, st>>>(logits, vocab, out, out_stride, next);
+  return cudaGetLastError();
+}
+
+// out[b] = x[b][S - 1] for rows of width d (the last position of each sequence).
+template <typename T>
+__global__ void gather_last_rows_kernel(const T *__restrict__ x, T *__restrict__ out, int B, int S, int d) {
+  constexpr int V = Vec16<T>::N;
+  const int nv = d / V;
+  const size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  if (idx >= (size_t)B * nv) return;
+  const int b = (int)(idx / nv), c = (int)(idx % nv) * V;
+  store16(out + (size_t)b * d + c, load16(x + ((size_t)b * S + S - 1) * d + c));
+}
+
+template <typename T>
+cudaError_t launch_gather_last_rows(const T *x, T *out, int B, int S, int d, cudaStream_t st) {
+  constexpr int V = Vec16<T>::N;
+  const size_t total = (size_t)B * (d / V);
+  if (total == 0) return cudaSuccess;
+  count_launch();
+  gather_last_rows_kernel<T><<<(unsigned)((total + 255) / 256), 256, 0, st>>>(x, out, B, S, d);
+  return cudaGetLastError();
+}
+
 #define INSTANTIATE(T)                                                                                            \
   template cudaError_t launch_rmsnorm<T>(const T *, const T *, T *, int, int, float, cudaStream_t);               \
   template cudaError_t launch_gemm_simt<T>(const T *, const T *, const T *, const T *, void *, int, int, int, int, \
@@ -423,7 +499,8 @@ cudaError_t launch_embed(const int32_t *tokens, const T *E, T *x, int ntok, int 
                                          int, cudaStream_t);                                                      \
   template cudaError_t launch_attention_simt<T>(const T *, const T *, const T *, T *, int, int, int, int, int,    \
                                                 int, int, cudaStream_t);                                          \
-  template cudaError_t launch_embed<T>(const int32_t *, const T *, T *, int, int, int, int *, cudaStream_t);
+  template cudaError_t launch_embed<T>(const int32_t *, const T *, T *, int, int, int, int *, cudaStream_t);    \
+  template cudaError_t launch_gather_last_rows<T>(const T *, T *, int, int, int, cudaStream_t);
 
 INSTANTIATE(float)
 INSTANTIATE(bf16)

@@ -136,6 +136,28 @@ llama_status llama_stack_forward(llama_stack *stk, const int32_t *tokens, int32_
                                  int32_t start_pos, const llama_kv_cache *kv, float *logits,
                                  llama_stream stream);
 
+/* Greedy decoding ("Full Llama 3 transformer block", How it works: the prompt
+ * fills the cache at start_pos, then one new token per step at the next
+ * position; "The Evolving Transformer 04 · LLaMA", §07 Assemble: the last
+ * position's logits choose the next token).
+ *   prompt     int32 [B][S_prompt] in [0, vocab) (device), run at start_pos;
+ *   n_new      tokens to choose; each is the arg-max of the logits of the
+ *              previous position (lowest id among equal maxima) and, except
+ *              the last, is run as a one-token step at the next position;
+ *   out_tokens int32 [B][n_new] (device), the chosen ids;
+ *   logits     fp32 [B][vocab] (device), scratch; holds the logits that chose
+ *              out_tokens[:, n_new - 1] on return;
+ *   kv         n_layers caches; positions start_pos .. start_pos + S_prompt +
+ *              n_new - 2 are written.
+ * Range: B * S_prompt <= max_tokens, B <= kv.max_batch and start_pos +
+ * S_prompt + n_new - 1 <= min(cfg.max_seq_len, kv.max_seq_len), else
+ * LLAMA_ERR_RANGE.  Enqueues the whole loop on stream (no host sync): per
+ * token the embedding gather, n_layers blocks, the final norm, the LM head and
+ * the arg-max. */
+llama_status llama_stack_generate(llama_stack *stk, const int32_t *prompt, int32_t B, int32_t S_prompt,
+                                  int32_t start_pos, int32_t n_new, const llama_kv_cache *kv,
+                                  int32_t *out_tokens, float *logits, llama_stream stream);
+
 void llama_stack_destroy(llama_stack *stk);
 
 /* Bytes of one layer's K plus V cache for max_batch x max_seq_len positions:

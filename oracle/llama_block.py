@@ -43,7 +43,7 @@ import numpy as np
 
 __all__ = [
     "rms_norm", "rope_frequencies", "rope", "silu", "linear", "gqa_attention",
-    "gqa_attention_rows", "block_forward", "block_forward_rows", "stack_forward",
+    "gqa_attention_rows", "block_forward", "block_forward_rows", "stack_forward", "greedy_generate",
     "ffn_hidden_dim", "kv_values_per_token", "block_param_count", "model_param_count",
 ]
 
@@ -272,6 +272,34 @@ def stack_forward(cfg: dict, layers, embed, final_norm, lm_head, tokens, start_p
         new_caches.append((kc2, vc2))
     n = rms_norm(x, final_norm, cfg["norm_eps"])
     return linear(n, lm_head), new_caches
+
+
+def greedy_generate(cfg: dict, layers, embed, final_norm, lm_head, prompt, start_pos: int, caches, n_new: int):
+    """Greedy decoding through the stack with the KV cache.
+
+    The prompt (int [B, S]) runs through the stack at start_pos, filling every
+    layer's cache; the next token of each sequence is the arg-max of the logits
+    at its last prompt position (the lowest id among equal maxima); that token
+    is then run as a one-token step at the next position, and so on, n_new
+    tokens in all.  [L3B] How it works (the cache-backed forward at start_pos,
+    one new token per step once the prompt is cached); [EVT] §07 Assemble
+    (logits of the last position choose the next token).
+    Returns (tokens [B, n_new], logits [B, vocab] of the last step, caches).
+    """
+    prompt = np.asarray(prompt)
+    B, S = prompt.shape
+    out = np.zeros((B, n_new), dtype=np.int64)
+    logits, caches = stack_forward(cfg, layers, embed, final_norm, lm_head, prompt, start_pos, caches)
+    last = logits[:, -1]
+    pos = start_pos + S
+    for i in range(n_new):
+        out[:, i] = np.argmax(last, axis=-1)  # first index of the maximum
+        if i + 1 == n_new:
+            break
+        logits, caches = stack_forward(cfg, layers, embed, final_norm, lm_head, out[:, i:i + 1], pos, caches)
+        last = logits[:, -1]
+        pos += 1
+    return out, last, caches
 
 
 # ---------------------------------------------------------------------------

@@ -390,6 +390,91 @@ def test_stack_zero_blocks_is_norm_then_head():
         np.testing.assert_allclose(logits[0, s], head @ n, atol=1e-12)
 
 
+# ------------------------------------------------- greedy generation --------
+
+def _identity_stack(cfg, n_layers, tag):
+    """Blocks whose output projections vanish (y = x) around random attention
+    and FFN weights, so the stack is embedding -> final norm -> head."""
+    layers = []
+    for l in range(n_layers):
+        w = _tiny_weights(cfg, f"{tag}{l}")
+        w["wo"] = np.zeros_like(w["wo"])
+        w["w_down"] = np.zeros_like(w["w_down"])
+        layers.append(w)
+    return layers
+
+
+def _one_hot_model(cfg, vocab, perm, scale=3.0):
+    """One-hot embeddings e_t * scale and head rows head[j] = e_perm[j]: the
+    logits of token t are sqrt(d)-scaled indicators of perm[j] == t, so the
+    next token is the j with perm[j] == t."""
+    d = cfg["d_model"]
+    emb = np.zeros((vocab, d))
+    emb[np.arange(vocab), np.arange(vocab)] = scale
+    head = np.zeros((vocab, d))
+    head[np.arange(vocab), np.asarray(perm)] = 1.0
+    return emb, head
+
+
+def test_greedy_generate_follows_the_closed_form_chain():
+    cfg = TINY
+    vocab, n_new, S, L = 13, 6, 4, 16
+    perm = synth.uniform_int(0, "pins/perm", (vocab,), 1 << 30).argsort()  # a fixed permutation
+    inv = np.argsort(perm)  # token t -> the j with perm[j] == t
+    emb, head = _one_hot_model(cfg, vocab, perm)
+    layers = _identity_stack(cfg, 2, "gg")
+    prompt = np.array([[1, 5, 2, 7], [0, 0, 12, 3]])
+    G, D = cfg["n_kv_heads"], cfg["d_model"] // cfg["n_heads"]
+    caches = [(np.zeros((2, G, L, D)), np.zeros((2, G, L, D))) for _ in layers]
+    toks, last, new = oracle.greedy_generate(cfg, layers, emb, np.ones(cfg["d_model"]), head, prompt, 3, caches, n_new)
+    for b in range(2):
+        t = prompt[b, -1]
+        for i in range(n_new):
+            t = inv[t]
+            assert toks[b, i] == t
+    # the last chosen token is not run: positions 3 .. 3 + S + n_new - 2 are cached, nothing after
+    for kc, vc in new:
+        assert np.all(np.abs(kc[:, :, 3:3 + S + n_new - 1]).sum(-1) > 0)
+        assert np.all(kc[:, :, :3] == 0) and np.all(kc[:, :, 3 + S + n_new - 1:] == 0)
+    # last logits: sqrt(d)-scaled indicator of the chosen token's preimage
+    assert np.all(np.argmax(last, -1) == toks[:, -1])
+
+
+def test_greedy_generate_breaks_ties_towards_the_lowest_id():
+    cfg = TINY
+    vocab = 9
+    emb = _rng("tie_e", (vocab, cfg["d_model"]))
+    layers = _identity_stack(cfg, 1, "tie")
+    G, D = cfg["n_kv_heads"], cfg["d_model"] // cfg["n_heads"]
+    caches = [(np.zeros((1, G, 8, D)), np.zeros((1, G, 8, D)))]
+    toks, _, _ = oracle.greedy_generate(cfg, layers, emb, np.ones(64), np.zeros((vocab, 64)), np.array([[4, 2]]), 0,
+                                        caches, 3)
+    assert toks.tolist() == [[0, 0, 0]]
+    head = np.zeros((vocab, 64))
+    head[[3, 7]] = emb[5]  # rows 3 and 7 tie for token 5's successor
+    toks, _, _ = oracle.greedy_generate(cfg, layers, emb, np.ones(64), head, np.array([[5]]), 0, caches, 1)
+    assert toks.tolist() == [[3]]
+
+
+def test_greedy_generate_equals_teacher_forced_argmax():
+    # incremental decoding with the cache == one-shot forward over prompt + generated tokens
+    cfg = TINY
+    vocab, S, n_new, L = 23, 5, 4, 12
+    layers = [_tiny_weights(cfg, f"tf{l}") for l in range(2)]
+    emb = _rng("tf_e", (vocab, 64))
+    head = _rng("tf_h", (vocab, 64))
+    gfin = _rng("tf_g", (64,), std=0.1, mean=1.0)
+    prompt = synth.uniform_int(0, "pins/tf_prompt", (2, S), vocab)
+    G, D = cfg["n_kv_heads"], 16
+    fresh = lambda: [(np.zeros((2, G, L, D)), np.zeros((2, G, L, D))) for _ in layers]
+    toks, last, _ = oracle.greedy_generate(cfg, layers, emb, gfin, head, prompt, 1, fresh(), n_new)
+    seq = np.concatenate([prompt, toks[:, :-1]], 1)
+    logits, _ = oracle.stack_forward(cfg, layers, emb, gfin, head, seq, 1, fresh())
+    np.testing.assert_array_equal(np.argmax(logits[:, S - 1:], -1), toks)
+    np.testing.assert_allclose(last, logits[:, -1], rtol=0, atol=1e-10)
+    assert len(set(toks.ravel().tolist())) > 1  # not a degenerate chain
+
+
 # ------------------------------------------------- printed counts ------------
 
 def test_kv_cache_counts_match_printed_values():
