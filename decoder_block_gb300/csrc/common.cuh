@@ -74,7 +74,11 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + __expf(-z)); }
+// SiLU(z) = z * sigmoid(z) = z / (1 + e^-z).  The quotient uses the fast
+// division intrinsic (about 2 ulp; z -> -inf gives -0, z -> +inf gives z):
+// the IEEE-exact division is a long dependent sequence that dominated the
+// SwiGLU epilogue when only a few warps per SM are live (decode shapes).
+__device__ __forceinline__ float silu_f32(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // Budget for a bounded spin on an mbarrier or flag, in SM clock cycles
 // (about 2 s at 2 GHz); long enough that no legitimate wait reaches it.

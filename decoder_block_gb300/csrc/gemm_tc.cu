@@ -18,9 +18,10 @@
 // Split-K (for few output tiles, e.g. the decode step's M = 64 rows, so that
 // every SM streams a share of the weights): a work unit is (tile, K split);
 // each epilogue warp adds its 32-row fp32 partial into the tile's fp32
-// accumulator in the workspace (vector reductions at L2, cleared before the
-// launch), counts arrivals on a per-(tile, quarter) counter, and the last
-// arriving warp reads the sums back once and applies the epilogue.
+// accumulator in the workspace (vector reductions at L2), counts arrivals on a
+// per-(tile, quarter) counter, and the last arriving warp reads the sums back
+// once, applies the epilogue and returns the accumulator and the counter to
+// zero, so the scratch needs no clearing between launches.
 // Every mbarrier wait is bounded (clock budget); on expiry the kernel records a
 // status code, drains in-flight copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -57,8 +58,8 @@ struct GemmArgs {
   int *status;
   int splits;        // K splits per output tile (1: no split)
   int ksteps_split;  // BK steps per split
-  float *part;       // split-K accumulators [tiles][BM][BN] fp32 (zero at launch)
-  int *counters;     // split-K arrivals [tiles][4]
+  float *part;       // split-K accumulators [tiles][BM][BN] fp32 (zero at launch; left zero at exit)
+  int *counters;     // split-K arrivals [tiles][4] (zero at launch; left zero at exit)
   const float *ss_in;  // ROWSCALE epilogues: per-row sum of squares of A's rows
   float *ss_out;       // EPI_RESIDUAL_SQSUM: per-row sum of squares of C (accumulated)
   float inv_d, eps;    // RMSNorm: scale = rsqrt(ss * inv_d + eps)
@@ -391,24 +392,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (prev == args.splits - 1) {  // every split has added its partial: finish the tile
             __threadfence();
             float sq = 0.f;
-#pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-              float v[32];
+            // the next chunk's sums are loaded while this chunk runs its epilogue
+            auto load_sums = [&](int c, float (&v)[32]) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 4) {
+                const float4 p4 = m < args.M ? __ldcg(reinterpret_cast<const float4 *>(acc_row + c + i))
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[i] = p4.x;
+                v[i + 1] = p4.y;
+                v[i + 2] = p4.z;
+                v[i + 3] = p4.w;
+              }
+            };
+            // leave the scratch zero for the next launch: this warp is the only
+            // reader and every other split has already added its part
+            auto clear_sums = [&](int c) {
               if (m < args.M) {
 #pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                  const float4 p4 = __ldcg(reinterpret_cast<const float4 *>(acc_row + c + i));
-                  v[i] = p4.x;
-                  v[i + 1] = p4.y;
-                  v[i + 2] = p4.z;
-                  v[i + 3] = p4.w;
-                }
-              } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                for (int i = 0; i < 32; i += 4)
+                  __stcg(reinterpret_cast<float4 *>(acc_row + c + i), make_float4(0.f, 0.f, 0.f, 0.f));
+              }
+            };
+            float v[32], nx[32];
+            load_sums(0, v);
+            clear_sums(0);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+              if (c + 32 < BN) {
+                load_sums(c + 32, nx);
+                clear_sums(c + 32);
               }
               sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + c);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = nx[i];
             }
+            if (lane == 0) args.counters[tile * 4 + q] = 0;
             if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
               if (m < args.M) atomicAdd(args.ss_out + m, sq);
             }
@@ -473,11 +491,6 @@ cudaError_t launch_cfg(const bf16 *A, const bf16 *W, GemmArgs args, cudaStream_t
     return cudaErrorInvalidValue;
   const int tiles = ((args.M + BM - 1) / BM) * ((args.N + BN - 1) / BN);
   const int units = tiles * args.splits;
-  if (args.splits > 1) {
-    cudaError_t e = cudaMemsetAsync(args.counters, 0, (size_t)tiles * 4 * sizeof(int), st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(args.part, 0, (size_t)tiles * BM * BN * sizeof(float), st);
-    if (e != cudaSuccess) return e;
-  }
   const int grid = units < sm_count() ? units : sm_count();
   count_launch();
   gemm_tc_kernel<EPI, BN><<<grid, NUM_THREADS, G::SMEM_BYTES, st>>>(ma, mb, args);

@@ -210,6 +210,16 @@ llama_status copy_weights(const Dims &dm, const llama_block_weights *w, Allocs &
   return err == cudaSuccess ? LLAMA_OK : LLAMA_ERR_CUDA;
 }
 
+// Zero the split-K scratch of a workspace.  The GEMM leaves it zero after every
+// launch that completes (the last-arriving warp clears what it consumed), so
+// this runs at create and after a kernel gave up a bounded wait.
+cudaError_t clear_gemm_scratch(const GemmWorkspace &g) {
+  cudaError_t e = cudaSuccess;
+  if (g.part != nullptr) e = cudaMemset(g.part, 0, g.part_bytes);
+  if (e == cudaSuccess && g.counters != nullptr) e = cudaMemset(g.counters, 0, (size_t)g.counter_slots * sizeof(int));
+  return e;
+}
+
 llama_status alloc_workspace(const Dims &dm, int max_tokens, bool staging, Allocs &al, Workspace *ws) {
   const size_t e = dm.esize, T = (size_t)max_tokens;
   ws->max_tokens = max_tokens;
@@ -238,7 +248,9 @@ llama_status alloc_workspace(const Dims &dm, int max_tokens, bool staging, Alloc
     ws->ss_x = (float *)al.alloc(T * sizeof(float));
     ws->ss_h = (float *)al.alloc(T * sizeof(float));
   }
-  return al.failed ? LLAMA_ERR_OOM : LLAMA_OK;
+  if (al.failed) return LLAMA_ERR_OOM;
+  if (clear_gemm_scratch(ws->gemm) != cudaSuccess) return LLAMA_ERR_CUDA;
+  return LLAMA_OK;
 }
 
 #define LAUNCH(expr)                                 \
@@ -360,7 +372,7 @@ llama_status validate_call(const Dims &dm, int max_tokens, int B, int S, int sta
   return check_ptr(kv->v);
 }
 
-llama_status read_status(int *dev_status, int device) {
+llama_status read_status(int *dev_status, int device, const GemmWorkspace *scratch) {
   int prev = 0;
   if (cudaGetDevice(&prev) != cudaSuccess) return LLAMA_ERR_CUDA;
   if (prev != device && cudaSetDevice(device) != cudaSuccess) return LLAMA_ERR_CUDA;
@@ -368,6 +380,7 @@ llama_status read_status(int *dev_status, int device) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e == cudaSuccess) e = cudaMemcpy(&v, dev_status, sizeof(int), cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemset(dev_status, 0, sizeof(int));
+  if (e == cudaSuccess && v != 0 && v != DEV_BAD_TOKEN && scratch != nullptr) e = clear_gemm_scratch(*scratch);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (prev != device) cudaSetDevice(prev);
   if (e != cudaSuccess) return LLAMA_ERR_CUDA;
@@ -530,7 +543,7 @@ const char *llama_profile_step_name(int32_t step) {
 
 llama_status llama_block_device_status(llama_block *blk) {
   if (blk == nullptr) return LLAMA_ERR_INVALID_ARG;
-  return read_status(blk->status, blk->device);
+  return read_status(blk->status, blk->device, &blk->ws.gemm);
 }
 
 llama_status llama_stack_create(const llama_config *cfg, int32_t n_layers, int32_t vocab, const void *embed,
@@ -709,7 +722,7 @@ void llama_stack_destroy(llama_stack *stk) {
 
 llama_status llama_stack_device_status(llama_stack *stk) {
   if (stk == nullptr) return LLAMA_ERR_INVALID_ARG;
-  return read_status(stk->status, stk->device);
+  return read_status(stk->status, stk->device, &stk->ws.gemm);
 }
 
 size_t llama_kv_cache_bytes(const llama_config *cfg, int32_t max_batch, int32_t max_seq_len) {
