@@ -65,13 +65,14 @@ struct DtArgs {
 // exchange is one mbarrier phase (one arrival per warp) waited on with the
 // same bounded wait as every other barrier, so a warp that gives up can never
 // leave the others blocked.
-__device__ __forceinline__ bool exchange(float *slot_row, const float (&v)[DT_N], uint32_t bar, uint32_t parity,
+template <int N>
+__device__ __forceinline__ bool exchange(float *slot_row, const float (&v)[N], uint32_t bar, uint32_t parity,
                                          volatile int *abort, int *status) {
   const int lane = threadIdx.x & 31;
-  if (lane < DT_N) {
+  if (lane < N) {
     float x = v[0];
 #pragma unroll
-    for (int h = 1; h < DT_N; ++h)
+    for (int h = 1; h < N; ++h)
       if (lane == h) x = v[h];
     slot_row[lane] = x;
   }
@@ -81,6 +82,9 @@ __device__ __forceinline__ bool exchange(float *slot_row, const float (&v)[DT_N]
   return __all_sync(0xffffffffu, ok);
 }
 
+// RN: head columns the softmax works on (the smallest of 4, 8, 16 that is >= r);
+// P^T rows RN .. 15 stay zero, so the MMAs' padded columns contribute nothing.
+template <int RN>
 __global__ void __launch_bounds__(DT_THREADS, 1)
     attn_decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, DtArgs a) {
@@ -256,6 +260,11 @@ __global__ void __launch_bounds__(DT_THREADS, 1)
     const int qq = warp & 3;             // TMEM lane quarter
     const int row = qq * 32 + lane;      // tile position (S^T) / d (O^T)
     const uint32_t lane_base = tmem + ((uint32_t)(qq * 32) << 16);
+    if (RN < DT_N) {  // P^T rows the softmax never writes: zero once for both buffers
+      uint4 *pz = reinterpret_cast<uint4 *>(smem + L::OFF_P);
+      for (int i = threadIdx.x - 64; i < 2 * L::P_BYTES / 16; i += 128) pz[i] = make_uint4(0, 0, 0, 0);
+      ptx::fence_proxy_async_smem();
+    }
     int tile = 0, nq = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < a.n_items && ok; it += gridDim.x, ++nq) {
@@ -263,9 +272,9 @@ __global__ void __launch_bounds__(DT_THREADS, 1)
       item_coords(it, b, g, k0, nt);
       const int ob = nq & 1;
       const int k1 = min(a.kv_len, k0 + DT_CHUNK);
-      float m_run[DT_N], l_run[DT_N];
+      float m_run[RN], l_run[RN];
 #pragma unroll
-      for (int h = 0; h < DT_N; ++h) {
+      for (int h = 0; h < RN; ++h) {
         m_run[h] = -INFINITY;
         l_run[h] = 0.f;
       }
@@ -282,9 +291,9 @@ __global__ void __launch_bounds__(DT_THREADS, 1)
         ptx::tmem_ld_wait();
         const bool valid = k0 + j * DT_TILE + row < k1;
         // per-head tile max over the 128 positions: warp shuffles, then across the 4 warps
-        float mx[DT_N];
+        float mx[RN];
 #pragma unroll
-        for (int h = 0; h < DT_N; ++h) {
+        for (int h = 0; h < RN; ++h) {
           float v = (valid && h < a.r) ? s[h] : -INFINITY;
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
@@ -296,9 +305,9 @@ __global__ void __launch_bounds__(DT_THREADS, 1)
           break;
         }
         bool need_any = false;
-        float alpha[DT_N];
+        float alpha[RN];
 #pragma unroll
-        for (int h = 0; h < DT_N; ++h) {
+        for (int h = 0; h < RN; ++h) {
           const float t = fmaxf(fmaxf(rs[h], rs[DT_N + h]), fmaxf(rs[2 * DT_N + h], rs[3 * DT_N + h]));
           const float mt = t * a.scale_log2;
           alpha[h] = 1.f;
@@ -317,7 +326,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1)
         uint8_t *pbuf = smem + L::OFF_P + sb * L::P_BYTES + (row / 64) * (DT_N * 128);
         const int c = row % 64;
 #pragma unroll
-        for (int h = 0; h < DT_N; ++h) {
+        for (int h = 0; h < RN; ++h) {
           const float p = (valid && h < a.r) ? ptx::ex2_approx(fmaf(s[h], a.scale_log2, -m_run[h])) : 0.f;
           l_run[h] = l_run[h] * alpha[h] + p;
           const int chunk = (c >> 3) ^ (h & 7);
@@ -336,7 +345,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1)
           ptx::tmem_ld_wait();
           uint32_t wv[DT_N];
 #pragma unroll
-          for (int h = 0; h < DT_N; ++h) wv[h] = __float_as_uint(ov[h] * alpha[h]);
+          for (int h = 0; h < DT_N; ++h) wv[h] = __float_as_uint(h < RN ? ov[h] * alpha[h < RN ? h : 0] : ov[h]);
           ptx::tmem_st16(lane_base + 32 + ob * DT_N, wv);
           ptx::tmem_st_wait();
         }
@@ -358,7 +367,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(o_free(ob));
 #pragma unroll
-      for (int h = 0; h < DT_N; ++h) {
+      for (int h = 0; h < RN; ++h) {
         float v = l_run[h];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1)
       }
       const int d = row;
 #pragma unroll
-      for (int h = 0; h < DT_N; ++h) {
+      for (int h = 0; h < RN; ++h) {
         if (h >= a.r) continue;
         const float lsum = ls[h] + ls[DT_N + h] + ls[2 * DT_N + h] + ls[3 * DT_N + h];
         const int hq = g * a.r + h;
@@ -440,8 +449,14 @@ cudaError_t launch_attn_decode_tc(const bf16 *q, const bf16 *kc, const bf16 *vc,
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(attn_decode_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     DtLayout::BYTES);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(attn_decode_tc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      DtLayout::BYTES);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(attn_decode_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      DtLayout::BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
   DtArgs a;
@@ -473,7 +488,12 @@ cudaError_t launch_attn_decode_tc(const bf16 *q, const bf16 *kc, const bf16 *vc,
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = a.n_items < sms ? a.n_items : sms;
   count_launch();
-  attn_decode_tc_kernel<<<grid, DT_THREADS, DtLayout::BYTES, st>>>(mq, mk, mv, a);
+  if (a.r <= 4)
+    attn_decode_tc_kernel<4><<<grid, DT_THREADS, DtLayout::BYTES, st>>>(mq, mk, mv, a);
+  else if (a.r <= 8)
+    attn_decode_tc_kernel<8><<<grid, DT_THREADS, DtLayout::BYTES, st>>>(mq, mk, mv, a);
+  else
+    attn_decode_tc_kernel<16><<<grid, DT_THREADS, DtLayout::BYTES, st>>>(mq, mk, mv, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.n_split == 1) return e;
   return launch_decode_combine(a.part, o, B * H, DT_D, a.n_split, st);

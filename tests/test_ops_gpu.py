@@ -153,6 +153,8 @@ ATTN_CASES = [
     (1, 1, 40, 8, 2, 128, "bf16"),    # decode with fewer query rows than one 16-row operand
     (2, 1, 600, 4, 4, 128, "bf16"),   # decode, MHA, d_head 128
     (2, 1, 2047, 32, 8, 128, "bf16"), # decode, chunk edge (2048 cached positions)
+    (2, 1, 900, 32, 2, 128, "bf16"),  # decode, n_rep 16 (all sixteen head columns live)
+    (3, 1, 520, 24, 4, 128, "bf16"),  # decode, n_rep 6 (eight-column softmax, two padded)
     (2, 3, 0, 2, 1, 32, "bf16"),
 ]
 
