@@ -142,6 +142,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // programmatic dependent launch: q and the cache come from earlier kernels
+  allow_dependents_launch();
+  grid_dependency_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -453,8 +456,7 @@ cudaError_t launch_prefill(const bf16 *q, const bf16 *kc, const bf16 *vc, bf16 *
   args.status = status;
   const unsigned grid = (unsigned)(B * G * args.nqb);
   count_launch();
-  attn_prefill_kernel<D><<<grid, ATT_THREADS, L::BYTES, st>>>(mq, mk, mv, args);
-  return cudaGetLastError();
+  return launch_pdl(attn_prefill_kernel<D>, dim3(grid), dim3(ATT_THREADS), L::BYTES, st, mq, mk, mv, args);
 }
 
 }  // namespace

@@ -80,6 +80,34 @@ __device__ __forceinline__ float warp_max(float v) {
 // SwiGLU epilogue when only a few warps per SM are live (decode shapes).
 __device__ __forceinline__ float silu_f32(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
+// Programmatic dependent launch.  A kernel started with launch_pdl may begin
+// while the previous kernel on the stream is still running: before it reads
+// anything an earlier kernel wrote, or writes anything, it calls
+// grid_dependency_wait(), which returns once every earlier kernel of the stream
+// has completed and its memory is visible (at once when there is none).  Work
+// that touches only data no kernel writes -- the weights -- may come first.
+// allow_dependents_launch() lets the next such kernel be scheduled early.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args &&...args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Budget for a bounded spin on an mbarrier or flag, in SM clock cycles
 // (about 2 s at 2 GHz); long enough that no legitimate wait reaches it.
 constexpr long long kWaitBudgetCycles = 4000000000LL;

@@ -266,6 +266,8 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(DecArgs a) {
 template <int D>
 __global__ void __launch_bounds__(D) attn_decode_combine(const float *__restrict__ part, bf16 *__restrict__ o, int H,
                                                          int n_split) {
+  allow_dependents_launch();
+  grid_dependency_wait();
   const int bh = blockIdx.x, d = threadIdx.x;
   const float *p = part + (size_t)bh * n_split * (D + 2);
   float m = -INFINITY;
@@ -339,14 +341,12 @@ size_t attn_decode_scratch_bytes(int max_tokens, int H, int D, int max_seq) {
 cudaError_t launch_decode_combine(const float *part, bf16 *o, int BH, int D, int n_split, cudaStream_t st) {
   if (D == 128) {
     count_launch();
-    attn_decode_combine<128><<<BH, 128, 0, st>>>(part, o, 0, n_split);
+    return launch_pdl(attn_decode_combine<128>, dim3(BH), dim3(128), 0, st, part, o, 0, n_split);
   } else if (D == 64) {
     count_launch();
-    attn_decode_combine<64><<<BH, 64, 0, st>>>(part, o, 0, n_split);
-  } else {
-    return cudaErrorInvalidValue;
+    return launch_pdl(attn_decode_combine<64>, dim3(BH), dim3(64), 0, st, part, o, 0, n_split);
   }
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 bool attn_decode_supported(int H, int G, int D) {

@@ -141,6 +141,9 @@ __global__ void __launch_bounds__(DT_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // programmatic dependent launch: q and the cache come from earlier kernels
+  allow_dependents_launch();
+  grid_dependency_wait();
 
   // Work item -> (b, g, chunk).
   auto item_coords = [&](int it, int &b, int &g, int &k0, int &nt) {
@@ -488,13 +491,8 @@ cudaError_t launch_attn_decode_tc(const bf16 *q, const bf16 *kc, const bf16 *vc,
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = a.n_items < sms ? a.n_items : sms;
   count_launch();
-  if (a.r <= 4)
-    attn_decode_tc_kernel<4><<<grid, DT_THREADS, DtLayout::BYTES, st>>>(mq, mk, mv, a);
-  else if (a.r <= 8)
-    attn_decode_tc_kernel<8><<<grid, DT_THREADS, DtLayout::BYTES, st>>>(mq, mk, mv, a);
-  else
-    attn_decode_tc_kernel<16><<<grid, DT_THREADS, DtLayout::BYTES, st>>>(mq, mk, mv, a);
-  cudaError_t e = cudaGetLastError();
+  auto kernel = a.r <= 4 ? attn_decode_tc_kernel<4> : (a.r <= 8 ? attn_decode_tc_kernel<8> : attn_decode_tc_kernel<16>);
+  cudaError_t e = launch_pdl(kernel, dim3(grid), dim3(DT_THREADS), DtLayout::BYTES, st, mq, mk, mv, a);
   if (e != cudaSuccess || a.n_split == 1) return e;
   return launch_decode_combine(a.part, o, B * H, DT_D, a.n_split, st);
 }

@@ -22,6 +22,10 @@
 // per-(tile, quarter) counter, and the last arriving warp reads the sums back
 // once, applies the epilogue and returns the accumulator and the counter to
 // zero, so the scratch needs no clearing between launches.
+// Launched as a programmatic dependent: for weights the library owns (written
+// once at create, by no kernel of a forward) the producer requests the first
+// stages' weights before it waits for the previous kernel; everything else
+// (activations, residuals, row statistics, outputs) is touched after the wait.
 // Every mbarrier wait is bounded (clock budget); on expiry the kernel records a
 // status code, drains in-flight copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -64,6 +68,7 @@ struct GemmArgs {
   float *ss_out;       // EPI_RESIDUAL_SQSUM: per-row sum of squares of C (accumulated)
   float inv_d, eps;    // RMSNorm: scale = rsqrt(ss * inv_d + eps)
   QkvScatter qkv;      // EPI_QKV_ROPE destinations
+  int prefetch_w;      // W is written by no kernel: load it before the grid dependency wait
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int &mt, int &nt) {
@@ -275,8 +280,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  allow_dependents_launch();
   if (warp == 0) {
     if (lane == 0) {
+      // The weights of the first unit's first stages depend on no earlier
+      // kernel: request them before waiting for the activations.
+      int pre = 0;
+      if (args.prefetch_w && (int)blockIdx.x < num_units) {
+        int mt, nt, k0, k1;
+        unit_coords(blockIdx.x, mt, nt, k0, k1);
+        pre = min(STAGES, k1 - k0);
+        for (int i = 0; i < pre; ++i) {
+          const uint32_t sb = smem0 + i * G::STAGE_BYTES + G::A_BYTES;
+          ptx::mbar_arrive_expect_tx(full_bar(i), G::STAGE_BYTES);
+          ptx::tma_load_2d(sb, &tmB, (k0 + i) * BK, nt * BN, full_bar(i));
+        }
+      }
+      grid_dependency_wait();
       int it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
@@ -285,11 +305,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int k = k0; k < k1; ++k) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
+          const uint32_t sa = smem0 + s * G::STAGE_BYTES, sb = sa + G::A_BYTES;
+          if (it < pre) {  // stage s is fresh and its weights are already on the way
+            ptx::tma_load_2d(sa, &tmA, k * BK, mt * BM, full_bar(s));
+            ++it;
+            continue;
+          }
           if (!ptx::mbar_wait(empty_bar(s), ph ^ 1, abort_flag, args.status, DEV_TIMEOUT_PRODUCER)) {
             ok = false;
             break;
           }
-          const uint32_t sa = smem0 + s * G::STAGE_BYTES, sb = sa + G::A_BYTES;
           ptx::mbar_arrive_expect_tx(full_bar(s), G::STAGE_BYTES);
           ptx::tma_load_2d(sa, &tmA, k * BK, mt * BM, full_bar(s));
           ptx::tma_load_2d(sb, &tmB, k * BK, nt * BN, full_bar(s));
@@ -340,6 +365,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_wait(fin_bar, 0, &dummy, args.status, DEV_TIMEOUT_MMA);
     }
   } else {
+    grid_dependency_wait();  // the epilogue reads R / row statistics and writes C
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     int tcount = 0;
@@ -493,8 +519,7 @@ cudaError_t launch_cfg(const bf16 *A, const bf16 *W, GemmArgs args, cudaStream_t
   const int units = tiles * args.splits;
   const int grid = units < sm_count() ? units : sm_count();
   count_launch();
-  gemm_tc_kernel<EPI, BN><<<grid, NUM_THREADS, G::SMEM_BYTES, st>>>(ma, mb, args);
-  return cudaGetLastError();
+  return launch_pdl(gemm_tc_kernel<EPI, BN>, dim3(grid), dim3(NUM_THREADS), G::SMEM_BYTES, st, ma, mb, args);
 }
 
 template <int EPI>
@@ -587,7 +612,7 @@ int gemm_splitk_counter_slots() { return 4 * sm_count() * 4; }
 
 cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C, int M, int N, int K, int epi,
                            int *status, cudaStream_t st, const GemmWorkspace *ws, const RowNorm *norm,
-                           const QkvScatter *scatter) {
+                           const QkvScatter *scatter, bool weights_static) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   if (K <= 0 || (K & 7) != 0) return cudaErrorInvalidValue;
   if ((epi == EPI_SWIGLU || epi == EPI_SWIGLU_ROWSCALE) && (N & 31) != 0) return cudaErrorInvalidValue;
@@ -600,7 +625,8 @@ cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C,
       return cudaErrorInvalidValue;
   }
   const GemmPlan plan = plan_gemm(M, N, K, ws != nullptr ? ws->part_bytes : 0, ws != nullptr ? ws->counter_slots : 0);
-  GemmArgs args{R, C, M, N, K, status, 1, (K + BK - 1) / BK, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f, {}};
+  GemmArgs args{R, C, M, N, K, status, 1, (K + BK - 1) / BK, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f, {},
+                weights_static ? 1 : 0};
   if (scatter != nullptr) args.qkv = *scatter;
   if (norm != nullptr) {
     args.ss_in = norm->ss_in;

@@ -293,8 +293,7 @@ llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, c
   pf.begin_forward();
   // attention_norm statistics; the normalisation itself happens in the QKV GEMM
   pf.mark(0, 0, st);
-  LAUNCH(launch_row_sqsum(x, ws.ss_x, M, dm.d, st));
-  if (cudaMemsetAsync(ws.ss_h, 0, (size_t)M * sizeof(float), st) != cudaSuccess) return LLAMA_ERR_CUDA;
+  LAUNCH(launch_row_sqsum(x, ws.ss_x, ws.ss_h, M, dm.d, st));
   pf.mark(0, 1, st);
   RowNorm norm_x;
   norm_x.ss_in = ws.ss_x;
@@ -315,14 +314,14 @@ llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, c
     sc.cache_seq = kv->max_seq_len;
     pf.mark(1, 0, st);
     LAUNCH(launch_gemm_tc(x, (const bf16 *)w.wqkv, nullptr, nullptr, M, dm.QKV, dm.d, EPI_QKV_ROPE, status, st,
-                          &ws.gemm, &norm_x, &sc));
+                          &ws.gemm, &norm_x, &sc, true));
     pf.mark(1, 1, st);
     pf.mark(2, 0, st);  // RoPE + KV write: fused into the QKV epilogue
     pf.mark(2, 1, st);
   } else {
     pf.mark(1, 0, st);
     LAUNCH(launch_gemm_tc(x, (const bf16 *)w.wqkv, nullptr, qkv, M, dm.QKV, dm.d, EPI_STORE_ROWSCALE, status, st,
-                          &ws.gemm, &norm_x));
+                          &ws.gemm, &norm_x, nullptr, true));
     pf.mark(1, 1, st);
     pf.mark(2, 0, st);
     LAUNCH(launch_rope_kv<bf16>(qkv, q, kc, vc, rope, B, S, start_pos, dm.H, dm.G, dm.D, kv->max_seq_len, st));
@@ -339,16 +338,17 @@ llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, c
   norm_h.d = dm.d;
   pf.mark(4, 0, st);
   LAUNCH(launch_gemm_tc(o, (const bf16 *)w.wo, x, h, M, dm.d, dm.H * dm.D, EPI_RESIDUAL_SQSUM, status, st, &ws.gemm,
-                        &norm_h));
+                        &norm_h, nullptr, true));
   pf.mark(4, 1, st);
   pf.mark(5, 0, st);  // ffn_norm: fused into the O and gate/up GEMM epilogues
   pf.mark(5, 1, st);
   pf.mark(6, 0, st);
   LAUNCH(launch_gemm_tc(h, (const bf16 *)w.w_gu, nullptr, act, M, 2 * dm.F, dm.d, EPI_SWIGLU_ROWSCALE, status, st,
-                        &ws.gemm, &norm_h));
+                        &ws.gemm, &norm_h, nullptr, true));
   pf.mark(6, 1, st);
   pf.mark(7, 0, st);
-  LAUNCH(launch_gemm_tc(act, (const bf16 *)w.w_down, h, y, M, dm.d, dm.F, EPI_RESIDUAL, status, st, &ws.gemm));
+  LAUNCH(launch_gemm_tc(act, (const bf16 *)w.w_down, h, y, M, dm.d, dm.F, EPI_RESIDUAL, status, st, &ws.gemm,
+                        nullptr, nullptr, true));
   pf.mark(7, 1, st);
   return LLAMA_OK;
 }
@@ -634,7 +634,7 @@ llama_status stack_head(llama_stack *stk, const void *hidden, int rows, float *l
     LAUNCH(launch_rmsnorm<bf16>((const bf16 *)hidden, (const bf16 *)stk->final_norm, (bf16 *)stk->xn, rows, dm.d,
                                 dm.eps, st));
     LAUNCH(launch_gemm_tc((const bf16 *)stk->xn, (const bf16 *)stk->lm_head, nullptr, logits, rows, stk->vocab, dm.d,
-                          EPI_F32OUT, stk->status, st, &stk->ws.gemm));
+                          EPI_F32OUT, stk->status, st, &stk->ws.gemm, nullptr, nullptr, true));
   } else {
     LAUNCH(launch_rmsnorm<float>((const float *)hidden, (const float *)stk->final_norm, (float *)stk->xn, rows, dm.d,
                                  dm.eps, st));

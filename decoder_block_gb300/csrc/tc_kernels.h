@@ -59,9 +59,13 @@ struct QkvScatter {
 // status: device status word for bounded-wait expiry (may be null).
 // ws: split-K scratch (null: never split).  norm: required by the ROWSCALE, SQSUM
 // and QKV_ROPE epilogues; scatter: required by EPI_QKV_ROPE (C unused there).
+// weights_static: W is not written by any kernel that may still be running
+// (library-owned weights), so its first tiles are requested before the kernel
+// waits for its predecessor (programmatic dependent launch).
 cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C, int M, int N, int K, int epi,
                            int *status, cudaStream_t st, const GemmWorkspace *ws = nullptr,
-                           const RowNorm *norm = nullptr, const QkvScatter *scatter = nullptr);
+                           const RowNorm *norm = nullptr, const QkvScatter *scatter = nullptr,
+                           bool weights_static = false);
 
 // out[32j + i] = gate[16j + i], out[32j + 16 + i] = up[16j + i] (rows of width d), F % 16 == 0.
 cudaError_t launch_interleave_rows(const bf16 *gate, const bf16 *up, bf16 *out, int F, int d, cudaStream_t st);
