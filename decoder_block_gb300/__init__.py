@@ -28,6 +28,8 @@ LLAMA_ERR_DEVICE_TIMEOUT = 8
 
 LLAMA_F32 = 0
 LLAMA_BF16 = 1
+LLAMA_ROPE_INTERLEAVED = 0
+LLAMA_ROPE_HALVES = 1
 
 EPI_STORE = 0
 EPI_RESIDUAL = 1
@@ -43,7 +45,9 @@ class LlamaError(RuntimeError):
 
 class llama_config(ctypes.Structure):
     _fields_ = [("d_model", c_int32), ("n_heads", c_int32), ("n_kv_heads", c_int32), ("d_ff", c_int32),
-                ("max_seq_len", c_int32), ("norm_eps", c_float), ("rope_theta", c_float), ("dtype", c_int32)]
+                ("max_seq_len", c_int32), ("norm_eps", c_float), ("rope_theta", c_float), ("dtype", c_int32),
+                ("rope_layout", c_int32), ("rope_scaling_factor", c_float), ("rope_low_freq_factor", c_float),
+                ("rope_high_freq_factor", c_float), ("rope_original_max_pos", c_int32)]
 
 
 WEIGHT_FIELDS = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")
@@ -100,11 +104,12 @@ def load() -> ctypes.CDLL:
         "llama_op_attention_workspace_bytes": (c_size_t, [c_int32, c_int32, c_int32, c_int32, c_int32, c_int32]),
         "llama_op_attention": (st, [c_int32, c_void_p, POINTER(llama_kv_cache), c_void_p, c_int32, c_int32, c_int32,
                                     c_int32, c_int32, c_int32, c_void_p, c_size_t, c_void_p]),
-        "llama_op_rope_table": (st, [c_void_p, c_int32, c_int32, c_float, c_void_p]),
+        "llama_op_rope_table": (st, [c_void_p, c_int32, c_int32, c_float, c_float, c_float, c_float, c_int32,
+                                     c_void_p]),
         "llama_op_attention_decode_noalloc": (st, [c_void_p, POINTER(llama_kv_cache), c_void_p, c_int32, c_int32,
                                                    c_int32, c_int32, c_int32, c_void_p]),
         "llama_op_rope_kv_write": (st, [c_int32, c_void_p, c_void_p, POINTER(llama_kv_cache), c_void_p, c_int32,
-                                        c_int32, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p]),
+                                        c_int32, c_int32, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -133,8 +138,13 @@ def _stream(s):
 
 # ---------------------------------------------------------------- structs ---
 
-def make_config(d_model, n_heads, n_kv_heads, d_ff, max_seq_len, norm_eps, rope_theta, dtype) -> llama_config:
-    return llama_config(d_model, n_heads, n_kv_heads, d_ff, max_seq_len, norm_eps, rope_theta, dtype)
+def make_config(d_model, n_heads, n_kv_heads, d_ff, max_seq_len, norm_eps, rope_theta, dtype,
+                rope_layout=0, rope_scaling=None) -> llama_config:
+    """rope_scaling: None or a dict with factor, low_freq_factor, high_freq_factor, original_max_pos."""
+    sc = rope_scaling or {}
+    return llama_config(d_model, n_heads, n_kv_heads, d_ff, max_seq_len, norm_eps, rope_theta, dtype, rope_layout,
+                        float(sc.get("factor", 0.0)), float(sc.get("low_freq_factor", 0.0)),
+                        float(sc.get("high_freq_factor", 0.0)), int(sc.get("original_max_pos", 0)))
 
 
 def make_weights(w: dict) -> llama_block_weights:
@@ -258,14 +268,17 @@ def llama_op_attention(dtype, q, kv: llama_kv_cache, o, B, S, start_pos, H, G, D
                                      workspace_bytes, _stream(stream))
 
 
-def llama_op_rope_table(table, max_seq, D, theta, stream=None) -> int:
-    return load().llama_op_rope_table(_p(table), max_seq, D, theta, _stream(stream))
+def llama_op_rope_table(table, max_seq, D, theta, scaling=None, stream=None) -> int:
+    sc = scaling or {}
+    return load().llama_op_rope_table(_p(table), max_seq, D, theta, float(sc.get("factor", 0.0)),
+                                      float(sc.get("low_freq_factor", 0.0)), float(sc.get("high_freq_factor", 0.0)),
+                                      int(sc.get("original_max_pos", 0)), _stream(stream))
 
 
 def llama_op_rope_kv_write(dtype, qkv, q_out, kv: llama_kv_cache, table, table_max_seq, B, S, start_pos, H, G, D,
-                           stream=None) -> int:
+                           layout=0, stream=None) -> int:
     return load().llama_op_rope_kv_write(dtype, _p(qkv), _p(q_out), byref(kv), _p(table), table_max_seq, B, S,
-                                         start_pos, H, G, D, _stream(stream))
+                                         start_pos, H, G, D, layout, _stream(stream))
 
 
 LLAMA_NOALLOC_SCRATCH_BYTES = 32 << 20

@@ -161,6 +161,26 @@ __device__ __forceinline__ void qkv_rope_chunk32(const float (&v)[32], const Gem
   if (head < r.H + r.G) {
     // "The Evolving Transformer 04 · LLaMA", §02 RoPE: (a cos - b sin, a sin + b cos)
     const float4 *cs = reinterpret_cast<const float4 *>(r.table + (size_t)p * (r.D / 2) + e / 2);
+    if (r.halves) {
+      // pairs (i, i + D/2), i = e/2 .. e/2 + 15: first members to i, second to i + D/2
+      uint32_t lo[8], hi[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4 c = __ldg(cs + k);
+        const float a0 = v[4 * k], b0 = v[4 * k + 1], a1 = v[4 * k + 2], b1 = v[4 * k + 3];
+        lo[k] = pack_bf16(a0 * c.x - b0 * c.y, a1 * c.z - b1 * c.w);
+        hi[k] = pack_bf16(a0 * c.y + b0 * c.x, a1 * c.w + b1 * c.z);
+      }
+      bf16 *base = head < r.H ? r.q + (size_t)m * r.H * r.D + head * r.D
+                              : r.kc + (((size_t)b * r.G + (head - r.H)) * r.cache_seq + p) * r.D;
+      uint4 *d_lo = reinterpret_cast<uint4 *>(base + e / 2);
+      uint4 *d_hi = reinterpret_cast<uint4 *>(base + r.D / 2 + e / 2);
+      d_lo[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      d_lo[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+      d_hi[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      d_hi[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+      return;
+    }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const float4 c = __ldg(cs + k);  // {cos_i, sin_i, cos_i+1, sin_i+1}
@@ -532,6 +552,17 @@ cudaError_t launch_epi(const bf16 *A, const bf16 *W, GemmArgs args, int bn, cuda
   return cudaErrorInvalidValue;
 }
 
+__global__ void permute_halves_rows_kernel(const uint4 *__restrict__ W, uint4 *__restrict__ out, int heads, int D,
+                                           int vec_per_row) {
+  const size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  const size_t total = (size_t)heads * D * vec_per_row;
+  if (idx >= total) return;
+  const int orow = (int)(idx / vec_per_row), c = (int)(idx % vec_per_row);
+  const int head = orow / D, j = orow % D;
+  const int srow = head * D + (j & 1 ? j / 2 + D / 2 : j / 2);
+  out[idx] = W[(size_t)srow * vec_per_row + c];
+}
+
 __global__ void interleave_rows_kernel(const uint4 *__restrict__ gate, const uint4 *__restrict__ up,
                                        uint4 *__restrict__ out, int F, int vec_per_row) {
   const size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
@@ -651,6 +682,17 @@ cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C,
     case EPI_QKV_ROPE: return launch_epi<EPI_QKV_ROPE>(A, W, args, plan.bn, st);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_permute_halves_rows(const bf16 *W, bf16 *out, int heads, int D, int d, cudaStream_t st) {
+  if ((D & 1) != 0 || (d & 7) != 0) return cudaErrorInvalidValue;
+  const int vpr = d / 8;
+  const size_t total = (size_t)heads * D * vpr;
+  if (total == 0) return cudaSuccess;
+  count_launch();
+  permute_halves_rows_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(
+      reinterpret_cast<const uint4 *>(W), reinterpret_cast<uint4 *>(out), heads, D, vpr);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_interleave_rows(const bf16 *gate, const bf16 *up, bf16 *out, int F, int d, cudaStream_t st) {

@@ -40,14 +40,22 @@ template <typename T>
 cudaError_t launch_gemm_simt(const T *A, const T *W, const T *W3, const T *R, void *C, int M, int N, int K,
                              int epi, cudaStream_t st);
 
-// cos/sin table [max_seq][D/2] (float2 = {cos, sin}) of p * theta^(-2i/D), computed in fp64.
-cudaError_t launch_rope_table(float2 *table, int max_seq, int D, double theta, cudaStream_t st);
+// Llama 3.1 RoPE frequency stretch (factor <= 1: none); see llama_config.
+struct RopeScaling {
+  double factor = 0.0, low = 0.0, high = 0.0, original_max_pos = 0.0;
+};
+
+// cos/sin table [max_seq][D/2] (float2 = {cos, sin}) of p * f_i with
+// f_i = theta^(-2i/D), stretched when sc.factor > 1; computed in fp64.
+cudaError_t launch_rope_table(float2 *table, int max_seq, int D, double theta, const RopeScaling &sc,
+                              cudaStream_t st);
 
 // RoPE on q and k of qkv [T][(H + 2G) D] and the KV-cache write.
 //   q_out [T][H D] (rotated q); kc/vc [cache_batch][G][cache_seq][D].
+// halves = 0: pairs (2i, 2i+1); 1: pairs (i, i + D/2); natural component order in and out.
 template <typename T>
 cudaError_t launch_rope_kv(const T *qkv, T *q_out, T *kc, T *vc, const float2 *table, int B, int S,
-                           int start_pos, int H, int G, int D, int cache_seq, cudaStream_t st);
+                           int start_pos, int H, int G, int D, int cache_seq, int halves, cudaStream_t st);
 
 // Reference causal GQA attention: one warp per (token, query head), online softmax in fp32.
 template <typename T>

@@ -111,18 +111,33 @@ llama_status llama_op_attention(int32_t dtype, const void *q, const llama_kv_cac
                                                 (float *)o, B, S, start_pos, H, G, D, kv->max_seq_len, st));
 }
 
-llama_status llama_op_rope_table(float *table, int32_t max_seq, int32_t D, float theta, llama_stream stream) {
+llama_status llama_op_rope_table(float *table, int32_t max_seq, int32_t D, float theta, float scaling_factor,
+                                 float low_freq_factor, float high_freq_factor, int32_t original_max_pos,
+                                 llama_stream stream) {
   if (max_seq <= 0 || D <= 0 || D % 2 != 0 || !(theta > 0.f)) return LLAMA_ERR_INVALID_ARG;
+  RopeScaling sc;
+  if (scaling_factor > 1.f) {
+    if (!(low_freq_factor > 0.f && high_freq_factor > low_freq_factor && original_max_pos > 0))
+      return LLAMA_ERR_INVALID_ARG;
+    sc.factor = scaling_factor;
+    sc.low = low_freq_factor;
+    sc.high = high_freq_factor;
+    sc.original_max_pos = original_max_pos;
+  } else if (!(scaling_factor <= 1.f)) {
+    return LLAMA_ERR_INVALID_ARG;
+  }
   llama_status s = check(table);
   if (s != LLAMA_OK) return s;
-  return status_of(launch_rope_table(reinterpret_cast<float2 *>(table), max_seq, D, (double)theta,
+  return status_of(launch_rope_table(reinterpret_cast<float2 *>(table), max_seq, D, (double)theta, sc,
                                      (cudaStream_t)stream));
 }
 
 llama_status llama_op_rope_kv_write(int32_t dtype, const void *qkv, void *q_out, const llama_kv_cache *kv,
                                     const float *table, int32_t table_max_seq, int32_t B, int32_t S,
-                                    int32_t start_pos, int32_t H, int32_t G, int32_t D, llama_stream stream) {
+                                    int32_t start_pos, int32_t H, int32_t G, int32_t D, int32_t layout,
+                                    llama_stream stream) {
   if (dtype != LLAMA_F32 && dtype != LLAMA_BF16) return LLAMA_ERR_INVALID_ARG;
+  if (layout != LLAMA_ROPE_INTERLEAVED && layout != LLAMA_ROPE_HALVES) return LLAMA_ERR_INVALID_ARG;
   if (kv == nullptr || B <= 0 || S <= 0 || start_pos < 0 || H <= 0 || G <= 0 || D <= 0)
     return LLAMA_ERR_INVALID_ARG;
   if (H % G != 0) return LLAMA_ERR_SHAPE;
@@ -137,9 +152,9 @@ llama_status llama_op_rope_kv_write(int32_t dtype, const void *qkv, void *q_out,
   const float2 *t2 = reinterpret_cast<const float2 *>(table);
   if (dtype == LLAMA_BF16)
     return status_of(launch_rope_kv<bf16>((const bf16 *)qkv, (bf16 *)q_out, (bf16 *)kv->k, (bf16 *)kv->v, t2, B, S,
-                                          start_pos, H, G, D, kv->max_seq_len, st));
+                                          start_pos, H, G, D, kv->max_seq_len, layout, st));
   return status_of(launch_rope_kv<float>((const float *)qkv, (float *)q_out, (float *)kv->k, (float *)kv->v, t2, B,
-                                         S, start_pos, H, G, D, kv->max_seq_len, st));
+                                         S, start_pos, H, G, D, kv->max_seq_len, layout, st));
 }
 
 }  // extern "C"

@@ -47,8 +47,14 @@ struct Dims {
   int d, H, G, D, F, QKV, max_seq;
   float eps;
   double theta;
+  RopeScaling rope_scaling;
+  int rope_halves;          // pairs (i, i + D/2) instead of (2i, 2i+1)
   int dtype;
   size_t esize;
+  // halves RoPE on the fused QKV epilogue: the q / k rows of Wqkv are stored
+  // reordered so that each pair lands in adjacent accumulator columns
+  bool fused_qkv_rope() const { return dtype == LLAMA_BF16 && D % 32 == 0; }
+  bool permute_halves() const { return rope_halves && fused_qkv_rope(); }
 };
 
 // Device allocations owned by one handle, freed together.
@@ -141,8 +147,15 @@ llama_status validate_config(const llama_config *c, Dims *dm) {
   const int D = c->d_model / c->n_heads;
   if (D % 2 != 0) return LLAMA_ERR_SHAPE;
   if (D != 16 && D != 32 && D != 64 && D != 128) return LLAMA_ERR_UNSUPPORTED;
+  if (c->rope_layout != LLAMA_ROPE_INTERLEAVED && c->rope_layout != LLAMA_ROPE_HALVES) return LLAMA_ERR_INVALID_ARG;
+  const bool scaled = c->rope_scaling_factor > 1.f;
+  if (!scaled && !(c->rope_scaling_factor <= 1.f)) return LLAMA_ERR_INVALID_ARG;  // NaN
+  if (scaled && !(c->rope_low_freq_factor > 0.f && c->rope_high_freq_factor > c->rope_low_freq_factor &&
+                  c->rope_original_max_pos > 0))
+    return LLAMA_ERR_INVALID_ARG;
   const int vec = c->dtype == LLAMA_BF16 ? 8 : 4;
   if (c->d_model % vec != 0 || c->d_ff % vec != 0) return LLAMA_ERR_UNSUPPORTED;
+  if (c->rope_layout == LLAMA_ROPE_HALVES && (D / 2) % vec != 0) return LLAMA_ERR_UNSUPPORTED;
   if (c->dtype == LLAMA_BF16 && c->d_ff % 16 != 0) return LLAMA_ERR_UNSUPPORTED;  // gate/up interleave groups
   dm->d = c->d_model;
   dm->H = c->n_heads;
@@ -153,6 +166,14 @@ llama_status validate_config(const llama_config *c, Dims *dm) {
   dm->max_seq = c->max_seq_len;
   dm->eps = c->norm_eps;
   dm->theta = (double)c->rope_theta;
+  dm->rope_halves = c->rope_layout == LLAMA_ROPE_HALVES ? 1 : 0;
+  dm->rope_scaling = RopeScaling();
+  if (scaled) {
+    dm->rope_scaling.factor = (double)c->rope_scaling_factor;
+    dm->rope_scaling.low = (double)c->rope_low_freq_factor;
+    dm->rope_scaling.high = (double)c->rope_high_freq_factor;
+    dm->rope_scaling.original_max_pos = (double)c->rope_original_max_pos;
+  }
   dm->dtype = c->dtype;
   dm->esize = c->dtype == LLAMA_BF16 ? 2 : 4;
   return LLAMA_OK;
@@ -187,8 +208,15 @@ llama_status copy_weights(const Dims &dm, const llama_block_weights *w, Allocs &
   };
   cp(out->attn_norm, w->attn_norm, dm.d * e);
   cp(out->ffn_norm, w->ffn_norm, dm.d * e);
-  cp(qkv, w->wq, dq);
-  cp(qkv + dq, w->wk, dkv);
+  if (dm.permute_halves()) {
+    if (err == cudaSuccess)
+      err = launch_permute_halves_rows((const bf16 *)w->wq, (bf16 *)qkv, dm.H, dm.D, dm.d, nullptr);
+    if (err == cudaSuccess)
+      err = launch_permute_halves_rows((const bf16 *)w->wk, (bf16 *)(qkv + dq), dm.G, dm.D, dm.d, nullptr);
+  } else {
+    cp(qkv, w->wq, dq);
+    cp(qkv + dq, w->wk, dkv);
+  }
   cp(qkv + dq + dkv, w->wv, dkv);
   cp(out->wo, w->wo, (size_t)dm.d * dm.H * dm.D * e);
   cp(out->w_down, w->w_down, (size_t)dm.d * dm.F * e);
@@ -227,7 +255,7 @@ llama_status alloc_workspace(const Dims &dm, int max_tokens, bool staging, Alloc
     ws->xn = al.alloc(T * dm.d * e);
     ws->hn = al.alloc(T * dm.d * e);
   }
-  if (dm.dtype != LLAMA_BF16 || dm.D % 32 != 0)  // unrotated qkv (the bf16 path rotates in the GEMM epilogue)
+  if (!dm.fused_qkv_rope())  // unrotated qkv (the bf16 path rotates in the GEMM epilogue)
     ws->qkv = al.alloc(T * dm.QKV * e);
   ws->q = al.alloc(T * dm.H * dm.D * e);
   ws->o = al.alloc(T * dm.H * dm.D * e);
@@ -271,7 +299,7 @@ llama_status forward_simt(const Dims &dm, const Weights &w, const Workspace &ws,
   LAUNCH(launch_rmsnorm<T>(x, (const T *)w.attn_norm, xn, M, dm.d, dm.eps, st));
   LAUNCH(launch_gemm_simt<T>(xn, (const T *)w.wqkv, nullptr, nullptr, qkv, M, dm.QKV, dm.d, EPI_STORE, st));
   LAUNCH(launch_rope_kv<T>(qkv, q, (T *)kv->k, (T *)kv->v, rope, B, S, start_pos, dm.H, dm.G, dm.D,
-                           kv->max_seq_len, st));
+                           kv->max_seq_len, dm.rope_halves, st));
   LAUNCH(launch_attention_simt<T>(q, (const T *)kv->k, (const T *)kv->v, o, B, S, start_pos, dm.H, dm.G, dm.D,
                                   kv->max_seq_len, st));
   LAUNCH(launch_gemm_simt<T>(o, (const T *)w.wo, nullptr, x, h, M, dm.d, dm.H * dm.D, EPI_RESIDUAL, st));
@@ -299,7 +327,7 @@ llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, c
   norm_x.ss_in = ws.ss_x;
   norm_x.eps = dm.eps;
   norm_x.d = dm.d;
-  if (dm.D % 32 == 0) {
+  if (dm.fused_qkv_rope()) {
     // QKV projection, RoPE and the cache write in one GEMM epilogue
     QkvScatter sc;
     sc.table = rope;
@@ -312,6 +340,7 @@ llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, c
     sc.G = dm.G;
     sc.D = dm.D;
     sc.cache_seq = kv->max_seq_len;
+    sc.halves = dm.rope_halves;
     pf.mark(1, 0, st);
     LAUNCH(launch_gemm_tc(x, (const bf16 *)w.wqkv, nullptr, nullptr, M, dm.QKV, dm.d, EPI_QKV_ROPE, status, st,
                           &ws.gemm, &norm_x, &sc, true));
@@ -324,7 +353,8 @@ llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, c
                           &ws.gemm, &norm_x, nullptr, true));
     pf.mark(1, 1, st);
     pf.mark(2, 0, st);
-    LAUNCH(launch_rope_kv<bf16>(qkv, q, kc, vc, rope, B, S, start_pos, dm.H, dm.G, dm.D, kv->max_seq_len, st));
+    LAUNCH(launch_rope_kv<bf16>(qkv, q, kc, vc, rope, B, S, start_pos, dm.H, dm.G, dm.D, kv->max_seq_len,
+                                dm.rope_halves, st));
     pf.mark(2, 1, st);
   }
   pf.mark(3, 0, st);
@@ -436,7 +466,7 @@ llama_status llama_block_create(const llama_config *cfg, const llama_block_weigh
     if (b->al.failed) s = LLAMA_ERR_OOM;
   }
   if (s == LLAMA_OK) {
-    if (launch_rope_table(b->rope, dm.max_seq, dm.D, dm.theta, nullptr) != cudaSuccess ||
+    if (launch_rope_table(b->rope, dm.max_seq, dm.D, dm.theta, dm.rope_scaling, nullptr) != cudaSuccess ||
         cudaMemset(b->status, 0, sizeof(int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
       s = LLAMA_ERR_CUDA;
   }
@@ -586,7 +616,7 @@ llama_status llama_stack_create(const llama_config *cfg, int32_t n_layers, int32
     cudaError_t err = cudaMemcpy(k->embed, embed, (size_t)vocab * dm.d * e, cudaMemcpyDeviceToDevice);
     if (err == cudaSuccess) err = cudaMemcpy(k->lm_head, lm_head, (size_t)vocab * dm.d * e, cudaMemcpyDeviceToDevice);
     if (err == cudaSuccess) err = cudaMemcpy(k->final_norm, final_norm, dm.d * e, cudaMemcpyDeviceToDevice);
-    if (err == cudaSuccess) err = launch_rope_table(k->rope, dm.max_seq, dm.D, dm.theta, nullptr);
+    if (err == cudaSuccess) err = launch_rope_table(k->rope, dm.max_seq, dm.D, dm.theta, dm.rope_scaling, nullptr);
     if (err == cudaSuccess) err = cudaMemset(k->status, 0, sizeof(int));
     if (err == cudaSuccess) err = cudaDeviceSynchronize();
     if (err != cudaSuccess) s = LLAMA_ERR_CUDA;

@@ -248,37 +248,55 @@ cudaError_t launch_gemm_simt(const T *A, const T *W, const T *W3, const T *R, vo
 
 // ------------------------------------------------------------ RoPE table ---
 // "Mini Llama 2 Implementation", Rotary positional embeddings: angle of pair i
-// at position p is p * theta^(-2i/D).  Built once per block in fp64, stored fp32.
-__global__ void rope_table_kernel(float2 *table, int max_seq, int D, double theta) {
+// at position p is p * theta^(-2i/D).  With a scaling factor > 1 the frequency
+// is stretched as "From GPT-2 to Llama: four changes and the reason for each",
+// Positions become a rotation describes for Llama 3.1: long wavelengths slowed
+// by the factor, short ones kept, linear blend in between.  Built once per
+// block in fp64, stored fp32.
+__device__ double rope_frequency(int i, int D, double theta, RopeScaling sc) {
+  const double f = pow(theta, -2.0 * (double)i / (double)D);
+  if (!(sc.factor > 1.0)) return f;
+  const double lam = 2.0 * 3.14159265358979323846 / f;
+  if (lam < sc.original_max_pos / sc.high) return f;
+  if (lam > sc.original_max_pos / sc.low) return f / sc.factor;
+  const double w = (sc.original_max_pos / lam - sc.low) / (sc.high - sc.low);
+  return (1.0 - w) * f / sc.factor + w * f;
+}
+
+__global__ void rope_table_kernel(float2 *table, int max_seq, int D, double theta, RopeScaling sc) {
   const int half = D / 2;
   const size_t n = (size_t)max_seq * half;
   for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < n; idx += (size_t)gridDim.x * blockDim.x) {
     const int p = (int)(idx / half), i = (int)(idx % half);
-    const double f = pow(theta, -2.0 * (double)i / (double)D);
+    const double f = rope_frequency(i, D, theta, sc);
     double s, c;
     sincos((double)p * f, &s, &c);
     table[idx] = make_float2((float)c, (float)s);
   }
 }
 
-cudaError_t launch_rope_table(float2 *table, int max_seq, int D, double theta, cudaStream_t st) {
+cudaError_t launch_rope_table(float2 *table, int max_seq, int D, double theta, const RopeScaling &sc,
+                              cudaStream_t st) {
   const size_t n = (size_t)max_seq * (D / 2);
   const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
   count_launch();
-  rope_table_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(table, max_seq, D, theta);
+  rope_table_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(table, max_seq, D, theta, sc);
   return cudaGetLastError();
 }
 
 // ------------------------------------------------------ RoPE + KV write ---
 // Each thread owns one 16-byte vector of a token's fused [q | k | v] row; a
-// vector never straddles a head (D % 8 == 0) and holds whole (2i, 2i+1) pairs.
-// q: rotated into q_out; k: rotated into the K cache at position start_pos + s;
-// v: copied into the V cache ("Full Llama 3 transformer block", How it works:
-// RoPE rotates Q and K, keys/values are written into a cache).
+// vector never straddles a head (D % 8 == 0).  Interleaved layout: the vector
+// holds whole (2i, 2i+1) pairs.  Halves layout: the thread of a vector in the
+// first half of a q / k head also loads the matching vector D/2 further on and
+// writes both (pairs (i, i + D/2)); threads of second-half vectors have nothing
+// to do.  q: rotated into q_out; k: rotated into the K cache at position
+// start_pos + s; v: copied into the V cache ("Full Llama 3 transformer block",
+// How it works: RoPE rotates Q and K, keys/values are written into a cache).
 template <typename T>
 __global__ void rope_kv_kernel(const T *__restrict__ qkv, T *__restrict__ q_out, T *__restrict__ kc,
                                T *__restrict__ vc, const float2 *__restrict__ table, int ntok, int S, int start_pos,
-                               int H, int G, int D, int cache_seq) {
+                               int H, int G, int D, int cache_seq, int halves) {
   constexpr int V = Vec16<T>::N;
   const int row_vecs = (H + 2 * G) * D / V;
   const size_t total = (size_t)ntok * row_vecs;
@@ -288,8 +306,16 @@ __global__ void rope_kv_kernel(const T *__restrict__ qkv, T *__restrict__ q_out,
   const int col = (int)(idx % row_vecs) * V;
   const int head = col / D, e = col % D;
   const int b = t / S, s = t % S, p = start_pos + s;
-  Vec16<T> x = load16(qkv + (size_t)t * (H + 2 * G) * D + col);
-  if (head < H + G) {
+  const T *src = qkv + (size_t)t * (H + 2 * G) * D + col;
+  Vec16<T> x = load16(src);
+  if (head >= H + G) {
+    const int g = head - H - G;
+    store16(vc + (((size_t)b * G + g) * cache_seq + p) * D + e, x);
+    return;
+  }
+  T *dst = head < H ? q_out + (size_t)t * H * D + head * D
+                    : kc + (((size_t)b * G + (head - H)) * cache_seq + p) * D;
+  if (!halves) {
     const float2 *cs = table + (size_t)p * (D / 2) + e / 2;
     Vec16<T> o;
 #pragma unroll
@@ -299,28 +325,34 @@ __global__ void rope_kv_kernel(const T *__restrict__ qkv, T *__restrict__ q_out,
       o.set(2 * k, a * c.x - bb * c.y);
       o.set(2 * k + 1, a * c.y + bb * c.x);
     }
-    if (head < H) {
-      store16(q_out + (size_t)t * H * D + col, o);
-    } else {
-      const int g = head - H;
-      store16(kc + (((size_t)b * G + g) * cache_seq + p) * D + e, o);
+    store16(dst + e, o);
+  } else if (e < D / 2) {
+    const float2 *cs = table + (size_t)p * (D / 2) + e;
+    Vec16<T> y = load16(src + D / 2);
+    Vec16<T> lo, hi;
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const float2 c = cs[k];
+      const float a = x.get(k), bb = y.get(k);
+      lo.set(k, a * c.x - bb * c.y);
+      hi.set(k, a * c.y + bb * c.x);
     }
-  } else {
-    const int g = head - H - G;
-    store16(vc + (((size_t)b * G + g) * cache_seq + p) * D + e, x);
+    store16(dst + e, lo);
+    store16(dst + e + D / 2, hi);
   }
 }
 
 template <typename T>
 cudaError_t launch_rope_kv(const T *qkv, T *q_out, T *kc, T *vc, const float2 *table, int B, int S,
-                           int start_pos, int H, int G, int D, int cache_seq, cudaStream_t st) {
+                           int start_pos, int H, int G, int D, int cache_seq, int halves, cudaStream_t st) {
   constexpr int V = Vec16<T>::N;
   const size_t total = (size_t)B * S * ((H + 2 * G) * D / V);
   if (total == 0) return cudaSuccess;
+  if (halves && (D / 2) % V != 0) return cudaErrorInvalidValue;
   const int threads = 256;
   count_launch();
   rope_kv_kernel<T><<<(unsigned)((total + threads - 1) / threads), threads, 0, st>>>(
-      qkv, q_out, kc, vc, table, B * S, S, start_pos, H, G, D, cache_seq);
+      qkv, q_out, kc, vc, table, B * S, S, start_pos, H, G, D, cache_seq, halves);
   return cudaGetLastError();
 }
 
@@ -503,7 +535,7 @@ cudaError_t launch_gather_last_rows(const T *x, T *out, int B, int S, int d, cud
   template cudaError_t launch_gemm_simt<T>(const T *, const T *, const T *, const T *, void *, int, int, int, int, \
                                            cudaStream_t);                                                         \
   template cudaError_t launch_rope_kv<T>(const T *, T *, T *, T *, const float2 *, int, int, int, int, int, int,  \
-                                         int, cudaStream_t);                                                      \
+                                         int, int, cudaStream_t);                                                 \
   template cudaError_t launch_attention_simt<T>(const T *, const T *, const T *, T *, int, int, int, int, int,    \
                                                 int, int, cudaStream_t);                                          \
   template cudaError_t launch_embed<T>(const int32_t *, const T *, T *, int, int, int, int *, cudaStream_t);    \

@@ -50,10 +50,13 @@ struct RowNorm {
 // and [(H+G) D, (H+2G) D) v.  q and k pairs (2i, 2i+1) of each head are
 // rotated by table[p][i] = {cos, sin}; rotated q goes to q [T][H D], rotated k
 // and v to kc / vc [batch][G][cache_seq][D].  Needs D % 32 == 0.
+// halves = 1: the q / k rows of W were reordered by launch_permute_halves_rows,
+// so accumulator columns (2i, 2i+1) of a head hold components (i, i + D/2); the
+// pair is rotated as above and stored back at i and i + D/2 (natural order).
 struct QkvScatter {
   const float2 *table = nullptr;
   bf16 *q = nullptr, *kc = nullptr, *vc = nullptr;
-  int S = 1, start_pos = 0, H = 0, G = 0, D = 0, cache_seq = 0;
+  int S = 1, start_pos = 0, H = 0, G = 0, D = 0, cache_seq = 0, halves = 0;
 };
 
 // status: device status word for bounded-wait expiry (may be null).
@@ -66,6 +69,11 @@ cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C,
                            int *status, cudaStream_t st, const GemmWorkspace *ws = nullptr,
                            const RowNorm *norm = nullptr, const QkvScatter *scatter = nullptr,
                            bool weights_static = false);
+
+// Reorder the rows of each of `heads` consecutive D-row heads of W [heads*D][d]:
+// out row 2i <- row i, out row 2i+1 <- row i + D/2 (the halves RoPE pairs become
+// adjacent output columns of x W^T).  d % 8 == 0.
+cudaError_t launch_permute_halves_rows(const bf16 *W, bf16 *out, int heads, int D, int d, cudaStream_t st);
 
 // out[32j + i] = gate[16j + i], out[32j + 16 + i] = up[16j + i] (rows of width d), F % 16 == 0.
 cudaError_t launch_interleave_rows(const bf16 *gate, const bf16 *up, bf16 *out, int F, int d, cudaStream_t st);

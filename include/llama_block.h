@@ -54,6 +54,13 @@ typedef enum {
 
 typedef enum { LLAMA_F32 = 0, LLAMA_BF16 = 1 } llama_dtype;
 
+/* Which components of a head RoPE rotates together ("The Evolving Transformer
+ * 04 · LLaMA", §02 RoPE and "Mini Llama 2 Implementation": interleaved pairs
+ * (2i, 2i+1); "From GPT-2 to Llama: four changes and the reason for each",
+ * Positions become a rotation: halves, pair i = (i, i + d_head/2), the
+ * rotate_half form).  Pair i turns at the same frequency in both layouts. */
+typedef enum { LLAMA_ROPE_INTERLEAVED = 0, LLAMA_ROPE_HALVES = 1 } llama_rope_layout;
+
 /* Fields follow LlamaConfig / ModelArgs ("The Evolving Transformer 04 · LLaMA",
  * §00 Config; "Full Llama 3 transformer block", How it works).  d_head is
  * derived as d_model / n_heads.  max_seq_len bounds start_pos + S and sizes the
@@ -69,6 +76,20 @@ typedef struct {
     float norm_eps;
     float rope_theta;
     int32_t dtype; /* llama_dtype */
+    /* RoPE variants ("From GPT-2 to Llama: four changes and the reason for
+     * each", Positions become a rotation).  Zero-initialised fields give the
+     * interleaved layout without scaling. */
+    int32_t rope_layout;           /* llama_rope_layout */
+    /* Llama 3.1 frequency stretch, applied when rope_scaling_factor > 1: with
+     * wavelength lam_i = 2 pi / f_i and L = rope_original_max_pos, pairs with
+     * lam_i < L / rope_high_freq_factor keep f_i, pairs with lam_i >
+     * L / rope_low_freq_factor turn at f_i / rope_scaling_factor, and in
+     * between f_i is blended as (1 - w) f_i / factor + w f_i with
+     * w = (L / lam_i - low) / (high - low).  Requires 0 < low < high and L > 0. */
+    float rope_scaling_factor;
+    float rope_low_freq_factor;
+    float rope_high_freq_factor;
+    int32_t rope_original_max_pos;
 } llama_config;
 
 /* Device pointers to one block's parameters, dtype = config.dtype.

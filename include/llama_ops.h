@@ -47,17 +47,26 @@ llama_status llama_op_attention(int32_t dtype, const void *q, const llama_kv_cac
 
 /* RoPE cos/sin table: table[p][i] = {cos(p f_i), sin(p f_i)}, f_i = theta^(-2i/D),
  * p in [0, max_seq), i in [0, D/2), fp32 pairs computed in fp64 ("Mini Llama 2
- * Implementation", Rotary positional embeddings).  table: float[max_seq][D/2][2]. */
-llama_status llama_op_rope_table(float *table, int32_t max_seq, int32_t D, float theta, llama_stream stream);
+ * Implementation", Rotary positional embeddings).  table: float[max_seq][D/2][2].
+ * scaling_factor > 1 applies the Llama 3.1 stretch to f_i with low_freq_factor,
+ * high_freq_factor and original_max_pos exactly as the llama_config fields of the
+ * same names describe; scaling_factor <= 1 leaves f_i unscaled (the other three
+ * are then ignored). */
+llama_status llama_op_rope_table(float *table, int32_t max_seq, int32_t D, float theta, float scaling_factor,
+                                 float low_freq_factor, float high_freq_factor, int32_t original_max_pos,
+                                 llama_stream stream);
 
 /* RoPE + KV-cache write: qkv [B*S][(H + 2G) D] holds, per token, q (H heads),
  * k (G heads), v (G heads).  Writes q rotated at position start_pos + s to
  * q_out [B*S][H][D], k rotated to kv->k[b][g][start_pos + s], v unrotated to
- * kv->v[b][g][start_pos + s]; nothing else in the cache changes.
+ * kv->v[b][g][start_pos + s]; nothing else in the cache changes.  layout
+ * (llama_rope_layout) picks the pairs rotated together; the vectors keep their
+ * natural component order in both layouts.
  * table from llama_op_rope_table with max_seq >= start_pos + S. */
 llama_status llama_op_rope_kv_write(int32_t dtype, const void *qkv, void *q_out, const llama_kv_cache *kv,
                                     const float *table, int32_t table_max_seq, int32_t B, int32_t S,
-                                    int32_t start_pos, int32_t H, int32_t G, int32_t D, llama_stream stream);
+                                    int32_t start_pos, int32_t H, int32_t G, int32_t D, int32_t layout,
+                                    llama_stream stream);
 
 /* Decode-step attention that allocates nothing.  The method's pages have no
  * counterpart: this entry point exists for callers that cannot allocate device

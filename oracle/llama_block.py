@@ -42,7 +42,7 @@ import math
 import numpy as np
 
 __all__ = [
-    "rms_norm", "rope_frequencies", "rope", "silu", "linear", "gqa_attention",
+    "rms_norm", "rope_frequencies", "scale_rope_frequencies", "rope", "silu", "linear", "gqa_attention",
     "gqa_attention_rows", "block_forward", "block_forward_rows", "stack_forward", "greedy_generate",
     "ffn_hidden_dim", "kv_values_per_token", "block_param_count", "model_param_count",
 ]
@@ -59,35 +59,83 @@ def rms_norm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
     return x / np.sqrt(ms + eps) * np.asarray(g, dtype=np.float64)
 
 
-def rope_frequencies(d_head: int, theta: float) -> np.ndarray:
+def rope_frequencies(d_head: int, theta: float, scaling=None) -> np.ndarray:
     """Angular frequency of pair i: theta^(-2i / d_head), i = 0 .. d_head/2 - 1.
 
     [ML2] Rotary positional embeddings (theta ** (-2 * arange(D/2) / D));
     [L4S] Worked example; [EVT] §02 (base^(arange(0, D, 2) / D) inverted).
+    With ``scaling`` (a dict, see :func:`scale_rope_frequencies`) the
+    frequencies are stretched for contexts longer than the trained one.
     """
     i = np.arange(d_head // 2, dtype=np.float64)
-    return np.power(float(theta), -2.0 * i / d_head)
+    f = np.power(float(theta), -2.0 * i / d_head)
+    return f if scaling is None else scale_rope_frequencies(f, scaling)
 
 
-def rope(x: np.ndarray, positions: np.ndarray, theta: float) -> np.ndarray:
-    """Rotate interleaved pairs (x[2i], x[2i+1]) of x[..., S, heads, D] by p_s * f_i.
+def scale_rope_frequencies(f: np.ndarray, scaling: dict) -> np.ndarray:
+    """Llama 3.1 frequency stretch.  [G2L] Positions become a rotation: the
+    slowest pairs are slowed by the factor, the fastest are left alone and the
+    ones between are blended.
+
+    scaling = {factor, low_freq_factor, high_freq_factor, original_max_pos}.
+    A pair's wavelength is lam = 2 pi / f.  Pairs with lam shorter than
+    original_max_pos / high_freq_factor keep f; pairs with lam longer than
+    original_max_pos / low_freq_factor get f / factor; in between, f is blended
+    linearly, (1 - w) f / factor + w f, with the weight
+    w = (original_max_pos / lam - low_freq_factor) / (high_freq_factor - low_freq_factor),
+    which is 1 at the short-wavelength edge and 0 at the long one.  The pages
+    state the three bands, not the blend; the linear blend in turns-per-context
+    is the reading taken (it is continuous at both edges).
+    """
+    f = np.asarray(f, dtype=np.float64)
+    factor = float(scaling["factor"])
+    lo, hi = float(scaling["low_freq_factor"]), float(scaling["high_freq_factor"])
+    orig = float(scaling["original_max_pos"])
+    lam = 2.0 * math.pi / f
+    out = np.empty_like(f)
+    for i, (fi, li) in enumerate(zip(f, lam)):
+        if li < orig / hi:
+            out[i] = fi
+        elif li > orig / lo:
+            out[i] = fi / factor
+        else:
+            w = (orig / li - lo) / (hi - lo)
+            out[i] = (1.0 - w) * fi / factor + w * fi
+    return out
+
+
+def rope(x: np.ndarray, positions: np.ndarray, theta: float, layout: str = "interleaved",
+         scaling=None) -> np.ndarray:
+    """Rotate the pairs of x[..., S, heads, D] by p_s * f_i.
 
     (a, b) -> (a cos - b sin, a sin + b cos) with p_s = positions[s].
-    [EVT] §02 RoPE (even/odd split, rotate, stack); [ML2] Rotary positional
-    embeddings (reshape(-1, 2) real/imag form); [L3B] How it works (positions
-    start_pos .. start_pos + S - 1).
+    layout "interleaved": pair i is (x[2i], x[2i+1]) -- [EVT] §02 RoPE
+    (even/odd split, rotate, stack); [ML2] Rotary positional embeddings
+    (reshape(-1, 2) real/imag form).  layout "halves": pair i is (x[i],
+    x[i + D/2]) -- [G2L] Positions become a rotation (q cos + rotate_half(q)
+    sin).  [L3B] How it works (positions start_pos .. start_pos + S - 1).
     """
     x = np.asarray(x, dtype=np.float64)
     D = x.shape[-1]
-    ang = np.asarray(positions, dtype=np.float64)[:, None] * rope_frequencies(D, theta)[None, :]
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * rope_frequencies(D, theta, scaling)[None, :]
     cos = np.cos(ang)[:, None, :]  # [S, 1, D/2] broadcast over heads
     sin = np.sin(ang)[:, None, :]
-    a = x[..., 0::2]
-    b = x[..., 1::2]
+    if layout == "interleaved":
+        ia, ib = slice(0, D, 2), slice(1, D, 2)
+    elif layout == "halves":
+        ia, ib = slice(0, D // 2), slice(D // 2, D)
+    else:
+        raise ValueError(f"unknown RoPE layout {layout!r}")
+    a = x[..., ia]
+    b = x[..., ib]
     out = np.empty_like(x)
-    out[..., 0::2] = a * cos - b * sin
-    out[..., 1::2] = a * sin + b * cos
+    out[..., ia] = a * cos - b * sin
+    out[..., ib] = a * sin + b * cos
     return out
+
+
+def _rope_cfg(cfg, x, positions):
+    return rope(x, positions, cfg["rope_theta"], cfg.get("rope_layout", "interleaved"), cfg.get("rope_scaling"))
 
 
 def silu(z: np.ndarray) -> np.ndarray:
@@ -178,8 +226,8 @@ def _project_qkv(cfg, w, x, start_pos):
     k = linear(u, w["wk"]).reshape(B, S, G, D)
     v = linear(u, w["wv"]).reshape(B, S, G, D)
     pos = start_pos + np.arange(S)
-    q = rope(q, pos, cfg["rope_theta"])
-    k = rope(k, pos, cfg["rope_theta"])
+    q = _rope_cfg(cfg, q, pos)
+    k = _rope_cfg(cfg, k, pos)
     return q, k, v
 
 
@@ -239,7 +287,7 @@ def block_forward_rows(cfg: dict, w: dict, x: np.ndarray, start_pos: int, k_cach
     B, S, _ = x.shape
     u = rms_norm(x, w["attn_norm"], cfg["norm_eps"])
     pos = start_pos + np.arange(S)
-    k = rope(linear(u, w["wk"]).reshape(B, S, G, D), pos, cfg["rope_theta"])
+    k = _rope_cfg(cfg, linear(u, w["wk"]).reshape(B, S, G, D), pos)
     v = linear(u, w["wv"]).reshape(B, S, G, D)
     kc, vc = _write_cache(np.asarray(k_cache[:B], dtype=np.float64), np.asarray(v_cache[:B], dtype=np.float64),
                           k, v, start_pos)
@@ -247,7 +295,7 @@ def block_forward_rows(cfg: dict, w: dict, x: np.ndarray, start_pos: int, k_cach
     bi, si = rows[:, 0], rows[:, 1]
     ur = u[bi, si]  # [n, d]
     qr = linear(ur, w["wq"]).reshape(-1, 1, H, D)
-    qr = np.stack([rope(qr[t:t + 1], np.array([start_pos + si[t]]), cfg["rope_theta"])[0, 0]
+    qr = np.stack([_rope_cfg(cfg, qr[t:t + 1], np.array([start_pos + si[t]]))[0, 0]
                    for t in range(len(si))]) if len(si) else qr.reshape(0, H, D)
     o = gqa_attention_rows(qr, bi, start_pos + si, kc, vc).reshape(-1, H * D)
     h = x[bi, si] + linear(o, w["wo"])

@@ -103,9 +103,11 @@ def llama_dtype(shape):
 
 def make_cfg(shape, max_seq_len=None):
     import decoder_block_gb300 as lb
+    layout = {"interleaved": lb.LLAMA_ROPE_INTERLEAVED, "halves": lb.LLAMA_ROPE_HALVES}[
+        shape.get("rope_layout", "interleaved")]
     return lb.make_config(shape["d_model"], shape["n_heads"], shape["n_kv_heads"], shape["d_ff"],
                           max_seq_len or shape["max_seq_len"], shape["norm_eps"], shape["rope_theta"],
-                          llama_dtype(shape))
+                          llama_dtype(shape), layout, shape.get("rope_scaling"))
 
 
 def f64_weights(w: dict) -> dict:

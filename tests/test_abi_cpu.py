@@ -69,6 +69,14 @@ def test_status_strings(lib):
     (dict(norm_eps=-1.0), "LLAMA_ERR_INVALID_ARG"),
     (dict(rope_theta=0.0), "LLAMA_ERR_INVALID_ARG"),
     (dict(d_ff=14336 + 8), "LLAMA_ERR_UNSUPPORTED"),         # bf16 gate/up interleave needs d_ff % 16
+    (dict(rope_layout=2), "LLAMA_ERR_INVALID_ARG"),           # neither interleaved nor halves
+    (dict(rope_scaling=dict(factor=8.0, low_freq_factor=0.0, high_freq_factor=4.0, original_max_pos=8192)),
+     "LLAMA_ERR_INVALID_ARG"),                                # stretch needs 0 < low < high
+    (dict(rope_scaling=dict(factor=8.0, low_freq_factor=4.0, high_freq_factor=1.0, original_max_pos=8192)),
+     "LLAMA_ERR_INVALID_ARG"),
+    (dict(rope_scaling=dict(factor=8.0, low_freq_factor=1.0, high_freq_factor=4.0, original_max_pos=0)),
+     "LLAMA_ERR_INVALID_ARG"),
+    (dict(rope_scaling=dict(factor=float("nan"))), "LLAMA_ERR_INVALID_ARG"),
 ])
 def test_create_rejects_bad_configs_before_touching_the_gpu(lib, fields, expected):
     base = dict(d_model=4096, n_heads=32, n_kv_heads=8, d_ff=14336, max_seq_len=8192, norm_eps=1e-5,

@@ -72,6 +72,28 @@ def test_ragged_and_offset_shapes_bf16(B, S, start_pos, L):
     _check_full(s, B, S, start_pos, L, fill_upto=start_pos, tag=f"xr{B}{S}")
 
 
+LLAMA31_SCALING = dict(factor=8.0, low_freq_factor=1.0, high_freq_factor=4.0, original_max_pos=8192)
+
+
+@pytest.mark.parametrize("name,dtype", [("tiny_f32", "f32"), ("tiny_f32", "bf16"), ("smollm2_135m", "bf16")])
+def test_halves_rope_layout_block(name, dtype):
+    """Pairs (i, i + D/2): the CUDA-core path and the d_head-16 bf16 path rotate in the standalone kernel,
+    the SmolLM2-shaped bf16 block in the QKV epilogue over reordered weight rows."""
+    shape = dict(synth.SHAPES[name], dtype=dtype, rope_layout="halves")
+    _check_full(shape, 2, 40, 0, 48, tag="halves")
+    _check_full(shape, 3, 1, 30, 40, fill_upto=30, tag="halves_dec")
+
+
+@pytest.mark.parametrize("layout", ["interleaved", "halves"])
+def test_llama31_scaled_rope_past_the_original_context(layout):
+    """Llama 3.1 frequency stretch at positions beyond the 8192 the unscaled model was trained at:
+    a prefill chunk at 12000 and a decode step at 20000 over pre-filled caches."""
+    shape = dict(synth.SHAPES["llama3_8b_prefill_b1s8192"], rope_layout=layout, rope_scaling=LLAMA31_SCALING,
+                 max_seq_len=20004)
+    _check_full(shape, 1, 40, 12000, 12040, fill_upto=12000, tag="scaled")
+    _check_full(shape, 2, 1, 20000, 20004, fill_upto=20000, tag="scaled_dec")
+
+
 def test_tiny_f32_decode_after_prefix():
     s = dict(synth.SHAPES["tiny_f32"], max_seq_len=24)
     _check_full(s, 2, 1, 9, 24, fill_upto=9, tag="xd")

@@ -93,12 +93,19 @@ def test_rmsnorm(lb, T, d, dtype):
 
 # ------------------------------------------------------- RoPE + KV write ---
 
-@pytest.mark.parametrize("B,S,start_pos,H,G,D,dtype,theta", [
-    (1, 16, 0, 4, 2, 16, "f32", 1e4),
-    (3, 37, 5, 9, 3, 64, "bf16", 1e5),
-    (2, 70, 4000, 32, 8, 128, "bf16", 5e5),
+LLAMA31_SCALING = dict(factor=8.0, low_freq_factor=1.0, high_freq_factor=4.0, original_max_pos=8192)
+
+
+@pytest.mark.parametrize("B,S,start_pos,H,G,D,dtype,theta,layout,scaling", [
+    (1, 16, 0, 4, 2, 16, "f32", 1e4, "interleaved", None),
+    (3, 37, 5, 9, 3, 64, "bf16", 1e5, "interleaved", None),
+    (2, 70, 4000, 32, 8, 128, "bf16", 5e5, "interleaved", None),
+    (1, 16, 3, 4, 2, 16, "f32", 1e4, "halves", None),
+    (3, 37, 5, 9, 3, 64, "bf16", 1e5, "halves", None),
+    (2, 9, 20000, 8, 2, 128, "bf16", 5e5, "halves", LLAMA31_SCALING),
+    (1, 12, 30000, 4, 2, 128, "f32", 5e5, "interleaved", LLAMA31_SCALING),
 ])
-def test_rope_kv_write(lb, B, S, start_pos, H, G, D, dtype, theta):
+def test_rope_kv_write(lb, B, S, start_pos, H, G, D, dtype, theta, layout, scaling):
     t = torch()
     conv = (lambda a: a) if dtype == "f32" else synth.f32_to_bf16_bits
     L = start_pos + S + 3
@@ -106,17 +113,18 @@ def test_rope_kv_write(lb, B, S, start_pos, H, G, D, dtype, theta):
     k0 = conv(synth.normal(0, "ops/k0", (B + 1, G, L, D)))
     v0 = conv(synth.normal(0, "ops/v0", (B + 1, G, L, D)))
     table = t.empty((L, D // 2, 2), dtype=t.float32, device="cuda")
-    lb.check(lb.llama_op_rope_table(table, L, D, theta))
+    lb.check(lb.llama_op_rope_table(table, L, D, theta, scaling))
     qd, kd, vd = to_dev(qkv), to_dev(k0), to_dev(v0)
     q_out = t.empty((B * S, H * D), dtype=qd.dtype, device="cuda")
     kv = lb.make_kv_cache(kd, vd, B + 1, L)
     dt = lb.LLAMA_BF16 if dtype == "bf16" else lb.LLAMA_F32
-    lb.check(lb.llama_op_rope_kv_write(dt, qd, q_out, kv, table, L, B, S, start_pos, H, G, D))
+    lcode = lb.LLAMA_ROPE_HALVES if layout == "halves" else lb.LLAMA_ROPE_INTERLEAVED
+    lb.check(lb.llama_op_rope_kv_write(dt, qd, q_out, kv, table, L, B, S, start_pos, H, G, D, lcode))
     t.cuda.synchronize()
     x = synth.as_f64(qkv).reshape(B, S, H + 2 * G, D)
     pos = start_pos + np.arange(S)
-    q_ref = oracle.rope(x[:, :, :H], pos, theta)
-    k_ref = oracle.rope(x[:, :, H:H + G], pos, theta)
+    q_ref = oracle.rope(x[:, :, :H], pos, theta, layout, scaling)
+    k_ref = oracle.rope(x[:, :, H:H + G], pos, theta, layout, scaling)
     v_ref = x[:, :, H + G:]
     assert_parity(to_f64(q_out).reshape(B, S, H, D), q_ref, dtype, "rotated q")
     kg, vg = to_f64(kd), to_f64(vd)
@@ -130,7 +138,7 @@ def test_rope_kv_write(lb, B, S, start_pos, H, G, D, dtype, theta):
     np.testing.assert_array_equal(vg[mask], vb[mask])
     # the table itself: fp32 rounding of cos/sin of the exact angle
     tab = table.cpu().numpy().astype(np.float64)
-    ang = np.arange(L)[:, None] * oracle.rope_frequencies(D, theta)[None, :]
+    ang = np.arange(L)[:, None] * oracle.rope_frequencies(D, theta, scaling)[None, :]
     assert np.max(np.abs(tab[..., 0] - np.cos(ang))) < 1e-6
     assert np.max(np.abs(tab[..., 1] - np.sin(ang))) < 1e-6
 

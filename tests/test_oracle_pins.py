@@ -116,6 +116,99 @@ def test_rope_equals_complex_multiplication_on_interleaved_pairs():
     assert np.max(np.abs(halves - oracle.rope(x, pos, theta))) > 1e-2
 
 
+def _halves_to_interleaved(D):
+    """Index map: interleaved position 2i <- halves position i, 2i+1 <- i + D/2."""
+    idx = np.empty(D, dtype=np.int64)
+    idx[0::2] = np.arange(D // 2)
+    idx[1::2] = np.arange(D // 2) + D // 2
+    return idx
+
+
+def test_rope_halves_equals_complex_multiplication_on_halves():
+    # the halves form: (x[i] + j x[i + D/2]) * exp(j p f_i)
+    D, theta = 16, 1e5
+    x = _rng("rope_h", (3, 2, D))
+    pos = np.array([0.0, 9.0, 3000.0])
+    zc = x[..., : D // 2] + 1j * x[..., D // 2:]
+    f = theta ** (-np.arange(0, D, 2) / D)
+    w = zc * np.exp(1j * pos[:, None, None] * f[None, None, :])
+    ref = np.concatenate([w.real, w.imag], -1)
+    np.testing.assert_allclose(oracle.rope(x, pos, theta, layout="halves"), ref, rtol=0, atol=1e-12)
+
+
+def test_rope_halves_is_interleaved_rope_of_the_permuted_vector():
+    # Reordering each head as (x0, x_{D/2}, x1, x_{D/2+1}, ...) turns the halves rotation into the
+    # interleaved one; dot products are unchanged by a common reordering of q and k.
+    D, theta = 32, 5e5
+    x = _rng("rope_p", (4, 3, D))
+    pos = np.array([1.0, 17.0, 4095.0, 20000.0])
+    idx = _halves_to_interleaved(D)
+    via_interleaved = np.empty_like(x)
+    via_interleaved[..., idx] = oracle.rope(x[..., idx], pos, theta)
+    np.testing.assert_allclose(oracle.rope(x, pos, theta, layout="halves"), via_interleaved, rtol=0, atol=1e-12)
+
+
+def test_rope_halves_score_depends_only_on_offset_and_keeps_norms():
+    D, theta = 64, 1e5
+    q = _rng("rope_hq", (1, 1, D))
+    k = _rng("rope_hk", (1, 1, D))
+
+    def score(m, n):
+        return float(np.sum(oracle.rope(q, np.array([m]), theta, "halves") *
+                            oracle.rope(k, np.array([n]), theta, "halves")))
+
+    assert abs(score(10, 3) - score(1010, 1003)) <= 1e-12 * abs(score(10, 3))
+    assert abs(score(10, 3) - score(10, 4)) > 1e-3
+    y = oracle.rope(q, np.array([321.0]), theta, "halves")
+    np.testing.assert_allclose(np.linalg.norm(y), np.linalg.norm(q), rtol=1e-13)
+
+
+LLAMA31_SCALING = dict(factor=8.0, low_freq_factor=1.0, high_freq_factor=4.0, original_max_pos=8192)
+
+
+def test_rope_scaling_bands_match_printed_counts():
+    g = GOLDEN["rope_scaling_llama31_8b"]
+    f = oracle.rope_frequencies(g["d_head"], g["theta"])
+    fs = oracle.rope_frequencies(g["d_head"], g["theta"], LLAMA31_SCALING)
+    assert len(f) == g["pairs"]
+    ratio = f / fs
+    unchanged = int(np.sum(np.abs(ratio - 1.0) < 1e-12))
+    slowed = int(np.sum(np.abs(ratio - g["slow_factor"]) < 1e-9))
+    blended = int(np.sum((ratio > 1.0 + 1e-12) & (ratio < g["slow_factor"] - 1e-9)))
+    assert (unchanged, slowed, blended) == (g["unchanged"], g["slowed"], g["blended"])
+    # the fastest pairs are the unchanged ones, the slowest the slowed ones
+    assert np.all(np.abs(ratio[: g["unchanged"]] - 1.0) < 1e-12)
+    assert np.all(np.abs(ratio[-g["slowed"]:] - g["slow_factor"]) < 1e-9)
+    assert g["max_pos"] // g["original_max_pos"] == 16  # 8192 -> 131072 positions
+
+
+def test_rope_scaling_is_continuous_and_monotone():
+    orig, lo, hi, fac = 8192.0, 1.0, 4.0, 8.0
+    sc = dict(factor=fac, low_freq_factor=lo, high_freq_factor=hi, original_max_pos=orig)
+    eps = 1e-9
+    for lam in (orig / hi, orig / lo):  # the two band edges
+        f_in, f_out = 2 * math.pi / (lam * (1 - eps)), 2 * math.pi / (lam * (1 + eps))
+        a, b = oracle.scale_rope_frequencies(np.array([f_in, f_out]), sc)
+        assert abs(a - b) <= 1e-6 * a
+    lam = np.linspace(100.0, 3 * orig, 2001)
+    fs = oracle.scale_rope_frequencies(2 * math.pi / lam, sc)
+    assert np.all(np.diff(fs) < 0)  # longer wavelength, lower scaled frequency
+    # factor 1 is the identity
+    f = oracle.rope_frequencies(128, 5e5)
+    np.testing.assert_allclose(oracle.scale_rope_frequencies(f, dict(sc, factor=1.0)), f, rtol=1e-15, atol=0)
+
+
+def test_rope_with_scaling_rotates_by_the_scaled_frequencies():
+    D, theta = 128, 5e5
+    x = np.zeros((1, 1, D))
+    x[0, 0, 2 * 63] = 1.0  # the slowest pair
+    p = 100000.0
+    y = oracle.rope(x, np.array([p]), theta, scaling=LLAMA31_SCALING)
+    a = p * theta ** (-126.0 / D) / 8.0
+    assert y[0, 0, 126] == pytest.approx(math.cos(a), abs=1e-12)
+    assert y[0, 0, 127] == pytest.approx(math.sin(a), abs=1e-12)
+
+
 # ------------------------------------------------------------- RMSNorm -------
 
 def test_rmsnorm_unit_gain_gives_unit_rms():
