@@ -44,6 +44,7 @@ import numpy as np
 __all__ = [
     "rms_norm", "rope_frequencies", "scale_rope_frequencies", "rope", "silu", "linear", "gqa_attention",
     "gqa_attention_rows", "block_forward", "block_forward_rows", "stack_forward", "greedy_generate",
+    "swiglu", "moe_route", "moe_ffn",
     "ffn_hidden_dim", "kv_values_per_token", "block_param_count", "model_param_count",
 ]
 
@@ -241,15 +242,63 @@ def _write_cache(k_cache, v_cache, k, v, start_pos):
     return kc, vc
 
 
-def _ffn(cfg, w, h):
-    """ffn_norm then SwiGLU: W2(SiLU(W1 v) * W3 v).  [L3B] How it works; [EVT] §04."""
+def swiglu(v: np.ndarray, w_gate, w_up, w_down) -> np.ndarray:
+    """W2(SiLU(W1 v) * W3 v).  [EVT] §04 SwiGLU; [L3B] How it works."""
+    return linear(silu(linear(v, w_gate)) * linear(v, w_up), w_down)
+
+
+def moe_route(cfg: dict, w: dict, v: np.ndarray):
+    """Router of a mixture-of-experts feed-forward: logits = v W_router^T over
+    the n_experts experts; each token goes to the top_k largest logits (the
+    lowest expert id among equal logits), weighted by a softmax over the
+    logits of the chosen experts.  [G2L] The feed-forward grows a gate (a small
+    layer that picks a few feed-forwards per token); [L4S] MoE (top-k of N
+    experts, compute scales with k).  The pages name the top-k choice, not how
+    the chosen outputs are weighted: a softmax over the chosen logits is the
+    reading taken.
+    Returns (ids int [T, k], weights [T, k], logits [T, E]) for v [T, d].
+    """
+    k = int(cfg["top_k"])
+    logits = linear(v, w["router"])
+    ids = np.argsort(-logits, axis=-1, kind="stable")[:, :k]  # stable: equal logits keep id order
+    top = np.take_along_axis(logits, ids, -1)
+    e = np.exp(top - top.max(-1, keepdims=True))
+    return ids, e / e.sum(-1, keepdims=True), logits
+
+
+def moe_ffn(cfg: dict, w: dict, v: np.ndarray, route=None) -> np.ndarray:
+    """Mixture-of-experts SwiGLU feed-forward on normalised tokens v [..., d]:
+    sum over the k chosen experts of weight * expert_e(v), plus the always-on
+    shared expert when the block has one.  [L4S] MoE with a shared expert
+    (Llama 4 keeps one shared expert every token uses).  Experts are stacked:
+    w_gate, w_up [E, F, d], w_down [E, d, F]; shared_gate, shared_up [F_s, d],
+    shared_down [d, F_s].  route = (ids, weights) overrides the router's
+    choice (used to evaluate the block on another implementation's routing).
+    """
+    shp = v.shape
+    v = np.asarray(v, dtype=np.float64).reshape(-1, shp[-1])
+    ids, wts = route if route is not None else moe_route(cfg, w, v)[:2]
+    out = np.zeros_like(v)
+    for e in np.unique(ids):
+        rows, slot = np.nonzero(ids == e)
+        ye = swiglu(v[rows], w["w_gate"][e], w["w_up"][e], w["w_down"][e])
+        np.add.at(out, rows, wts[rows, slot][:, None] * ye)
+    if cfg.get("d_ff_shared", 0):
+        out = out + swiglu(v, w["shared_gate"], w["shared_up"], w["shared_down"])
+    return out.reshape(shp)
+
+
+def _ffn(cfg, w, h, route=None):
+    """ffn_norm then the feed-forward: SwiGLU W2(SiLU(W1 v) * W3 v) ([L3B] How
+    it works; [EVT] §04), or the mixture of experts when cfg has n_experts."""
     v2 = rms_norm(h, w["ffn_norm"], cfg["norm_eps"])
-    a = silu(linear(v2, w["w_gate"])) * linear(v2, w["w_up"])
-    return linear(a, w["w_down"])
+    if cfg.get("n_experts", 0):
+        return moe_ffn(cfg, w, v2, route)
+    return swiglu(v2, w["w_gate"], w["w_up"], w["w_down"])
 
 
 def block_forward(cfg: dict, w: dict, x: np.ndarray, start_pos: int, k_cache: np.ndarray,
-                  v_cache: np.ndarray):
+                  v_cache: np.ndarray, route=None):
     """One pre-norm block: h = x + Attn(RMSNorm(x)); y = h + FFN(RMSNorm(h)).
 
     x: [B, S, d]; caches [B_max, G, L_max, D] (B_max >= B; rows >= B untouched).
@@ -257,6 +306,8 @@ def block_forward(cfg: dict, w: dict, x: np.ndarray, start_pos: int, k_cache: np
     positions start_pos .. start_pos + S - 1 of sequences 0 .. B - 1 written.
     [L3B] Overview / How it works (the two residual branches, untied norms);
     [EVT] §06 Block; [ML2] Self-attention and transformer blocks.
+    route: for a mixture-of-experts block, optional (ids, weights) [B*S, k]
+    replacing the router's choice (see moe_ffn).
     """
     d, H, G, D = _dims(cfg)
     x = np.asarray(x, dtype=np.float64)
@@ -266,7 +317,7 @@ def block_forward(cfg: dict, w: dict, x: np.ndarray, start_pos: int, k_cache: np
                           k, v, start_pos)
     o = gqa_attention(q, kc, vc, start_pos).reshape(B, S, H * D)
     h = x + linear(o, w["wo"])
-    y = h + _ffn(cfg, w, h)
+    y = h + _ffn(cfg, w, h, route)
     kfull = np.array(k_cache, dtype=np.float64, copy=True)
     vfull = np.array(v_cache, dtype=np.float64, copy=True)
     kfull[:B] = kc

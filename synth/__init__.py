@@ -199,9 +199,12 @@ SHAPES = {
 WEIGHT_NAMES = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")
 
 
-def weight_shapes(d_model, n_heads, n_kv_heads, d_ff, **_):
+def weight_shapes(d_model, n_heads, n_kv_heads, d_ff, n_experts=0, d_ff_shared=0, **_):
+    """Parameter shapes of one block.  With n_experts > 0 the feed-forward is a
+    mixture of experts: w_gate / w_up / w_down stacked per expert, a router
+    [n_experts, d_model] and, when d_ff_shared > 0, a shared expert."""
     dh = d_model // n_heads
-    return {
+    out = {
         "attn_norm": (d_model,),
         "wq": (n_heads * dh, d_model),
         "wk": (n_kv_heads * dh, d_model),
@@ -212,6 +215,16 @@ def weight_shapes(d_model, n_heads, n_kv_heads, d_ff, **_):
         "w_up": (d_ff, d_model),
         "w_down": (d_model, d_ff),
     }
+    if n_experts:
+        out["w_gate"] = (n_experts, d_ff, d_model)
+        out["w_up"] = (n_experts, d_ff, d_model)
+        out["w_down"] = (n_experts, d_model, d_ff)
+        out["router"] = (n_experts, d_model)
+        if d_ff_shared:
+            out["shared_gate"] = (d_ff_shared, d_model)
+            out["shared_up"] = (d_ff_shared, d_model)
+            out["shared_down"] = (d_model, d_ff_shared)
+    return out
 
 
 def _store(a32: np.ndarray, dtype: str) -> np.ndarray:

@@ -483,6 +483,115 @@ def test_stack_zero_blocks_is_norm_then_head():
         np.testing.assert_allclose(logits[0, s], head @ n, atol=1e-12)
 
 
+# ------------------------------------------------- mixture of experts -------
+
+MOE = dict(TINY, n_experts=6, top_k=2, d_ff=32, d_ff_shared=48)
+
+
+def _moe_weights(cfg, tag):
+    return {n: _rng(tag + n, s, std=0.1, mean=1.0) if n.endswith("norm") else _rng(tag + n, s, std=0.2)
+            for n, s in synth.weight_shapes(**cfg).items()}
+
+
+def test_moe_single_expert_without_shared_is_the_dense_ffn():
+    cfg = dict(MOE, n_experts=1, top_k=1, d_ff_shared=0)
+    w = _moe_weights(cfg, "m1")
+    v = _rng("m1v", (7, 64))
+    np.testing.assert_allclose(oracle.moe_ffn(cfg, w, v),
+                               oracle.swiglu(v, w["w_gate"][0], w["w_up"][0], w["w_down"][0]), rtol=0, atol=1e-12)
+    # and inside a whole block: equal to the dense block with that expert's weights
+    dense = {k: (v_[0] if k in ("w_gate", "w_up", "w_down") else v_) for k, v_ in w.items() if k != "router"}
+    wd, x, kc, vc = _tiny_inputs(TINY, B=1, S=5, Lmax=8, tag="m1b")
+    wd.update(dense)
+    wm = dict(wd, router=w["router"], w_gate=w["w_gate"], w_up=w["w_up"], w_down=w["w_down"])
+    y_dense, _, _ = oracle.block_forward(dict(TINY, d_ff=32), wd, x, 0, kc, vc)
+    y_moe, _, _ = oracle.block_forward(cfg, wm, x, 0, kc, vc)
+    np.testing.assert_allclose(y_moe, y_dense, rtol=0, atol=1e-12)
+
+
+def test_moe_identical_experts_make_routing_irrelevant():
+    cfg = dict(MOE, d_ff_shared=0)
+    w = _moe_weights(cfg, "mi")
+    for n in ("w_gate", "w_up", "w_down"):
+        w[n] = np.repeat(w[n][:1], cfg["n_experts"], axis=0)
+    v = _rng("miv", (9, 64))
+    np.testing.assert_allclose(oracle.moe_ffn(cfg, w, v),
+                               oracle.swiglu(v, w["w_gate"][0], w["w_up"][0], w["w_down"][0]), rtol=0, atol=1e-12)
+
+
+def test_moe_matches_bruteforce_top_k_with_shared_expert():
+    cfg = MOE
+    w = _moe_weights(cfg, "mb")
+    v = _rng("mbv", (11, 64))
+    out = oracle.moe_ffn(cfg, w, v)
+    E, k = cfg["n_experts"], cfg["top_k"]
+    for t in range(v.shape[0]):
+        logits = [float(np.dot(w["router"][e], v[t])) for e in range(E)]
+        chosen = []
+        for _ in range(k):  # repeated arg-max, lowest id first among equals
+            best = None
+            for e in range(E):
+                if e not in chosen and (best is None or logits[e] > logits[best]):
+                    best = e
+            chosen.append(best)
+        ex = [math.exp(logits[e] - logits[chosen[0]]) for e in chosen]
+        ref = np.zeros(64)
+        for e, a in zip(chosen, ex):
+            h = np.array([float(np.dot(w["w_gate"][e][f], v[t])) for f in range(cfg["d_ff"])])
+            u = np.array([float(np.dot(w["w_up"][e][f], v[t])) for f in range(cfg["d_ff"])])
+            ref += a / sum(ex) * (w["w_down"][e] @ (h / (1 + np.exp(-h)) * u))
+        hs = w["shared_gate"] @ v[t]
+        ref += w["shared_down"] @ (hs / (1 + np.exp(-hs)) * (w["shared_up"] @ v[t]))
+        np.testing.assert_allclose(out[t], ref, rtol=0, atol=1e-11)
+
+
+def test_moe_is_invariant_to_renumbering_the_experts():
+    cfg = MOE
+    w = _moe_weights(cfg, "mp")
+    v = _rng("mpv", (13, 64))
+    perm = np.array([3, 0, 5, 1, 4, 2])
+    wp = dict(w)
+    for n in ("w_gate", "w_up", "w_down", "router"):
+        wp[n] = w[n][perm]
+    np.testing.assert_allclose(oracle.moe_ffn(cfg, wp, v), oracle.moe_ffn(cfg, w, v), rtol=0, atol=1e-12)
+
+
+def test_moe_with_every_expert_chosen_is_the_full_softmax_mixture():
+    cfg = dict(MOE, top_k=6, d_ff_shared=0)
+    w = _moe_weights(cfg, "ma")
+    v = _rng("mav", (5, 64))
+    logits = v @ w["router"].T
+    p = np.exp(logits - logits.max(-1, keepdims=True))
+    p /= p.sum(-1, keepdims=True)
+    ref = sum(p[:, e:e + 1] * oracle.swiglu(v, w["w_gate"][e], w["w_up"][e], w["w_down"][e]) for e in range(6))
+    np.testing.assert_allclose(oracle.moe_ffn(cfg, w, v), ref, rtol=0, atol=1e-12)
+
+
+def test_moe_router_ties_pick_the_lowest_id_and_weights_sum_to_one():
+    cfg = dict(MOE, top_k=1)
+    w = _moe_weights(cfg, "mt")
+    w["router"][5] = w["router"][2]  # experts 2 and 5 always tie
+    w["router"][[0, 1, 3, 4]] *= 0.0
+    v = np.abs(_rng("mtv", (4, 64)))
+    v = v * np.sign(w["router"][2])[None, :]  # positive logits for 2 and 5, zero for the rest
+    ids, wts, _ = oracle.moe_route(cfg, w, v)
+    assert ids.ravel().tolist() == [2, 2, 2, 2]
+    np.testing.assert_allclose(wts, 1.0)
+    ids2, wts2, _ = oracle.moe_route(MOE, dict(w), v)
+    assert ids2.tolist() == [[2, 5]] * 4
+    np.testing.assert_allclose(wts2.sum(-1), 1.0, rtol=1e-15)
+
+
+def test_moe_shared_expert_alone_when_routed_outputs_vanish():
+    cfg = MOE
+    w = _moe_weights(cfg, "ms")
+    w["w_down"] = np.zeros_like(w["w_down"])
+    v = _rng("msv", (6, 64))
+    np.testing.assert_allclose(oracle.moe_ffn(cfg, w, v),
+                               oracle.swiglu(v, w["shared_gate"], w["shared_up"], w["shared_down"]),
+                               rtol=0, atol=1e-12)
+
+
 # ------------------------------------------------- greedy generation --------
 
 def _identity_stack(cfg, n_layers, tag):
