@@ -364,6 +364,7 @@ def main():
                                          rope_theta=1e5, B=8, S=1024), args)
         secondary["llama3_8b_block_prefill_b4s2048"] = bench_block_shape(
             lb, torch, dev, stream, dict(SHAPE, B=4, S=2048), args, weights=w)
+        secondary["llama4_scout_shaped_moe_block"] = bench_moe(lb, torch, dev, stream, args)
     stack = None
     if not args.no_stack:
         del w
@@ -473,6 +474,59 @@ def bench_block_shape(lb, torch, dev, stream, s, args, weights=None):
             "ms_per_step_cuda_graph": ms_graph, "tokens_per_s": B * S / (ms / 1e3),
             "tflops": (lin + att) / (ms / 1e3) / 1e12, "steps": steps, "kernels_per_step": per_forward,
             "gpu_launches": per_forward * steps}
+
+
+def bench_moe(lb, torch, dev, stream, args, B=1, S=8192):
+    """A Llama-4-Scout-shaped mixture-of-experts block prefill: d 5120, 40 query / 8 KV heads of width 128,
+    16 experts of width 8192, top-1 routing, one shared expert of width 8192 (device-generated weights)."""
+    d, H, G, D, E, k, F, Fs = 5120, 40, 8, 128, 16, 1, 8192, 8192
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+
+    def rn(*shape, std=0.02, mean=0.0):
+        return (torch.randn(shape, generator=g, device=dev, dtype=torch.float32) * std + mean).to(torch.bfloat16)
+
+    w = {"attn_norm": rn(d, std=0.1, mean=1.0), "wq": rn(H * D, d), "wk": rn(G * D, d), "wv": rn(G * D, d),
+         "wo": rn(d, H * D), "ffn_norm": rn(d, std=0.1, mean=1.0), "w_gate": rn(E, F, d), "w_up": rn(E, F, d),
+         "w_down": rn(E, d, F), "router": rn(E, d), "shared_gate": rn(Fs, d), "shared_up": rn(Fs, d),
+         "shared_down": rn(d, Fs)}
+    cfg = lb.make_config(d, H, G, F, S, 1e-5, 5e5, lb.LLAMA_BF16, n_experts=E, top_k=k, d_ff_shared=Fs)
+    st, blk = lb.llama_block_create(cfg, lb.make_weights(w), B * S)
+    lb.check(st, "llama_block_create (moe)")
+    del w
+    torch.cuda.empty_cache()
+    x = torch.randn((B, S, d), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    y = torch.empty_like(x)
+    kc = torch.zeros((B, G, S, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    kv = lb.make_kv_cache(kc, vc, B, S)
+    for _ in range(args.warmup):
+        lb.check(lb.llama_block_forward(blk, x, y, B, S, 0, kv, stream))
+    steps = max(10, min(args.steps, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    n0 = lb.llama_kernel_launch_count()
+    e0.record(stream)
+    for _ in range(steps):
+        lb.check(lb.llama_block_forward(blk, x, y, B, S, 0, kv, stream))
+    e1.record(stream)
+    per_forward = (lb.llama_kernel_launch_count() - n0) // steps
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    ids = torch.empty((B * S, k), dtype=torch.int32, device=dev)
+    wts = torch.empty((B * S, k), dtype=torch.float32, device=dev)
+    lb.check(lb.llama_block_moe_routing(blk, ids, wts, stream))
+    torch.cuda.synchronize()
+    load = torch.bincount(ids.flatten().long(), minlength=E).cpu().tolist()
+    status = lb.llama_block_device_status(blk)
+    lb.llama_block_destroy(blk)
+    T = B * S
+    lin = 2.0 * T * (d * (H + 2 * G) * D + H * D * d + d * 64 + k * 3 * d * F + 3 * d * Fs)
+    att = 4.0 * D * H * (S * (S + 1) / 2) * B
+    return {"workload": "llama4_scout_shaped_moe_block_prefill_b1s8192_e16_top1_shared",
+            "ms_per_step": ms, "tokens_per_s": T / (ms / 1e3), "tflops": (lin + att) / (ms / 1e3) / 1e12,
+            "rows_per_expert": load, "steps": steps, "kernels_per_step": per_forward,
+            "gpu_launches": per_forward * steps, "device_status": status}
 
 
 def bench_stack(lb, torch, dev, stream, args, n_layers=32, vocab=128256, S=8192):

@@ -47,14 +47,16 @@ class llama_config(ctypes.Structure):
     _fields_ = [("d_model", c_int32), ("n_heads", c_int32), ("n_kv_heads", c_int32), ("d_ff", c_int32),
                 ("max_seq_len", c_int32), ("norm_eps", c_float), ("rope_theta", c_float), ("dtype", c_int32),
                 ("rope_layout", c_int32), ("rope_scaling_factor", c_float), ("rope_low_freq_factor", c_float),
-                ("rope_high_freq_factor", c_float), ("rope_original_max_pos", c_int32)]
+                ("rope_high_freq_factor", c_float), ("rope_original_max_pos", c_int32),
+                ("n_experts", c_int32), ("top_k", c_int32), ("d_ff_shared", c_int32)]
 
 
 WEIGHT_FIELDS = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")
+MOE_WEIGHT_FIELDS = ("router", "shared_gate", "shared_up", "shared_down")
 
 
 class llama_block_weights(ctypes.Structure):
-    _fields_ = [(n, c_void_p) for n in WEIGHT_FIELDS]
+    _fields_ = [(n, c_void_p) for n in WEIGHT_FIELDS + MOE_WEIGHT_FIELDS]
 
 
 class llama_kv_cache(ctypes.Structure):
@@ -97,6 +99,7 @@ def load() -> ctypes.CDLL:
         "llama_ffn_hidden_dim": (c_int32, [c_int32, c_int32, c_float]),
         "llama_status_string": (c_char_p, [c_int32]),
         "llama_last_cuda_error": (c_char_p, []),
+        "llama_block_moe_routing": (st, [c_void_p, c_void_p, c_void_p, c_void_p]),
         "llama_kernel_launch_count": (ctypes.c_ulonglong, []),
         "llama_op_rmsnorm": (st, [c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_void_p]),
         "llama_op_linear": (st, [c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
@@ -139,16 +142,19 @@ def _stream(s):
 # ---------------------------------------------------------------- structs ---
 
 def make_config(d_model, n_heads, n_kv_heads, d_ff, max_seq_len, norm_eps, rope_theta, dtype,
-                rope_layout=0, rope_scaling=None) -> llama_config:
-    """rope_scaling: None or a dict with factor, low_freq_factor, high_freq_factor, original_max_pos."""
+                rope_layout=0, rope_scaling=None, n_experts=0, top_k=0, d_ff_shared=0) -> llama_config:
+    """rope_scaling: None or a dict with factor, low_freq_factor, high_freq_factor, original_max_pos.
+    n_experts > 0 makes the feed-forward a mixture of experts (d_ff is then each expert's width)."""
     sc = rope_scaling or {}
     return llama_config(d_model, n_heads, n_kv_heads, d_ff, max_seq_len, norm_eps, rope_theta, dtype, rope_layout,
                         float(sc.get("factor", 0.0)), float(sc.get("low_freq_factor", 0.0)),
-                        float(sc.get("high_freq_factor", 0.0)), int(sc.get("original_max_pos", 0)))
+                        float(sc.get("high_freq_factor", 0.0)), int(sc.get("original_max_pos", 0)),
+                        n_experts, top_k, d_ff_shared)
 
 
 def make_weights(w: dict) -> llama_block_weights:
-    return llama_block_weights(*[_p(w[n]) for n in WEIGHT_FIELDS])
+    """Pointers of a weight dict (mixture-of-experts entries are optional)."""
+    return llama_block_weights(*[_p(w[n]) for n in WEIGHT_FIELDS], *[_p(w.get(n)) for n in MOE_WEIGHT_FIELDS])
 
 
 def make_kv_cache(k, v, max_batch, max_seq_len) -> llama_kv_cache:
@@ -244,6 +250,10 @@ def llama_status_string(status) -> str:
 
 def llama_last_cuda_error() -> str:
     return load().llama_last_cuda_error().decode()
+
+
+def llama_block_moe_routing(blk, ids, weights, stream=None) -> int:
+    return load().llama_block_moe_routing(blk, _p(ids), _p(weights), _stream(stream))
 
 
 def llama_kernel_launch_count() -> int:

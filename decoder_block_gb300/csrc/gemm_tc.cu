@@ -69,6 +69,11 @@ struct GemmArgs {
   float inv_d, eps;    // RMSNorm: scale = rsqrt(ss * inv_d + eps)
   QkvScatter qkv;      // EPI_QKV_ROPE destinations
   int prefetch_w;      // W is written by no kernel: load it before the grid dependency wait
+  // grouped mode (one GEMM per group, e.g. per expert): rows [group_off[g],
+  // group_off[g+1]) of A multiply rows [g * N, (g+1) * N) of W; offsets live on
+  // the device (written by an earlier kernel), so the tile count is found there
+  const int *group_off;
+  int n_groups;
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int &mt, int &nt) {
@@ -207,7 +212,8 @@ __device__ __forceinline__ void qkv_rope_chunk32(const float (&v)[32], const Gem
 
 template <int EPI>
 __device__ __forceinline__ float epilogue_chunk32(float (&v)[32], const GemmArgs &a, int m, int n) {
-  if constexpr (EPI == EPI_STORE_ROWSCALE || EPI == EPI_SWIGLU_ROWSCALE || EPI == EPI_QKV_ROPE) {
+  if constexpr (EPI == EPI_STORE_ROWSCALE || EPI == EPI_SWIGLU_ROWSCALE || EPI == EPI_QKV_ROPE ||
+                EPI == EPI_F32OUT_ROWSCALE) {
     // RMSNorm of A's row m, applied to the GEMM result (the gain is folded into W)
     const float r = m < a.M ? rsqrtf(a.ss_in[m] * a.inv_d + a.eps) : 0.f;
 #pragma unroll
@@ -229,6 +235,10 @@ __device__ __forceinline__ float epilogue_chunk32(float (&v)[32], const GemmArgs
   } else if constexpr (EPI == EPI_QKV_ROPE) {
     qkv_rope_chunk32(v, a, m, n);
     return 0.f;
+  } else if constexpr (EPI == EPI_F32OUT_ROWSCALE) {
+    epilogue_chunk16<EPI_F32OUT>(v, a, m, n);
+    epilogue_chunk16<EPI_F32OUT>(v + 16, a, m, n + 16);
+    return 0.f;
   } else if constexpr (EPI == EPI_STORE_ROWSCALE) {
     epilogue_chunk16<EPI_STORE>(v, a, m, n);
     epilogue_chunk16<EPI_STORE>(v + 16, a, m, n + 16);
@@ -242,7 +252,33 @@ __device__ __forceinline__ float epilogue_chunk32(float (&v)[32], const GemmArgs
   }
 }
 
-template <int EPI, int BN>
+// Tiles of the grouped mode: group g has ceil(rows_g / BM) x n_tiles tiles,
+// enumerated group by group, N-tile-major within a group (the m-tiles of one
+// weight tile run back to back).
+struct GroupedTiles {
+  const int *off;
+  int n_groups, n_tiles;
+  __device__ int count() const {
+    int t = 0;
+    for (int g = 0; g < n_groups; ++g) t += (off[g + 1] - off[g] + BM - 1) / BM * n_tiles;
+    return t;
+  }
+  __device__ void coords(int u, int &g, int &mt, int &nt) const {
+    for (g = 0; g < n_groups; ++g) {
+      const int mtg = (off[g + 1] - off[g] + BM - 1) / BM;
+      if (u < mtg * n_tiles) {
+        nt = u / mtg;
+        mt = u % mtg;
+        return;
+      }
+      u -= mtg * n_tiles;
+    }
+    g = n_groups - 1;
+    mt = nt = 0;
+  }
+};
+
+template <int EPI, int BN, bool GROUPED = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs args) {
   using G = GemmCfg<BN>;
@@ -263,15 +299,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tiles = (args.M + BM - 1) / BM, n_tiles = (args.N + BN - 1) / BN;
-  const int num_tiles = m_tiles * n_tiles;
-  const int num_units = num_tiles * args.splits;
   const int k_steps = (args.K + BK - 1) / BK;
-  // unit -> (tile, K range in BK steps)
-  auto unit_coords = [&](int u, int &mt, int &nt, int &k0, int &k1) {
-    const int tile = u / args.splits, sp = u % args.splits;
-    tile_coords(tile, m_tiles, n_tiles, mt, nt);
-    k0 = sp * args.ksteps_split;
-    k1 = min(k_steps, k0 + args.ksteps_split);
+  const GroupedTiles gt{args.group_off, args.n_groups, n_tiles};
+  if constexpr (GROUPED) grid_dependency_wait();  // every role reads the group offsets
+  const int num_units = GROUPED ? gt.count() : m_tiles * n_tiles * args.splits;
+  // unit -> first A row, first W row, end of the valid A rows, N tile, K range in BK steps
+  auto unit_coords = [&](int u, int &a_row, int &w_row, int &m_end, int &nt, int &k0, int &k1) {
+    if constexpr (GROUPED) {
+      int g, mt;
+      gt.coords(u, g, mt, nt);
+      a_row = args.group_off[g] + mt * BM;
+      m_end = min(args.group_off[g + 1], args.M);  // never past A, whatever the offsets say
+      w_row = g * args.N + nt * BN;
+      k0 = 0;
+      k1 = k_steps;
+    } else {
+      const int tile = u / args.splits, sp = u % args.splits;
+      int mt;
+      tile_coords(tile, m_tiles, n_tiles, mt, nt);
+      a_row = mt * BM;
+      m_end = args.M;
+      w_row = nt * BN;
+      k0 = sp * args.ksteps_split;
+      k1 = min(k_steps, k0 + args.ksteps_split);
+    }
   };
 
   if (threadIdx.x == 0) {
@@ -306,28 +357,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // The weights of the first unit's first stages depend on no earlier
       // kernel: request them before waiting for the activations.
       int pre = 0;
-      if (args.prefetch_w && (int)blockIdx.x < num_units) {
-        int mt, nt, k0, k1;
-        unit_coords(blockIdx.x, mt, nt, k0, k1);
+      if (!GROUPED && args.prefetch_w && (int)blockIdx.x < num_units) {
+        int a_row, w_row, m_end, nt, k0, k1;
+        unit_coords(blockIdx.x, a_row, w_row, m_end, nt, k0, k1);
         pre = min(STAGES, k1 - k0);
         for (int i = 0; i < pre; ++i) {
           const uint32_t sb = smem0 + i * G::STAGE_BYTES + G::A_BYTES;
           ptx::mbar_arrive_expect_tx(full_bar(i), G::STAGE_BYTES);
-          ptx::tma_load_2d(sb, &tmB, (k0 + i) * BK, nt * BN, full_bar(i));
+          ptx::tma_load_2d(sb, &tmB, (k0 + i) * BK, w_row, full_bar(i));
         }
       }
-      grid_dependency_wait();
+      if constexpr (!GROUPED) grid_dependency_wait();
       int it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        int mt, nt, k0, k1;
-        unit_coords(u, mt, nt, k0, k1);
+        int a_row, w_row, m_end, nt, k0, k1;
+        unit_coords(u, a_row, w_row, m_end, nt, k0, k1);
         for (int k = k0; k < k1; ++k) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           const uint32_t sa = smem0 + s * G::STAGE_BYTES, sb = sa + G::A_BYTES;
           if (it < pre) {  // stage s is fresh and its weights are already on the way
-            ptx::tma_load_2d(sa, &tmA, k * BK, mt * BM, full_bar(s));
+            ptx::tma_load_2d(sa, &tmA, k * BK, a_row, full_bar(s));
             ++it;
             continue;
           }
@@ -336,8 +387,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           ptx::mbar_arrive_expect_tx(full_bar(s), G::STAGE_BYTES);
-          ptx::tma_load_2d(sa, &tmA, k * BK, mt * BM, full_bar(s));
-          ptx::tma_load_2d(sb, &tmB, k * BK, nt * BN, full_bar(s));
+          ptx::tma_load_2d(sa, &tmA, k * BK, a_row, full_bar(s));
+          ptx::tma_load_2d(sb, &tmB, k * BK, w_row, full_bar(s));
           ++it;
         }
       }
@@ -353,8 +404,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int it = 0, tcount = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++tcount) {
-        int mt, nt, k0, k1;
-        unit_coords(u, mt, nt, k0, k1);
+        int a_row, w_row, m_end, nt, k0, k1;
+        unit_coords(u, a_row, w_row, m_end, nt, k0, k1);
         const int acc = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
         if (!ptx::mbar_wait(tempty_bar(acc), aph ^ 1, abort_flag, args.status, DEV_TIMEOUT_MMA)) break;
@@ -385,20 +436,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_wait(fin_bar, 0, &dummy, args.status, DEV_TIMEOUT_MMA);
     }
   } else {
-    grid_dependency_wait();  // the epilogue reads R / row statistics and writes C
+    if constexpr (!GROUPED) grid_dependency_wait();  // the epilogue reads R / row statistics and writes C
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     int tcount = 0;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++tcount) {
-      int mt, nt, k0, k1;
-      unit_coords(u, mt, nt, k0, k1);
+      int a_row, w_row, m_end, nt, k0, k1;
+      unit_coords(u, a_row, w_row, m_end, nt, k0, k1);
       const int acc = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
       bool ok = ptx::mbar_wait(tfull_bar(acc), aph, abort_flag, args.status, DEV_TIMEOUT_EPILOGUE);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
       const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      const int m = mt * BM + row;
+      // rows past the tile's valid range (the next group's rows, or past M) are
+      // passed as row M, which every epilogue skips
+      const int m = a_row + row < m_end ? a_row + row : args.M;
       if (args.splits == 1) {
         float sq = 0.f;
 #pragma unroll 1
@@ -416,7 +469,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // split-K: add this warp's 32 x BN fp32 partial into the tile's accumulator,
         // release TMEM, count arrivals; the last split's warp finishes the tile
         const int tile = u / args.splits;
-        const bool rows_live = mt * BM + q * 32 < args.M;
+        const bool rows_live = a_row + q * 32 < args.M;
         float *acc_row = args.part + ((size_t)tile * BM + row) * BN;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
@@ -521,25 +574,29 @@ int sm_count() {
   return n > 0 ? n : 1;
 }
 
-template <int EPI, int BN>
+template <int EPI, int BN, bool GROUPED = false>
 cudaError_t launch_cfg(const bf16 *A, const bf16 *W, GemmArgs args, cudaStream_t st) {
   using G = GemmCfg<BN>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<EPI, BN, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     G::SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap ma, mb;
+  const uint64_t w_rows = GROUPED ? (uint64_t)args.N * args.n_groups : (uint64_t)args.N;
   if (!make_map_2d(&ma, A, (uint64_t)args.M, (uint64_t)args.K, BM) ||
-      !make_map_2d(&mb, W, (uint64_t)args.N, (uint64_t)args.K, BN))
+      !make_map_2d(&mb, W, w_rows, (uint64_t)args.K, BN))
     return cudaErrorInvalidValue;
-  const int tiles = ((args.M + BM - 1) / BM) * ((args.N + BN - 1) / BN);
-  const int units = tiles * args.splits;
-  const int grid = units < sm_count() ? units : sm_count();
+  int grid = sm_count();
+  if (!GROUPED) {  // grouped: the tile count is on the device; every SM takes part
+    const int units = ((args.M + BM - 1) / BM) * ((args.N + BN - 1) / BN) * args.splits;
+    grid = units < grid ? units : grid;
+  }
   count_launch();
-  return launch_pdl(gemm_tc_kernel<EPI, BN>, dim3(grid), dim3(NUM_THREADS), G::SMEM_BYTES, st, ma, mb, args);
+  return launch_pdl(gemm_tc_kernel<EPI, BN, GROUPED>, dim3(grid), dim3(NUM_THREADS), G::SMEM_BYTES, st, ma, mb,
+                    args);
 }
 
 template <int EPI>
@@ -576,6 +633,39 @@ __global__ void interleave_rows_kernel(const uint4 *__restrict__ gate, const uin
 }
 
 }  // namespace
+
+cudaError_t launch_gemm_grouped(const bf16 *A, const bf16 *W, void *C, int M, int N, int K, int n_groups,
+                                const int *group_off, int epi, int *status, cudaStream_t st) {
+  if (M <= 0 || N <= 0 || n_groups <= 0) return cudaSuccess;
+  if (K <= 0 || (K & 7) != 0 || group_off == nullptr) return cudaErrorInvalidValue;
+  if (epi != EPI_STORE && epi != EPI_SWIGLU) return cudaErrorInvalidValue;
+  if (epi == EPI_SWIGLU && (N & 31) != 0) return cudaErrorInvalidValue;
+  // a tile never straddles two groups' weights: BN divides N; the widest tile
+  // that still gives every SM a tile (counting one tile per 128 rows)
+  const int m_tiles = (M + BM - 1) / BM;
+  int bn = 0;
+  if (N % 256 == 0 && m_tiles * (N / 256) >= sm_count())
+    bn = 256;
+  else if (N % 128 == 0)
+    bn = 128;
+  else if (N % 64 == 0)
+    bn = 64;
+  if (bn == 0) return cudaErrorInvalidValue;
+  GemmArgs args{nullptr, C, M, N, K, status, 1, (K + BK - 1) / BK, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f, {},
+                0, group_off, n_groups};
+  if (epi == EPI_STORE) {
+    switch (bn) {
+      case 256: return launch_cfg<EPI_STORE, 256, true>(A, W, args, st);
+      case 128: return launch_cfg<EPI_STORE, 128, true>(A, W, args, st);
+      default: return launch_cfg<EPI_STORE, 64, true>(A, W, args, st);
+    }
+  }
+  switch (bn) {
+    case 256: return launch_cfg<EPI_SWIGLU, 256, true>(A, W, args, st);
+    case 128: return launch_cfg<EPI_SWIGLU, 128, true>(A, W, args, st);
+    default: return launch_cfg<EPI_SWIGLU, 64, true>(A, W, args, st);
+  }
+}
 
 GemmPlan plan_gemm(int M, int N, int K, size_t ws_part_bytes, int ws_counter_slots) {
   const int sms = sm_count();
@@ -648,7 +738,7 @@ cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C,
   if (K <= 0 || (K & 7) != 0) return cudaErrorInvalidValue;
   if ((epi == EPI_SWIGLU || epi == EPI_SWIGLU_ROWSCALE) && (N & 31) != 0) return cudaErrorInvalidValue;
   const bool needs_norm = epi == EPI_STORE_ROWSCALE || epi == EPI_SWIGLU_ROWSCALE || epi == EPI_RESIDUAL_SQSUM ||
-                          epi == EPI_QKV_ROPE;
+                          epi == EPI_QKV_ROPE || epi == EPI_F32OUT_ROWSCALE;
   if (needs_norm && norm == nullptr) return cudaErrorInvalidValue;
   if (epi == EPI_QKV_ROPE) {
     if (scatter == nullptr || scatter->D <= 0 || (scatter->D & 31) != 0 || scatter->S <= 0 ||
@@ -657,7 +747,7 @@ cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C,
   }
   const GemmPlan plan = plan_gemm(M, N, K, ws != nullptr ? ws->part_bytes : 0, ws != nullptr ? ws->counter_slots : 0);
   GemmArgs args{R, C, M, N, K, status, 1, (K + BK - 1) / BK, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f, {},
-                weights_static ? 1 : 0};
+                weights_static ? 1 : 0, nullptr, 0};
   if (scatter != nullptr) args.qkv = *scatter;
   if (norm != nullptr) {
     args.ss_in = norm->ss_in;
@@ -680,6 +770,7 @@ cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C,
     case EPI_SWIGLU_ROWSCALE: return launch_epi<EPI_SWIGLU_ROWSCALE>(A, W, args, plan.bn, st);
     case EPI_RESIDUAL_SQSUM: return launch_epi<EPI_RESIDUAL_SQSUM>(A, W, args, plan.bn, st);
     case EPI_QKV_ROPE: return launch_epi<EPI_QKV_ROPE>(A, W, args, plan.bn, st);
+    case EPI_F32OUT_ROWSCALE: return launch_epi<EPI_F32OUT_ROWSCALE>(A, W, args, plan.bn, st);
   }
   return cudaErrorInvalidValue;
 }

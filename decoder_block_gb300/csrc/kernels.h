@@ -22,6 +22,7 @@ enum Epilogue : int {
   // QKV projection with the attention RMSNorm row scale, RoPE on the q and k
   // columns and the scatter of rotated q into q_out and of k / v into the cache
   EPI_QKV_ROPE = 7,
+  EPI_F32OUT_ROWSCALE = 8,  // C fp32 = r_m (A W^T)  (mixture-of-experts router logits)
 };
 
 // ss[t] = sum_j x[t][j]^2 (fp32) for rows of width d; zero_out[t] = 0 when not null.
@@ -66,6 +67,22 @@ cudaError_t launch_attention_simt(const T *q, const T *kc, const T *vc, T *o, in
 template <typename T>
 cudaError_t launch_embed(const int32_t *tokens, const T *E, T *x, int ntok, int d, int vocab, int *status,
                          cudaStream_t st);
+
+// Mixture-of-experts routing and data movement (moe.cu).  E <= 256, k <= min(E, 32).
+bool moe_supported(int E, int k);
+// ids / wts [T][k]: the k largest logits of row t (logits [T][ld], fp32) and a
+// softmax over them; counts[e] += number of choices of e (counts zero before).
+cudaError_t launch_moe_topk(const float *logits, int ld, int T, int E, int k, int *ids, float *wts, int *counts,
+                            cudaStream_t st);
+// offsets [E + 1] = exclusive prefix sums of counts; counts and fill left zero.
+cudaError_t launch_moe_offsets(int *counts, int *offsets, int *fill, int E, cudaStream_t st);
+// For each (t, j): pos[t][j] = a free row of expert ids[t][j]'s range, and that
+// row of xin = bf16(h[t] * rsqrt(ss[t] / d + eps) * g).
+cudaError_t launch_moe_dispatch(const bf16 *h, const float *ss, const bf16 *g, float eps, int T, int d, int k,
+                                const int *ids, const int *offsets, int *fill, int *pos, bf16 *xin, cudaStream_t st);
+// y[t] = base[t] + sum_j wts[t][j] * ye[pos[t][j]] (rows of width d).
+cudaError_t launch_moe_combine(const bf16 *base, const bf16 *ye, const int *pos, const float *wts, int T, int d,
+                               int k, bf16 *y, cudaStream_t st);
 
 // Greedy pick: out[r * out_stride] (and next[r], when not null) = arg-max of
 // logits row r [rows][vocab] fp32, lowest id among equal maxima.

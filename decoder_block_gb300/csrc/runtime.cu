@@ -49,8 +49,10 @@ struct Dims {
   double theta;
   RopeScaling rope_scaling;
   int rope_halves;          // pairs (i, i + D/2) instead of (2i, 2i+1)
+  int E = 0, topk = 0, Fs = 0, E_pad = 0;  // mixture of experts (E = 0: dense); router rows padded to 64
   int dtype;
   size_t esize;
+  bool moe() const { return E > 0; }
   // halves RoPE on the fused QKV epilogue: the q / k rows of Wqkv are stored
   // reordered so that each pair lands in adjacent accumulator columns
   bool fused_qkv_rope() const { return dtype == LLAMA_BF16 && D % 32 == 0; }
@@ -84,7 +86,11 @@ struct Weights {
   void *wo = nullptr;    // [d, H D]
   void *w_gate = nullptr, *w_up = nullptr;  // [F, d] each
   void *w_gu = nullptr;  // bf16 tensor-core path: gate/up rows interleaved per 16-row group, [2F, d]
-  void *w_down = nullptr;  // [d, F]
+  void *w_down = nullptr;  // [d, F]  (mixture of experts: [E d, F], one [d, F] slice per expert)
+  // mixture of experts: w_gu holds every expert's interleaved gate/up rows [E 2F, d];
+  // router [E_pad, d] with the ffn-norm gain folded in (rows >= E zero);
+  // shared expert: gate/up interleaved with the gain folded in [2 Fs, d], down [d, Fs]
+  void *router = nullptr, *shared_gu = nullptr, *shared_down = nullptr;
 };
 
 struct Workspace {
@@ -94,6 +100,14 @@ struct Workspace {
   AttnScratch attn;                      // split-KV partials of the decode path
   GemmWorkspace gemm;                    // split-K partials of few-row GEMMs (decode)
   float *ss_x = nullptr, *ss_h = nullptr;  // per-row sums of squares (fused RMSNorm statistics)
+  // mixture of experts: router logits [T][E_pad] fp32; per (token, choice) expert id,
+  // weight and row in the expert-grouped buffers; per-expert counts / offsets / fill;
+  // expert inputs [T k][d], SwiGLU outputs [T k][F], outputs [T k][d]; shared expert
+  // activations [T][Fs] and h + shared [T][d]
+  float *logits = nullptr, *route_w = nullptr;
+  int *route_ids = nullptr, *route_pos = nullptr, *counts = nullptr, *offsets = nullptr, *fill = nullptr;
+  void *xin_e = nullptr, *act_e = nullptr, *y_e = nullptr, *act_s = nullptr, *hs = nullptr;
+  int last_tokens = 0;  // B * S of the most recent forward (routing introspection)
 };
 
 // Optional per-step event timing of block forwards (llama_block_profile_*).
@@ -156,6 +170,12 @@ llama_status validate_config(const llama_config *c, Dims *dm) {
   const int vec = c->dtype == LLAMA_BF16 ? 8 : 4;
   if (c->d_model % vec != 0 || c->d_ff % vec != 0) return LLAMA_ERR_UNSUPPORTED;
   if (c->rope_layout == LLAMA_ROPE_HALVES && (D / 2) % vec != 0) return LLAMA_ERR_UNSUPPORTED;
+  if (c->n_experts < 0 || c->top_k < 0 || c->d_ff_shared < 0) return LLAMA_ERR_INVALID_ARG;
+  if (c->n_experts > 0) {
+    if (c->top_k < 1 || !moe_supported(c->n_experts, c->top_k)) return LLAMA_ERR_INVALID_ARG;
+    if (c->dtype != LLAMA_BF16) return LLAMA_ERR_UNSUPPORTED;
+    if (c->d_model % 64 != 0 || c->d_ff % 32 != 0 || c->d_ff_shared % 32 != 0) return LLAMA_ERR_UNSUPPORTED;
+  }
   if (c->dtype == LLAMA_BF16 && c->d_ff % 16 != 0) return LLAMA_ERR_UNSUPPORTED;  // gate/up interleave groups
   dm->d = c->d_model;
   dm->H = c->n_heads;
@@ -174,6 +194,10 @@ llama_status validate_config(const llama_config *c, Dims *dm) {
     dm->rope_scaling.high = (double)c->rope_high_freq_factor;
     dm->rope_scaling.original_max_pos = (double)c->rope_original_max_pos;
   }
+  dm->E = c->n_experts;
+  dm->topk = c->n_experts > 0 ? c->top_k : 0;
+  dm->Fs = c->n_experts > 0 ? c->d_ff_shared : 0;
+  dm->E_pad = (dm->E + 63) / 64 * 64;
   dm->dtype = c->dtype;
   dm->esize = c->dtype == LLAMA_BF16 ? 2 : 4;
   return LLAMA_OK;
@@ -186,16 +210,30 @@ llama_status copy_weights(const Dims &dm, const llama_block_weights *w, Allocs &
     llama_status s = check_ptr(p);
     if (s != LLAMA_OK) return s;
   }
+  if (dm.moe()) {
+    llama_status s = check_ptr(w->router);
+    for (const void *p : {w->shared_gate, w->shared_up, w->shared_down})
+      if (s == LLAMA_OK && dm.Fs > 0) s = check_ptr(p);
+    if (s != LLAMA_OK) return s;
+  }
   const size_t e = dm.esize;
   const size_t dq = (size_t)dm.H * dm.D * dm.d * e, dkv = (size_t)dm.G * dm.D * dm.d * e;
   out->attn_norm = al.alloc(dm.d * e);
   out->ffn_norm = al.alloc(dm.d * e);
   out->wqkv = al.alloc(dq + 2 * dkv);
   out->wo = al.alloc((size_t)dm.d * dm.H * dm.D * e);
-  out->w_down = al.alloc((size_t)dm.d * dm.F * e);
+  const size_t n_ffn = dm.moe() ? (size_t)dm.E : 1;  // feed-forward weight sets
+  out->w_down = al.alloc(n_ffn * dm.d * dm.F * e);
   const bool tc = dm.dtype == LLAMA_BF16;
+  if (dm.moe()) {
+    out->router = al.alloc((size_t)dm.E_pad * dm.d * e);
+    if (dm.Fs > 0) {
+      out->shared_gu = al.alloc((size_t)2 * dm.Fs * dm.d * e);
+      out->shared_down = al.alloc((size_t)dm.d * dm.Fs * e);
+    }
+  }
   if (tc) {
-    out->w_gu = al.alloc((size_t)2 * dm.F * dm.d * e);
+    out->w_gu = al.alloc(n_ffn * 2 * dm.F * dm.d * e);
   } else {
     out->w_gate = al.alloc((size_t)dm.F * dm.d * e);
     out->w_up = al.alloc((size_t)dm.F * dm.d * e);
@@ -219,17 +257,34 @@ llama_status copy_weights(const Dims &dm, const llama_block_weights *w, Allocs &
   }
   cp(qkv + dq + dkv, w->wv, dkv);
   cp(out->wo, w->wo, (size_t)dm.d * dm.H * dm.D * e);
-  cp(out->w_down, w->w_down, (size_t)dm.d * dm.F * e);
+  cp(out->w_down, w->w_down, n_ffn * dm.d * dm.F * e);
   if (tc) {
+    // gate/up rows interleaved in groups of 16 (for experts: one call over all of
+    // them, F % 16 == 0 keeps every group inside one expert)
     if (err == cudaSuccess)
-      err = launch_interleave_rows((const bf16 *)w->w_gate, (const bf16 *)w->w_up, (bf16 *)out->w_gu, dm.F, dm.d,
-                                   nullptr);
+      err = launch_interleave_rows((const bf16 *)w->w_gate, (const bf16 *)w->w_up, (bf16 *)out->w_gu,
+                                   (int)(n_ffn * dm.F), dm.d, nullptr);
     // RMSNorm gains folded into the consuming projections: (x g) W^T = x (W diag g)^T,
     // so the GEMMs read the raw activations and scale rows by rsqrt(mean(x^2) + eps).
+    // Experts read rows the dispatch step has already normalised (gain included).
     if (err == cudaSuccess)
       err = launch_scale_columns((bf16 *)out->wqkv, (const bf16 *)w->attn_norm, dm.QKV, dm.d, nullptr);
-    if (err == cudaSuccess)
+    if (err == cudaSuccess && !dm.moe())
       err = launch_scale_columns((bf16 *)out->w_gu, (const bf16 *)w->ffn_norm, 2 * dm.F, dm.d, nullptr);
+    if (dm.moe()) {
+      if (err == cudaSuccess) err = cudaMemset(out->router, 0, (size_t)dm.E_pad * dm.d * e);
+      cp(out->router, w->router, (size_t)dm.E * dm.d * e);
+      if (err == cudaSuccess)
+        err = launch_scale_columns((bf16 *)out->router, (const bf16 *)w->ffn_norm, dm.E, dm.d, nullptr);
+      if (dm.Fs > 0) {
+        if (err == cudaSuccess)
+          err = launch_interleave_rows((const bf16 *)w->shared_gate, (const bf16 *)w->shared_up,
+                                       (bf16 *)out->shared_gu, dm.Fs, dm.d, nullptr);
+        if (err == cudaSuccess)
+          err = launch_scale_columns((bf16 *)out->shared_gu, (const bf16 *)w->ffn_norm, 2 * dm.Fs, dm.d, nullptr);
+        cp(out->shared_down, w->shared_down, (size_t)dm.d * dm.Fs * e);
+      }
+    }
     if (err == cudaSuccess) err = cudaDeviceSynchronize();
   } else {
     cp(out->w_gate, w->w_gate, (size_t)dm.F * dm.d * e);
@@ -260,7 +315,24 @@ llama_status alloc_workspace(const Dims &dm, int max_tokens, bool staging, Alloc
   ws->q = al.alloc(T * dm.H * dm.D * e);
   ws->o = al.alloc(T * dm.H * dm.D * e);
   ws->h = al.alloc(T * dm.d * e);
-  ws->act = al.alloc(T * dm.F * e);
+  if (!dm.moe()) ws->act = al.alloc(T * dm.F * e);
+  if (dm.moe()) {
+    const size_t Tk = T * dm.topk;
+    ws->logits = (float *)al.alloc(T * dm.E_pad * sizeof(float));
+    ws->route_w = (float *)al.alloc(Tk * sizeof(float));
+    ws->route_ids = (int *)al.alloc(Tk * sizeof(int));
+    ws->route_pos = (int *)al.alloc(Tk * sizeof(int));
+    ws->counts = (int *)al.alloc((size_t)dm.E * sizeof(int));
+    ws->offsets = (int *)al.alloc((size_t)(dm.E + 1) * sizeof(int));
+    ws->fill = (int *)al.alloc((size_t)dm.E * sizeof(int));
+    ws->xin_e = al.alloc(Tk * dm.d * e);
+    ws->act_e = al.alloc(Tk * dm.F * e);
+    ws->y_e = al.alloc(Tk * dm.d * e);
+    if (dm.Fs > 0) {
+      ws->act_s = al.alloc(T * dm.Fs * e);
+      ws->hs = al.alloc(T * dm.d * e);
+    }
+  }
   if (staging) {
     ws->xin = al.alloc(T * dm.d * e);
     ws->yout = al.alloc(T * dm.d * e);
@@ -278,6 +350,9 @@ llama_status alloc_workspace(const Dims &dm, int max_tokens, bool staging, Alloc
   }
   if (al.failed) return LLAMA_ERR_OOM;
   if (clear_gemm_scratch(ws->gemm) != cudaSuccess) return LLAMA_ERR_CUDA;
+  if (dm.moe() && (cudaMemset(ws->counts, 0, (size_t)dm.E * sizeof(int)) != cudaSuccess ||
+                   cudaMemset(ws->fill, 0, (size_t)dm.E * sizeof(int)) != cudaSuccess))
+    return LLAMA_ERR_CUDA;
   return LLAMA_OK;
 }
 
@@ -307,6 +382,44 @@ llama_status forward_simt(const Dims &dm, const Weights &w, const Workspace &ws,
   LAUNCH(launch_gemm_simt<T>(hn, (const T *)w.w_gate, (const T *)w.w_up, nullptr, act, M, dm.F, dm.d, EPI_SWIGLU,
                              st));
   LAUNCH(launch_gemm_simt<T>(act, (const T *)w.w_down, nullptr, h, y, M, dm.d, dm.F, EPI_RESIDUAL, st));
+  return LLAMA_OK;
+}
+
+// Mixture-of-experts feed-forward of a bf16 block ("Llama 4 From Scratch", MoE):
+// router logits (GEMM with the ffn-norm row scale), top-k routing, per-expert
+// row offsets, dispatch of the normalised rows, the experts' SwiGLU as two
+// grouped GEMMs over those row ranges, the shared expert as the dense fused
+// path (its down projection adds the residual), and the weighted combine.
+llama_status forward_moe(const Dims &dm, const Weights &w, const Workspace &ws, const bf16 *h, bf16 *y, int M,
+                         const RowNorm &norm_h, int *status, Profiler &pf, cudaStream_t st) {
+  const int k = dm.topk, Mk = M * dm.topk;
+  bf16 *xin = (bf16 *)ws.xin_e, *act = (bf16 *)ws.act_e, *ye = (bf16 *)ws.y_e;
+  pf.mark(5, 0, st);  // ffn_norm slot: routing and dispatch
+  LAUNCH(launch_gemm_tc(h, (const bf16 *)w.router, nullptr, ws.logits, M, dm.E_pad, dm.d, EPI_F32OUT_ROWSCALE,
+                        status, st, &ws.gemm, &norm_h, nullptr, true));
+  LAUNCH(launch_moe_topk(ws.logits, dm.E_pad, M, dm.E, k, ws.route_ids, ws.route_w, ws.counts, st));
+  LAUNCH(launch_moe_offsets(ws.counts, ws.offsets, ws.fill, dm.E, st));
+  LAUNCH(launch_moe_dispatch(h, ws.ss_h, (const bf16 *)w.ffn_norm, dm.eps, M, dm.d, k, ws.route_ids, ws.offsets,
+                             ws.fill, ws.route_pos, xin, st));
+  pf.mark(5, 1, st);
+  pf.mark(6, 0, st);  // gate/up slot: experts and shared expert
+  LAUNCH(launch_gemm_grouped(xin, (const bf16 *)w.w_gu, act, Mk, 2 * dm.F, dm.d, dm.E, ws.offsets, EPI_SWIGLU,
+                             status, st));
+  if (dm.Fs > 0)
+    LAUNCH(launch_gemm_tc(h, (const bf16 *)w.shared_gu, nullptr, ws.act_s, M, 2 * dm.Fs, dm.d, EPI_SWIGLU_ROWSCALE,
+                          status, st, &ws.gemm, &norm_h, nullptr, true));
+  pf.mark(6, 1, st);
+  pf.mark(7, 0, st);  // down slot: experts, shared expert (+ residual), combine
+  LAUNCH(launch_gemm_grouped(act, (const bf16 *)w.w_down, ye, Mk, dm.d, dm.F, dm.E, ws.offsets, EPI_STORE, status,
+                             st));
+  const bf16 *base = h;
+  if (dm.Fs > 0) {
+    LAUNCH(launch_gemm_tc((const bf16 *)ws.act_s, (const bf16 *)w.shared_down, h, ws.hs, M, dm.d, dm.Fs,
+                          EPI_RESIDUAL, status, st, &ws.gemm, nullptr, nullptr, true));
+    base = (const bf16 *)ws.hs;
+  }
+  LAUNCH(launch_moe_combine(base, ye, ws.route_pos, ws.route_w, M, dm.d, k, y, st));
+  pf.mark(7, 1, st);
   return LLAMA_OK;
 }
 
@@ -370,6 +483,7 @@ llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, c
   LAUNCH(launch_gemm_tc(o, (const bf16 *)w.wo, x, h, M, dm.d, dm.H * dm.D, EPI_RESIDUAL_SQSUM, status, st, &ws.gemm,
                         &norm_h, nullptr, true));
   pf.mark(4, 1, st);
+  if (dm.moe()) return forward_moe(dm, w, ws, h, y, M, norm_h, status, pf, st);
   pf.mark(5, 0, st);  // ffn_norm: fused into the O and gate/up GEMM epilogues
   pf.mark(5, 1, st);
   pf.mark(6, 0, st);
@@ -402,7 +516,8 @@ llama_status validate_call(const Dims &dm, int max_tokens, int B, int S, int sta
   return check_ptr(kv->v);
 }
 
-llama_status read_status(int *dev_status, int device, const GemmWorkspace *scratch) {
+llama_status read_status(int *dev_status, int device, const Workspace *ws, const Dims *dm) {
+  const GemmWorkspace *scratch = ws != nullptr ? &ws->gemm : nullptr;
   int prev = 0;
   if (cudaGetDevice(&prev) != cudaSuccess) return LLAMA_ERR_CUDA;
   if (prev != device && cudaSetDevice(device) != cudaSuccess) return LLAMA_ERR_CUDA;
@@ -410,7 +525,11 @@ llama_status read_status(int *dev_status, int device, const GemmWorkspace *scrat
   cudaError_t e = cudaDeviceSynchronize();
   if (e == cudaSuccess) e = cudaMemcpy(&v, dev_status, sizeof(int), cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemset(dev_status, 0, sizeof(int));
-  if (e == cudaSuccess && v != 0 && v != DEV_BAD_TOKEN && scratch != nullptr) e = clear_gemm_scratch(*scratch);
+  if (e == cudaSuccess && v != 0 && v != DEV_BAD_TOKEN && scratch != nullptr) {
+    e = clear_gemm_scratch(*scratch);
+    if (e == cudaSuccess && dm != nullptr && dm->moe()) e = cudaMemset(ws->counts, 0, (size_t)dm->E * sizeof(int));
+    if (e == cudaSuccess && dm != nullptr && dm->moe()) e = cudaMemset(ws->fill, 0, (size_t)dm->E * sizeof(int));
+  }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (prev != device) cudaSetDevice(prev);
   if (e != cudaSuccess) return LLAMA_ERR_CUDA;
@@ -486,8 +605,10 @@ llama_status llama_block_forward(llama_block *blk, const void *x, void *y, int32
   if (s == LLAMA_OK) s = check_ptr(y);
   if (s == LLAMA_OK) s = validate_call(blk->dm, blk->ws.max_tokens, B, S, start_pos, kv);
   if (s != LLAMA_OK) return s;
-  return forward_any(blk->dm, blk->w, blk->ws, blk->rope, x, y, B, S, start_pos, kv, blk->status,
-                     (cudaStream_t)stream, &blk->prof);
+  s = forward_any(blk->dm, blk->w, blk->ws, blk->rope, x, y, B, S, start_pos, kv, blk->status, (cudaStream_t)stream,
+                  &blk->prof);
+  if (s == LLAMA_OK) blk->ws.last_tokens = B * S;
+  return s;
 }
 
 llama_status llama_block_forward_host(llama_block *blk, const void *x_host, void *y_host, int32_t B, int32_t S,
@@ -501,6 +622,7 @@ llama_status llama_block_forward_host(llama_block *blk, const void *x_host, void
   s = forward_any(blk->dm, blk->w, blk->ws, blk->rope, blk->ws.xin, blk->ws.yout, B, S, start_pos, kv,
                   blk->status, st, &blk->prof);
   if (s != LLAMA_OK) return s;
+  blk->ws.last_tokens = B * S;
   if (cudaMemcpyAsync(y_host, blk->ws.yout, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return LLAMA_ERR_CUDA;
   return LLAMA_OK;
 }
@@ -564,6 +686,19 @@ llama_status llama_block_profile_read(llama_block *blk, int32_t *launches, float
   return LLAMA_OK;
 }
 
+llama_status llama_block_moe_routing(llama_block *blk, int32_t *ids, float *weights, llama_stream stream) {
+  if (blk == nullptr || !blk->dm.moe() || blk->ws.last_tokens <= 0) return LLAMA_ERR_INVALID_ARG;
+  llama_status s = check_ptr(ids);
+  if (s == LLAMA_OK) s = check_ptr(weights);
+  if (s != LLAMA_OK) return s;
+  const size_t n = (size_t)blk->ws.last_tokens * blk->dm.topk;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(ids, blk->ws.route_ids, n * sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(weights, blk->ws.route_w, n * sizeof(float), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return LLAMA_ERR_CUDA;
+  return LLAMA_OK;
+}
+
 const char *llama_profile_step_name(int32_t step) {
   static const char *names[LLAMA_PROFILE_STEPS] = {"attention_norm", "qkv_projection", "rope_kv_write",
                                                    "attention", "o_projection_residual", "ffn_norm",
@@ -573,7 +708,7 @@ const char *llama_profile_step_name(int32_t step) {
 
 llama_status llama_block_device_status(llama_block *blk) {
   if (blk == nullptr) return LLAMA_ERR_INVALID_ARG;
-  return read_status(blk->status, blk->device, &blk->ws.gemm);
+  return read_status(blk->status, blk->device, &blk->ws, &blk->dm);
 }
 
 llama_status llama_stack_create(const llama_config *cfg, int32_t n_layers, int32_t vocab, const void *embed,
@@ -752,7 +887,7 @@ void llama_stack_destroy(llama_stack *stk) {
 
 llama_status llama_stack_device_status(llama_stack *stk) {
   if (stk == nullptr) return LLAMA_ERR_INVALID_ARG;
-  return read_status(stk->status, stk->device, &stk->ws.gemm);
+  return read_status(stk->status, stk->device, &stk->ws, &stk->dm);
 }
 
 size_t llama_kv_cache_bytes(const llama_config *cfg, int32_t max_batch, int32_t max_seq_len) {

@@ -70,6 +70,14 @@ cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C,
                            const RowNorm *norm = nullptr, const QkvScatter *scatter = nullptr,
                            bool weights_static = false);
 
+// Grouped GEMM (one per expert): rows [group_off[g], group_off[g+1]) of A [M][K]
+// times rows [g*N, (g+1)*N) of W [n_groups*N][K]; C [M][N] (EPI_STORE) or
+// [M][N/2] (EPI_SWIGLU, W rows interleaved per group as for the dense
+// gate/up).  group_off (n_groups + 1 ints, device) may be written by the
+// preceding kernel on the stream; N must be a multiple of 64.
+cudaError_t launch_gemm_grouped(const bf16 *A, const bf16 *W, void *C, int M, int N, int K, int n_groups,
+                                const int *group_off, int epi, int *status, cudaStream_t st);
+
 // Reorder the rows of each of `heads` consecutive D-row heads of W [heads*D][d]:
 // out row 2i <- row i, out row 2i+1 <- row i + D/2 (the halves RoPE pairs become
 // adjacent output columns of x W^T).  d % 8 == 0.

@@ -90,14 +90,33 @@ typedef struct {
     float rope_low_freq_factor;
     float rope_high_freq_factor;
     int32_t rope_original_max_pos;
+    /* Mixture-of-experts feed-forward ("Llama 4 From Scratch", MoE; "From
+     * GPT-2 to Llama: four changes and the reason for each", The feed-forward
+     * grows a gate).  n_experts = 0: the dense SwiGLU of width d_ff.
+     * n_experts > 0 (bf16 only): v = RMSNorm(h); router logits l = v W_router^T;
+     * each token takes the top_k experts of largest logit (the lowest id among
+     * equal logits) with weights softmax(l over the chosen experts); the
+     * feed-forward output is sum_j w_j SwiGLU_{e_j}(v) (each expert of width
+     * d_ff), plus SwiGLU_shared(v) of width d_ff_shared when d_ff_shared > 0.
+     * Requires n_experts <= 256, 1 <= top_k <= min(n_experts, 32), d_model % 64
+     * == 0, d_ff % 32 == 0, d_ff_shared % 32 == 0. */
+    int32_t n_experts;
+    int32_t top_k;
+    int32_t d_ff_shared;
 } llama_config;
 
 /* Device pointers to one block's parameters, dtype = config.dtype.
  * attn_norm, ffn_norm: [d_model]; wq: [n_heads*d_head, d_model];
  * wk, wv: [n_kv_heads*d_head, d_model]; wo: [d_model, n_heads*d_head];
- * w_gate, w_up: [d_ff, d_model]; w_down: [d_model, d_ff].  No biases. */
+ * w_gate, w_up: [d_ff, d_model]; w_down: [d_model, d_ff].  No biases.
+ * Mixture-of-experts blocks (n_experts > 0): w_gate, w_up: [n_experts][d_ff]
+ * [d_model] and w_down: [n_experts][d_model][d_ff], one slice per expert;
+ * router: [n_experts, d_model]; shared_gate, shared_up: [d_ff_shared, d_model]
+ * and shared_down: [d_model, d_ff_shared] when d_ff_shared > 0.  The last four
+ * are ignored (may be NULL) for dense blocks. */
 typedef struct {
     const void *attn_norm, *wq, *wk, *wv, *wo, *ffn_norm, *w_gate, *w_up, *w_down;
+    const void *router, *shared_gate, *shared_up, *shared_down;
 } llama_block_weights;
 
 /* Caller-owned KV cache of one layer: k and v are each
@@ -138,6 +157,13 @@ llama_status llama_block_forward(llama_block *blk, const void *x, void *y, int32
 llama_status llama_block_forward_host(llama_block *blk, const void *x_host, void *y_host, int32_t B,
                                       int32_t S, int32_t start_pos, const llama_kv_cache *kv,
                                       llama_stream stream);
+
+/* Routing of the most recent llama_block_forward of a mixture-of-experts block
+ * (tracing, and for checking a forward against another implementation):
+ * copies, on stream, ids int32 [B*S][top_k] (expert ids, in the order the
+ * router chose them) and weights fp32 [B*S][top_k] into the caller's device
+ * buffers.  LLAMA_ERR_INVALID_ARG for a dense block or before any forward. */
+llama_status llama_block_moe_routing(llama_block *blk, int32_t *ids, float *weights, llama_stream stream);
 
 void llama_block_destroy(llama_block *blk);
 

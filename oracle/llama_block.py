@@ -44,7 +44,7 @@ import numpy as np
 __all__ = [
     "rms_norm", "rope_frequencies", "scale_rope_frequencies", "rope", "silu", "linear", "gqa_attention",
     "gqa_attention_rows", "block_forward", "block_forward_rows", "stack_forward", "greedy_generate",
-    "swiglu", "moe_route", "moe_ffn",
+    "swiglu", "moe_route", "moe_ffn", "block_residual_h",
     "ffn_hidden_dim", "kv_values_per_token", "block_param_count", "model_param_count",
 ]
 
@@ -309,6 +309,22 @@ def block_forward(cfg: dict, w: dict, x: np.ndarray, start_pos: int, k_cache: np
     route: for a mixture-of-experts block, optional (ids, weights) [B*S, k]
     replacing the router's choice (see moe_ffn).
     """
+    x = np.asarray(x, dtype=np.float64)
+    B = x.shape[0]
+    h, kc, vc = block_residual_h(cfg, w, x, start_pos, k_cache, v_cache)
+    y = h + _ffn(cfg, w, h, route)
+    kfull = np.array(k_cache, dtype=np.float64, copy=True)
+    vfull = np.array(v_cache, dtype=np.float64, copy=True)
+    kfull[:B] = kc
+    vfull[:B] = vc
+    return y, kfull, vfull
+
+
+def block_residual_h(cfg: dict, w: dict, x: np.ndarray, start_pos: int, k_cache, v_cache):
+    """The attention half of the block: h = x + Wo Attn(RMSNorm(x)), plus the
+    caches of sequences 0 .. B - 1 with the new keys/values written.  The
+    first residual branch of [L3B] How it works; :func:`block_forward` adds the
+    feed-forward branch to it."""
     d, H, G, D = _dims(cfg)
     x = np.asarray(x, dtype=np.float64)
     B, S, _ = x.shape
@@ -316,13 +332,7 @@ def block_forward(cfg: dict, w: dict, x: np.ndarray, start_pos: int, k_cache: np
     kc, vc = _write_cache(np.asarray(k_cache, dtype=np.float64)[:B], np.asarray(v_cache, dtype=np.float64)[:B],
                           k, v, start_pos)
     o = gqa_attention(q, kc, vc, start_pos).reshape(B, S, H * D)
-    h = x + linear(o, w["wo"])
-    y = h + _ffn(cfg, w, h, route)
-    kfull = np.array(k_cache, dtype=np.float64, copy=True)
-    vfull = np.array(v_cache, dtype=np.float64, copy=True)
-    kfull[:B] = kc
-    vfull[:B] = vc
-    return y, kfull, vfull
+    return x + linear(o, w["wo"]), kc, vc
 
 
 def block_forward_rows(cfg: dict, w: dict, x: np.ndarray, start_pos: int, k_cache, v_cache, rows):

@@ -107,7 +107,8 @@ def make_cfg(shape, max_seq_len=None):
         shape.get("rope_layout", "interleaved")]
     return lb.make_config(shape["d_model"], shape["n_heads"], shape["n_kv_heads"], shape["d_ff"],
                           max_seq_len or shape["max_seq_len"], shape["norm_eps"], shape["rope_theta"],
-                          llama_dtype(shape), layout, shape.get("rope_scaling"))
+                          llama_dtype(shape), layout, shape.get("rope_scaling"), shape.get("n_experts", 0),
+                          shape.get("top_k", 0), shape.get("d_ff_shared", 0))
 
 
 def f64_weights(w: dict) -> dict:
