@@ -290,13 +290,21 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           for (int k = 0; k < 32; ++k) mx = fmaxf(mx, key0 + c + k > pos ? -INFINITY : sv[k]);
         }
       } else {
+        // four independent running maxima: the chain of dependent max operations is 4x shorter
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int c = 0; c < KV_TILE; c += 32) {
           float sv[32];
           ptx::tmem_ld32(s_col + c, sv);
 #pragma unroll
-          for (int k = 0; k < 32; k += 2) mx = ptx::max3(mx, sv[k], sv[k + 1]);
+          for (int k = 0; k < 32; k += 8) {
+            mq[0] = ptx::max3(mq[0], sv[k], sv[k + 1]);
+            mq[1] = ptx::max3(mq[1], sv[k + 2], sv[k + 3]);
+            mq[2] = ptx::max3(mq[2], sv[k + 4], sv[k + 5]);
+            mq[3] = ptx::max3(mq[3], sv[k + 6], sv[k + 7]);
+          }
         }
+        mx = fmaxf(ptx::max3(mq[0], mq[1], mq[2]), mq[3]);
       }
       const float m_tile = mx * a.scale_log2;
       const bool need = m_tile > m_run + RESCALE_THRESHOLD;
@@ -340,6 +348,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             if (key0 + c + k > pos) sv[k] = -INFINITY;
         }
         uint32_t pk[16];
+        uint64_t lc = ptx::f2pack(0.f, 0.f);  // this chunk's sum: a second, independent add chain
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
           float x0, x1, p0, p1;
@@ -350,9 +359,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             p0 = ptx::ex2_approx(x0);         // MUFU
             p1 = ptx::ex2_approx(x1);
           }
-          l2 = ptx::fadd2(l2, ptx::f2pack(p0, p1));
+          if ((k & 2) == 0)
+            l2 = ptx::fadd2(l2, ptx::f2pack(p0, p1));
+          else
+            lc = ptx::fadd2(lc, ptx::f2pack(p0, p1));
           pk[k / 2] = pack2(p0, p1);
         }
+        l2 = ptx::fadd2(l2, lc);
         ptx::tmem_st16(s_col + c / 2, pk);
       }
       ptx::tmem_st_wait();

@@ -277,6 +277,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+
 // Shared-memory matrix descriptor, K-major operand, 128-byte swizzle: rows of
 // 128 bytes, 8-row core groups 1024 bytes apart (stride byte offset), tile base
 // 1024-byte aligned; the start address advances by 32 bytes per K=16 step.
