@@ -60,8 +60,9 @@ struct GemmArgs {
   void *C;
   int M, N, K;
   int *status;
-  int splits;        // K splits per output tile (1: no split)
+  int splits;        // K splits of each split tile (1: no split)
   int ksteps_split;  // BK steps per split
+  int split_tiles;   // the last split_tiles tiles (raster order) are split; their pieces are the first units
   float *part;       // split-K accumulators [tiles][BM][BN] fp32 (zero at launch; left zero at exit)
   int *counters;     // split-K arrivals [tiles][4] (zero at launch; left zero at exit)
   const float *ss_in;  // ROWSCALE epilogues: per-row sum of squares of A's rows
@@ -302,9 +303,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int k_steps = (args.K + BK - 1) / BK;
   const GroupedTiles gt{args.group_off, args.n_groups, n_tiles};
   if constexpr (GROUPED) grid_dependency_wait();  // every role reads the group offsets
-  const int num_units = GROUPED ? gt.count() : m_tiles * n_tiles * args.splits;
-  // unit -> first A row, first W row, end of the valid A rows, N tile, K range in BK steps
-  auto unit_coords = [&](int u, int &a_row, int &w_row, int &m_end, int &nt, int &k0, int &k1) {
+  const int num_tiles = m_tiles * n_tiles;
+  const int split_units = GROUPED ? 0 : args.split_tiles * args.splits;
+  const int num_units = GROUPED ? gt.count() : split_units + (num_tiles - args.split_tiles);
+  // unit -> first A row, first W row, end of the valid A rows, N tile, K range in BK steps.
+  // Units [0, split_units) are the K pieces of the last split_tiles tiles (spread over
+  // every CTA first, so their reductions overlap the whole tiles that follow); the rest
+  // are whole tiles.  slot: the split tile's accumulator / counter index, -1 if whole.
+  auto unit_coords = [&](int u, int &a_row, int &w_row, int &m_end, int &nt, int &k0, int &k1, int &slot) {
     if constexpr (GROUPED) {
       int g, mt;
       gt.coords(u, g, mt, nt);
@@ -313,15 +319,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       w_row = g * args.N + nt * BN;
       k0 = 0;
       k1 = k_steps;
+      slot = -1;
     } else {
-      const int tile = u / args.splits, sp = u % args.splits;
+      int tile;
+      if (u < split_units) {
+        slot = u / args.splits;
+        tile = num_tiles - args.split_tiles + slot;
+        k0 = (u % args.splits) * args.ksteps_split;
+        k1 = min(k_steps, k0 + args.ksteps_split);
+      } else {
+        slot = -1;
+        tile = u - split_units;
+        k0 = 0;
+        k1 = k_steps;
+      }
       int mt;
       tile_coords(tile, m_tiles, n_tiles, mt, nt);
       a_row = mt * BM;
       m_end = args.M;
       w_row = nt * BN;
-      k0 = sp * args.ksteps_split;
-      k1 = min(k_steps, k0 + args.ksteps_split);
     }
   };
 
@@ -358,8 +374,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // kernel: request them before waiting for the activations.
       int pre = 0;
       if (!GROUPED && args.prefetch_w && (int)blockIdx.x < num_units) {
-        int a_row, w_row, m_end, nt, k0, k1;
-        unit_coords(blockIdx.x, a_row, w_row, m_end, nt, k0, k1);
+        int a_row, w_row, m_end, nt, k0, k1, slot;
+        unit_coords(blockIdx.x, a_row, w_row, m_end, nt, k0, k1, slot);
         pre = min(STAGES, k1 - k0);
         for (int i = 0; i < pre; ++i) {
           const uint32_t sb = smem0 + i * G::STAGE_BYTES + G::A_BYTES;
@@ -371,8 +387,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        int a_row, w_row, m_end, nt, k0, k1;
-        unit_coords(u, a_row, w_row, m_end, nt, k0, k1);
+        int a_row, w_row, m_end, nt, k0, k1, slot;
+        unit_coords(u, a_row, w_row, m_end, nt, k0, k1, slot);
         for (int k = k0; k < k1; ++k) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -404,8 +420,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int it = 0, tcount = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++tcount) {
-        int a_row, w_row, m_end, nt, k0, k1;
-        unit_coords(u, a_row, w_row, m_end, nt, k0, k1);
+        int a_row, w_row, m_end, nt, k0, k1, slot;
+        unit_coords(u, a_row, w_row, m_end, nt, k0, k1, slot);
         const int acc = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
         if (!ptx::mbar_wait(tempty_bar(acc), aph ^ 1, abort_flag, args.status, DEV_TIMEOUT_MMA)) break;
@@ -441,8 +457,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int row = q * 32 + lane;
     int tcount = 0;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++tcount) {
-      int a_row, w_row, m_end, nt, k0, k1;
-      unit_coords(u, a_row, w_row, m_end, nt, k0, k1);
+      int a_row, w_row, m_end, nt, k0, k1, slot;
+      unit_coords(u, a_row, w_row, m_end, nt, k0, k1, slot);
       const int acc = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
       bool ok = ptx::mbar_wait(tfull_bar(acc), aph, abort_flag, args.status, DEV_TIMEOUT_EPILOGUE);
@@ -452,7 +468,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // rows past the tile's valid range (the next group's rows, or past M) are
       // passed as row M, which every epilogue skips
       const int m = a_row + row < m_end ? a_row + row : args.M;
-      if (args.splits == 1) {
+      if (slot < 0) {
         float sq = 0.f;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
@@ -468,7 +484,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       } else {
         // split-K: add this warp's 32 x BN fp32 partial into the tile's accumulator,
         // release TMEM, count arrivals; the last split's warp finishes the tile
-        const int tile = u / args.splits;
+        const int tile = slot;
         const bool rows_live = a_row + q * 32 < args.M;
         float *acc_row = args.part + ((size_t)tile * BM + row) * BN;
 #pragma unroll 1
@@ -591,7 +607,8 @@ cudaError_t launch_cfg(const bf16 *A, const bf16 *W, GemmArgs args, cudaStream_t
     return cudaErrorInvalidValue;
   int grid = sm_count();
   if (!GROUPED) {  // grouped: the tile count is on the device; every SM takes part
-    const int units = ((args.M + BM - 1) / BM) * ((args.N + BN - 1) / BN) * args.splits;
+    const int tiles = ((args.M + BM - 1) / BM) * ((args.N + BN - 1) / BN);
+    const int units = args.split_tiles * args.splits + tiles - args.split_tiles;
     grid = units < grid ? units : grid;
   }
   count_launch();
@@ -651,8 +668,8 @@ cudaError_t launch_gemm_grouped(const bf16 *A, const bf16 *W, void *C, int M, in
   else if (N % 64 == 0)
     bn = 64;
   if (bn == 0) return cudaErrorInvalidValue;
-  GemmArgs args{nullptr, C, M, N, K, status, 1, (K + BK - 1) / BK, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f, {},
-                0, group_off, n_groups};
+  GemmArgs args{nullptr, C, M, N, K, status, 1, (K + BK - 1) / BK, 0, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f,
+                {}, 0, group_off, n_groups};
   if (epi == EPI_STORE) {
     switch (bn) {
       case 256: return launch_cfg<EPI_STORE, 256, true>(A, W, args, st);
@@ -687,6 +704,29 @@ GemmPlan plan_gemm(int M, int N, int K, size_t ws_part_bytes, int ws_counter_slo
         p.bn = bns[i];
       }
     }
+    // A short partial last wave (at most a quarter of the SMs busy) leaves most SMs
+    // idle for a whole tile time: split its tiles along K into pieces that every SM
+    // shares (run first, so their reductions overlap the full waves).  The tail then
+    // costs ceil(tail * s / sms) / s of a tile time instead of one, plus the pieces'
+    // reduction (charged as 0.05 of a tile).  Longer tails gain less than the L2
+    // reductions of their many pieces cost (measured), and so do short K loops.
+    const int tiles = tiles_for(p.bn), tail = tiles % sms;
+    if (tail > 0 && 4 * tail <= sms && k_steps >= 32 && (size_t)tail * BM * p.bn * sizeof(float) <= ws_part_bytes &&
+        tail * 4 <= ws_counter_slots) {
+      double best_tail = 1.0;
+      for (int s = 2; s <= 16 && k_steps / s >= 4; ++s) {
+        const double cost = (double)((tail * s + sms - 1) / sms) / s + 0.05;
+        if (cost < best_tail - 1e-9) {
+          best_tail = cost;
+          p.splits = s;
+        }
+      }
+      if (p.splits > 1) {
+        p.ksteps_split = (k_steps + p.splits - 1) / p.splits;
+        p.splits = (k_steps + p.ksteps_split - 1) / p.ksteps_split;
+        p.split_tiles = tail;
+      }
+    }
     return p;
   }
   // Few output tiles (decode: weight streaming): pick the tile width and K split
@@ -719,6 +759,7 @@ GemmPlan plan_gemm(int M, int N, int K, size_t ws_part_bytes, int ws_counter_slo
     }
   }
   if (p.splits == 1) p.ksteps_split = 0;
+  p.split_tiles = p.splits > 1 ? tiles_for(p.bn) : 0;
   return p;
 }
 
@@ -746,8 +787,8 @@ cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C,
       return cudaErrorInvalidValue;
   }
   const GemmPlan plan = plan_gemm(M, N, K, ws != nullptr ? ws->part_bytes : 0, ws != nullptr ? ws->counter_slots : 0);
-  GemmArgs args{R, C, M, N, K, status, 1, (K + BK - 1) / BK, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f, {},
-                weights_static ? 1 : 0, nullptr, 0};
+  GemmArgs args{R, C, M, N, K, status, 1, (K + BK - 1) / BK, 0, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f,
+                {}, weights_static ? 1 : 0, nullptr, 0};
   if (scatter != nullptr) args.qkv = *scatter;
   if (norm != nullptr) {
     args.ss_in = norm->ss_in;
@@ -758,6 +799,7 @@ cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C,
   if (plan.splits > 1) {
     args.splits = plan.splits;
     args.ksteps_split = plan.ksteps_split;
+    args.split_tiles = plan.split_tiles;
     args.part = ws->part;
     args.counters = ws->counters;
   }

@@ -27,11 +27,14 @@ struct GemmWorkspace {
 size_t gemm_splitk_part_bytes();
 int gemm_splitk_counter_slots();
 
-// Tile width and K split chosen for a shape (split-K only when ws can hold it).
+// Tile width and K split chosen for a shape (split-K only when ws can hold it):
+// few-row shapes split every tile; large shapes split only the tiles of a
+// partial last wave.
 struct GemmPlan {
   int bn = 256;
-  int splits = 1;
-  int ksteps_split = 0;
+  int splits = 1;       // K pieces of each split tile
+  int ksteps_split = 0;  // BK steps per piece
+  int split_tiles = 0;   // how many tiles (the last ones in raster order) are split
 };
 GemmPlan plan_gemm(int M, int N, int K, size_t ws_part_bytes, int ws_counter_slots);
 
