@@ -192,9 +192,16 @@ def max_over_ranks(v, world):
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_throughput(world, tokens_per_rank_step, steps, max_ms):
+    """Whole-job tokens/s of `world` replicas that each ran `steps` steps of `tokens_per_rank_step`
+    tokens, timed by the slowest rank (max_ms over the timed region)."""
+    return world * tokens_per_rank_step * steps / (max_ms / 1e3)
 
 
 def run_reference(args, world, rank):
@@ -319,7 +326,7 @@ def main():
     lb.check(lb.llama_block_device_status(blk), "device status")
     max_ms = max_over_ranks(elapsed_ms, world)
     ms_per_step = max_ms / args.steps
-    value = world * B * S * args.steps / (max_ms / 1e3)
+    value = replica_throughput(world, B * S, args.steps, max_ms)
 
     # ---- end to end: host buffers through llama_block_forward_host ----
     xh = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -336,7 +343,7 @@ def main():
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
-    e2e_value = world * B * S * e2e_steps / (e2e_ms / 1e3)
+    e2e_value = replica_throughput(world, B * S, e2e_steps, e2e_ms)
     io_bytes = B * S * d * 2
 
     # ---- roofline of the dominant kernel (gate/up + SwiGLU GEMM) ----
