@@ -94,8 +94,21 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 
 // Columns n .. n+15 of row m (EPI_STORE / EPI_RESIDUAL / EPI_F32OUT).  With
 // SQSUM, returns the sum of squares of the bf16 values stored.
+// Residual of columns n .. n+31 of row m as four 16-byte vectors, loaded ahead of its
+// epilogue chunk (vec false: the row is out of range or the columns are not whole; the
+// epilogue then loads what it needs itself).
+__device__ __forceinline__ void load_residual32(const GemmArgs &a, int m, int n, uint4 (&r)[4], bool &vec) {
+  vec = m < a.M && n + 32 <= a.N && (a.N & 7) == 0;
+  if (vec) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(a.R + (size_t)m * a.N + n);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = p[i];
+  }
+}
+
 template <int EPI, bool SQSUM = false>
-__device__ __forceinline__ float epilogue_chunk16(const float *v, const GemmArgs &a, int m, int n) {
+__device__ __forceinline__ float epilogue_chunk16(const float *v, const GemmArgs &a, int m, int n,
+                                                  const uint4 *res = nullptr) {
   if (m >= a.M || n >= a.N) return 0.f;
   const size_t base = (size_t)m * a.N + n;
   float sq = 0.f;
@@ -118,7 +131,8 @@ __device__ __forceinline__ float epilogue_chunk16(const float *v, const GemmArgs
     if constexpr (EPI == EPI_RESIDUAL) {
       const bf16 *r = a.R + base;
       if (vec) {
-        uint4 r0 = *reinterpret_cast<const uint4 *>(r), r1 = *reinterpret_cast<const uint4 *>(r + 8);
+        uint4 r0 = res != nullptr ? res[0] : *reinterpret_cast<const uint4 *>(r);
+        uint4 r1 = res != nullptr ? res[1] : *reinterpret_cast<const uint4 *>(r + 8);
         const bf16 *p0 = reinterpret_cast<const bf16 *>(&r0), *p1 = reinterpret_cast<const bf16 *>(&r1);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -212,7 +226,8 @@ __device__ __forceinline__ void qkv_rope_chunk32(const float (&v)[32], const Gem
 }
 
 template <int EPI>
-__device__ __forceinline__ float epilogue_chunk32(float (&v)[32], const GemmArgs &a, int m, int n) {
+__device__ __forceinline__ float epilogue_chunk32(float (&v)[32], const GemmArgs &a, int m, int n,
+                                                  const uint4 *res = nullptr) {
   if constexpr (EPI == EPI_STORE_ROWSCALE || EPI == EPI_SWIGLU_ROWSCALE || EPI == EPI_QKV_ROPE ||
                 EPI == EPI_F32OUT_ROWSCALE) {
     // RMSNorm of A's row m, applied to the GEMM result (the gain is folded into W)
@@ -245,10 +260,11 @@ __device__ __forceinline__ float epilogue_chunk32(float (&v)[32], const GemmArgs
     epilogue_chunk16<EPI_STORE>(v + 16, a, m, n + 16);
     return 0.f;
   } else if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
-    return epilogue_chunk16<EPI_RESIDUAL, true>(v, a, m, n) + epilogue_chunk16<EPI_RESIDUAL, true>(v + 16, a, m, n + 16);
+    return epilogue_chunk16<EPI_RESIDUAL, true>(v, a, m, n, res) +
+           epilogue_chunk16<EPI_RESIDUAL, true>(v + 16, a, m, n + 16, res != nullptr ? res + 2 : nullptr);
   } else {
-    epilogue_chunk16<EPI>(v, a, m, n);
-    epilogue_chunk16<EPI>(v + 16, a, m, n + 16);
+    epilogue_chunk16<EPI>(v, a, m, n, res);
+    epilogue_chunk16<EPI>(v + 16, a, m, n + 16, res != nullptr ? res + 2 : nullptr);
     return 0.f;
   }
 }
@@ -470,11 +486,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int m = a_row + row < m_end ? a_row + row : args.M;
       if (slot < 0) {
         float sq = 0.f;
+        if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_SQSUM) {
+          // the next chunk's residual is loaded while this chunk is finished
+          uint4 rc[4], rn[4];
+          bool vc, vn = false;
+          load_residual32(args, m, nt * BN, rc, vc);
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          float v[32];
-          ptx::tmem_ld32(trow + c, v);
-          sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + c);
+          for (int c = 0; c < BN; c += 32) {
+            if (c + 32 < BN) load_residual32(args, m, nt * BN + c + 32, rn, vn);
+            float v[32];
+            ptx::tmem_ld32(trow + c, v);
+            sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + c, vc ? rc : nullptr);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) rc[i] = rn[i];
+            vc = vn;
+          }
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < BN; c += 32) {
+            float v[32];
+            ptx::tmem_ld32(trow + c, v);
+            sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + c);
+          }
         }
         ptx::tc_fence_before();
         ptx::mbar_arrive(tempty_bar(acc));
