@@ -561,18 +561,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   __stcg(reinterpret_cast<float4 *>(acc_row + c + i), make_float4(0.f, 0.f, 0.f, 0.f));
               }
             };
+            constexpr bool kRes = EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_SQSUM;
             float v[32], nx[32];
+            uint4 rc[4], rn[4];  // residual of the current / next chunk (residual epilogues)
+            bool vc = false, vn = false;
             load_sums(0, v);
             clear_sums(0);
+            if (kRes) load_residual32(args, m, nt * BN, rc, vc);
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
               if (c + 32 < BN) {
                 load_sums(c + 32, nx);
                 clear_sums(c + 32);
+                if (kRes) load_residual32(args, m, nt * BN + c + 32, rn, vn);
               }
-              sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + c);
+              sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + c, vc ? rc : nullptr);
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] = nx[i];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) rc[i] = rn[i];
+              vc = vn;
             }
             if (lane == 0) args.counters[tile * 4 + q] = 0;
             if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
@@ -780,8 +788,11 @@ GemmPlan plan_gemm(int M, int N, int K, size_t ws_part_bytes, int ws_counter_slo
         continue;
       const int rounds = (units + sms - 1) / sms;
       // + 12 K steps of fixed per-unit cost (pipeline fill, epilogue; measured on the
-      // decode shapes); split reductions add the partial rows once more
-      const double cost = (double)rounds * (kss + 12) * (16.0 + bn / 8.0) + (splits > 1 ? bn / 8.0 : 0.0);
+      // decode shapes); each split piece's reduction into the tile's accumulator
+      // (L2 atomics on the same lines, then the last piece's serial finish) adds
+      // about two rows of weights' worth per piece (measured on the decode shapes:
+      // 9 pieces of a 256-wide tile lose to 4 of a 128-wide one)
+      const double cost = (double)rounds * (kss + 12) * (16.0 + bn / 8.0) + (splits > 1 ? splits * bn / 4.0 : 0.0);
       if (cost < best - 1e-9 || (cost <= best + 1e-9 && units > best_units && units <= sms)) {
         best = cost;
         best_units = units;
