@@ -686,24 +686,52 @@ def bench_decode(lb, torch, w, dev, stream, args, peaks):
     us_plain = 1e3 * e0.elapsed_time(e1) / steps
     # the decode step as a CUDA graph (launch-bound inner loop): one captured forward, replayed
     gstream = torch.cuda.Stream(device=dev)
-    graph = torch.cuda.CUDAGraph()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(gstream):
-        lb.check(lb.llama_block_forward(blk, x, y, B, 1, sp, kv, gstream))  # warm the capture stream
-        gstream.synchronize()
-        with torch.cuda.graph(graph, stream=gstream):
-            lb.check(lb.llama_block_forward(blk, x, y, B, 1, sp, kv, gstream))
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(steps):
-        graph.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
+
+    def graph_us():
+        graph = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(gstream):
+            lb.check(lb.llama_block_forward(blk, x, y, B, 1, sp, kv, gstream))  # warm the capture stream
+            gstream.synchronize()
+            with torch.cuda.graph(graph, stream=gstream):
+                lb.check(lb.llama_block_forward(blk, x, y, B, 1, sp, kv, gstream))
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return 1e3 * e0.elapsed_time(e1) / steps
+
+    us_kernels = graph_us()
     lb.check(lb.llama_block_device_status(blk))
+    # the same step as one cooperative kernel (fused decode mode)
+    fused = {"available": False}
+    if lb.llama_block_set_decode_mode(blk, lb.LLAMA_DECODE_FUSED) == lb.LLAMA_OK:
+        for _ in range(args.warmup):
+            lb.check(lb.llama_block_forward(blk, x, y, B, 1, sp, kv, stream))
+        torch.cuda.synchronize()
+        n0 = lb.llama_kernel_launch_count()
+        e0.record(stream)
+        for _ in range(steps):
+            lb.check(lb.llama_block_forward(blk, x, y, B, 1, sp, kv, stream))
+        e1.record(stream)
+        fused_per_forward = (lb.llama_kernel_launch_count() - n0) // steps
+        torch.cuda.synchronize()
+        fused = {"available": True, "us_per_step_plain_launches": 1e3 * e0.elapsed_time(e1) / steps,
+                 "kernels_per_step": fused_per_forward}
+        try:
+            fused["us_per_step"] = graph_us()
+        except Exception as ex:  # capture of a cooperative launch refused: plain launches only
+            torch.cuda.synchronize()
+            fused["graph_error"] = str(ex)[:200]
+            fused["us_per_step"] = fused["us_per_step_plain_launches"]
+        lb.check(lb.llama_block_device_status(blk))
+        lb.check(lb.llama_block_set_decode_mode(blk, lb.LLAMA_DECODE_KERNELS))
     lb.llama_block_destroy(blk)
-    us = 1e3 * e0.elapsed_time(e1) / steps
+    us = us_kernels
     att_ms = total_ms[3] / max(launches[3], 1)
     gbs = decode_attention_bytes(s) / (att_ms / 1e3) / 1e9
     hbm = float(peaks["hbm_gbs"])
@@ -714,6 +742,8 @@ def bench_decode(lb, torch, w, dev, stream, args, peaks):
             "step_hbm_gbs": step_bytes / (us / 1e6) / 1e9, "step_hbm_frac": step_bytes / (us / 1e6) / 1e9 / hbm,
             "attention_us": 1e3 * att_ms, "attention_gbs": gbs, "attention_hbm_frac": gbs / hbm,
             "hbm_peak_gbs": hbm, "kernels_per_step": per_forward, "gpu_launches": per_forward * steps,
+            "fused_kernel": dict(fused, **({"step_hbm_frac": step_bytes / (fused["us_per_step"] / 1e6) / 1e9 / hbm}
+                                           if fused.get("us_per_step") else {})),
             "step_us": {lb.llama_profile_step_name(i): 1e3 * total_ms[i] / max(launches[i], 1)
                         for i in range(len(launches))}}
 

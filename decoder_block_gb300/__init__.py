@@ -30,6 +30,8 @@ LLAMA_F32 = 0
 LLAMA_BF16 = 1
 LLAMA_ROPE_INTERLEAVED = 0
 LLAMA_ROPE_HALVES = 1
+LLAMA_DECODE_KERNELS = 0
+LLAMA_DECODE_FUSED = 1
 
 EPI_STORE = 0
 EPI_RESIDUAL = 1
@@ -83,6 +85,8 @@ def load() -> ctypes.CDLL:
                                           POINTER(llama_kv_cache), c_void_p]),
         "llama_block_destroy": (None, [c_void_p]),
         "llama_block_device_status": (st, [c_void_p]),
+        "llama_block_set_decode_mode": (st, [c_void_p, c_int32]),
+        "llama_stack_set_decode_mode": (st, [c_void_p, c_int32]),
         "llama_stack_create": (st, [POINTER(llama_config), c_int32, c_int32, c_void_p, POINTER(llama_block_weights),
                                     c_void_p, c_void_p, c_int32, POINTER(c_void_p)]),
         "llama_stack_generate": (st, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
@@ -183,6 +187,14 @@ def llama_block_destroy(blk) -> None:
 
 def llama_block_device_status(blk) -> int:
     return load().llama_block_device_status(blk)
+
+
+def llama_block_set_decode_mode(blk, mode: int) -> int:
+    return load().llama_block_set_decode_mode(blk, mode)
+
+
+def llama_stack_set_decode_mode(stk, mode: int) -> int:
+    return load().llama_stack_set_decode_mode(stk, mode)
 
 
 def llama_stack_create(cfg: llama_config, n_layers, vocab, embed, layers, final_norm, lm_head, max_tokens):

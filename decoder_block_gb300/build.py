@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libllama_block.so")
-SOURCES = ["runtime.cu", "ops.cu", "simt_kernels.cu", "gemm_tc.cu", "attention.cu", "decode_attn.cu", "decode_tc.cu", "noalloc.cu", "moe.cu"]
+SOURCES = ["runtime.cu", "ops.cu", "simt_kernels.cu", "gemm_tc.cu", "attention.cu", "decode_attn.cu", "decode_tc.cu", "noalloc.cu", "moe.cu", "decode_fused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

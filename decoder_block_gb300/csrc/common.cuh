@@ -19,6 +19,7 @@ enum DeviceStatusCode : int {
   DEV_TIMEOUT_MMA = 2,
   DEV_TIMEOUT_EPILOGUE = 3,
   DEV_TIMEOUT_ATTN = 4,
+  DEV_TIMEOUT_PHASE = 5,  // fused decode kernel: a phase barrier wait ran out
   DEV_BAD_TOKEN = 16,
 };
 

@@ -17,6 +17,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "decode_combine.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tc_kernels.h"
@@ -268,18 +269,7 @@ __global__ void __launch_bounds__(D) attn_decode_combine(const float *__restrict
                                                          int n_split) {
   allow_dependents_launch();
   grid_dependency_wait();
-  const int bh = blockIdx.x, d = threadIdx.x;
-  const float *p = part + (size_t)bh * n_split * (D + 2);
-  float m = -INFINITY;
-  for (int s = 0; s < n_split; ++s) m = fmaxf(m, p[s * (D + 2) + D]);
-  float ov = 0.f, lv = 0.f;
-  for (int s = 0; s < n_split; ++s) {
-    const float ms = p[s * (D + 2) + D];
-    const float f = (ms == -INFINITY) ? 0.f : ptx::ex2_approx(ms - m);
-    ov = fmaf(f, p[s * (D + 2) + d], ov);
-    lv = fmaf(f, p[s * (D + 2) + D + 1], lv);
-  }
-  o[(size_t)bh * D + d] = __float2bfloat16_rn(ov / lv);
+  decode_combine_element<D>(part, o, blockIdx.x, threadIdx.x, n_split);
 }
 
 template <int D, int RP>

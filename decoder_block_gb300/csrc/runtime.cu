@@ -108,6 +108,8 @@ struct Workspace {
   int *route_ids = nullptr, *route_pos = nullptr, *counts = nullptr, *offsets = nullptr, *fill = nullptr;
   void *xin_e = nullptr, *act_e = nullptr, *y_e = nullptr, *act_s = nullptr, *hs = nullptr;
   int last_tokens = 0;  // B * S of the most recent forward (routing introspection)
+  unsigned *fused_sync = nullptr;  // phase barrier words of the fused decode kernel
+  int decode_mode = LLAMA_DECODE_KERNELS;
 };
 
 // Optional per-step event timing of block forwards (llama_block_profile_*).
@@ -347,6 +349,7 @@ llama_status alloc_workspace(const Dims &dm, int max_tokens, bool staging, Alloc
     ws->gemm.counters = (int *)al.alloc((size_t)ws->gemm.counter_slots * sizeof(int));
     ws->ss_x = (float *)al.alloc(T * sizeof(float));
     ws->ss_h = (float *)al.alloc(T * sizeof(float));
+    ws->fused_sync = (unsigned *)al.alloc(2 * sizeof(unsigned));
   }
   if (al.failed) return LLAMA_ERR_OOM;
   if (clear_gemm_scratch(ws->gemm) != cudaSuccess) return LLAMA_ERR_CUDA;
@@ -423,9 +426,54 @@ llama_status forward_moe(const Dims &dm, const Weights &w, const Workspace &ws, 
   return LLAMA_OK;
 }
 
+// A decode step this handle may run as the fused kernel (decode_fused.cu).
+bool fused_decode_eligible(const Dims &dm, int S) {
+  return S == 1 && dm.dtype == LLAMA_BF16 && !dm.moe() && dm.fused_qkv_rope() &&
+         attn_decode_tc_supported(dm.H, dm.G, dm.D);
+}
+
+llama_status forward_decode_fused(const Dims &dm, const Weights &w, const Workspace &ws, const float2 *rope,
+                                  const bf16 *x, bf16 *y, int B, int start_pos, const llama_kv_cache *kv, int *status,
+                                  cudaStream_t st) {
+  DecodeFusedParams p;
+  p.x = x;
+  p.y = y;
+  p.wqkv = (const bf16 *)w.wqkv;
+  p.wo = (const bf16 *)w.wo;
+  p.w_gu = (const bf16 *)w.w_gu;
+  p.w_down = (const bf16 *)w.w_down;
+  p.q = (bf16 *)ws.q;
+  p.o = (bf16 *)ws.o;
+  p.h = (bf16 *)ws.h;
+  p.act = (bf16 *)ws.act;
+  p.ss_x = ws.ss_x;
+  p.ss_h = ws.ss_h;
+  p.rope = rope;
+  p.kc = (bf16 *)kv->k;
+  p.vc = (bf16 *)kv->v;
+  p.cache_seq = kv->max_seq_len;
+  p.B = B;
+  p.start_pos = start_pos;
+  p.d = dm.d;
+  p.H = dm.H;
+  p.G = dm.G;
+  p.D = dm.D;
+  p.F = dm.F;
+  p.halves = dm.rope_halves;
+  p.eps = dm.eps;
+  p.gemm = ws.gemm;
+  p.attn = ws.attn;
+  p.sync = ws.fused_sync;
+  p.status = status;
+  LAUNCH(launch_decode_block_fused(p, st));
+  return LLAMA_OK;
+}
+
 llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, const float2 *rope, const bf16 *x,
                         bf16 *y, int B, int S, int start_pos, const llama_kv_cache *kv, int *status, Profiler *prof,
                         cudaStream_t st) {
+  if (ws.decode_mode == LLAMA_DECODE_FUSED && fused_decode_eligible(dm, S))
+    return forward_decode_fused(dm, w, ws, rope, x, y, B, start_pos, kv, status, st);
   const int M = B * S;
   bf16 *qkv = (bf16 *)ws.qkv, *q = (bf16 *)ws.q, *o = (bf16 *)ws.o, *h = (bf16 *)ws.h, *act = (bf16 *)ws.act;
   bf16 *kc = (bf16 *)kv->k, *vc = (bf16 *)kv->v;
@@ -704,6 +752,30 @@ const char *llama_profile_step_name(int32_t step) {
                                                    "attention", "o_projection_residual", "ffn_norm",
                                                    "gate_up_swiglu", "down_projection_residual"};
   return (step >= 0 && step < LLAMA_PROFILE_STEPS) ? names[step] : "unknown";
+}
+
+static llama_status set_decode_mode(Workspace &ws, int device, int32_t mode) {
+  if (mode != LLAMA_DECODE_KERNELS && mode != LLAMA_DECODE_FUSED) return LLAMA_ERR_INVALID_ARG;
+  if (mode == LLAMA_DECODE_FUSED) {
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess) return LLAMA_ERR_CUDA;
+    if (prev != device && cudaSetDevice(device) != cudaSuccess) return LLAMA_ERR_CUDA;
+    const bool ok = ws.fused_sync != nullptr && decode_fused_available();
+    if (prev != device) cudaSetDevice(prev);
+    if (!ok) return LLAMA_ERR_UNSUPPORTED;
+  }
+  ws.decode_mode = mode;
+  return LLAMA_OK;
+}
+
+llama_status llama_block_set_decode_mode(llama_block *blk, int32_t mode) {
+  if (blk == nullptr) return LLAMA_ERR_INVALID_ARG;
+  return set_decode_mode(blk->ws, blk->device, mode);
+}
+
+llama_status llama_stack_set_decode_mode(llama_stack *stk, int32_t mode) {
+  if (stk == nullptr) return LLAMA_ERR_INVALID_ARG;
+  return set_decode_mode(stk->ws, stk->device, mode);
 }
 
 llama_status llama_block_device_status(llama_block *blk) {

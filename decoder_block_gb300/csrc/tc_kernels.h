@@ -112,6 +112,34 @@ cudaError_t launch_attn_decode_tc(const bf16 *q, const bf16 *kc, const bf16 *vc,
                                   int H, int G, int cache_seq, const AttnScratch &scratch, int *status,
                                   cudaStream_t st);
 
+// The decode step (S = 1) of a dense bf16 block with d_head = 128 as one
+// cooperative kernel (decode_fused.cu): attention-norm statistics, QKV GEMM +
+// RoPE + cache write, decode attention, chunk merge, O GEMM + residual, gate/up
+// GEMM + SwiGLU, down GEMM + residual, separated by grid-wide barriers.  The
+// buffers and weights are those of the multi-kernel path (weights as repacked
+// at create: norm gains folded, gate/up interleaved).  sync: two device words
+// of this handle (cleared by the launch).
+struct DecodeFusedParams {
+  const bf16 *x = nullptr;  // [B][d]
+  bf16 *y = nullptr;        // [B][d]
+  const bf16 *wqkv = nullptr, *wo = nullptr, *w_gu = nullptr, *w_down = nullptr;
+  bf16 *q = nullptr, *o = nullptr, *h = nullptr, *act = nullptr;  // workspace activations
+  float *ss_x = nullptr, *ss_h = nullptr;
+  const float2 *rope = nullptr;
+  bf16 *kc = nullptr, *vc = nullptr;
+  int cache_seq = 0;
+  int B = 0, start_pos = 0, d = 0, H = 0, G = 0, D = 0, F = 0, halves = 0;
+  float eps = 0.f;
+  GemmWorkspace gemm;
+  AttnScratch attn;
+  unsigned *sync = nullptr;
+  int *status = nullptr;
+};
+// True when this device can run the fused kernel (cooperative launch with one
+// CTA per SM).
+bool decode_fused_available();
+cudaError_t launch_decode_block_fused(const DecodeFusedParams &p, cudaStream_t st);
+
 // Causal GQA attention over the bf16 cache; picks the prefill or decode kernel.
 cudaError_t launch_attention(const bf16 *q, const bf16 *kc, const bf16 *vc, bf16 *o, int B, int S, int start_pos,
                              int H, int G, int D, int cache_seq, const AttnScratch &scratch, int *status,

@@ -245,6 +245,23 @@ llama_status llama_block_profile_disable(llama_block *blk);
 llama_status llama_block_profile_read(llama_block *blk, int32_t *launches, float *total_ms);
 const char *llama_profile_step_name(int32_t step);
 
+/* How decode steps run ("Full Llama 3 transformer block", How it works: each
+ * step feeds one new token per sequence through the block against the cache).
+ * Applies to forwards with S == 1 of dense bf16 blocks whose d_head is 128;
+ * every other forward always runs as one kernel per step.
+ *   LLAMA_DECODE_KERNELS (default): one kernel per step of the block, each a
+ *     programmatic dependent of the previous one;
+ *   LLAMA_DECODE_FUSED: the whole block as one cooperative kernel (one CTA per
+ *     SM) whose phases -- the same steps with the same tile plans -- are
+ *     separated by grid-wide barriers.  Results equal the default's up to the
+ *     order of fp32 reductions.  Fused forwards are not profiled.
+ * Returns LLAMA_ERR_UNSUPPORTED (mode unchanged) when the device cannot run the
+ * fused kernel, LLAMA_ERR_INVALID_ARG for an unknown mode.  Not thread-safe
+ * against forwards of the same handle in flight on another host thread. */
+typedef enum { LLAMA_DECODE_KERNELS = 0, LLAMA_DECODE_FUSED = 1 } llama_decode_mode;
+llama_status llama_block_set_decode_mode(llama_block *blk, int32_t mode);
+llama_status llama_stack_set_decode_mode(llama_stack *stk, int32_t mode);
+
 /* Read and clear the handle's device status word.  Synchronises the device the
  * handle lives on.  Returns LLAMA_OK when no kernel reported a problem since
  * the last read, LLAMA_ERR_DEVICE_TIMEOUT when a bounded wait ran out,
