@@ -78,14 +78,16 @@ def kernel_traffic(name):
     with open(p) as f:
         table = json.load(f)
     ent = table.get(name)
-    if not ent:
+    if not ent or "sources" not in ent:
         return None
-    src = os.path.join(ROOT, ent["source"])
-    if not os.path.exists(src):
-        return None
-    with open(src, "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()
-    return ent["dram_bytes_per_launch"] if digest == ent["source_sha256"] else None
+    h = hashlib.sha256()
+    for rel in ent["sources"]:  # the kernel's source files, hashed in the listed order
+        src = os.path.join(ROOT, rel)
+        if not os.path.exists(src):
+            return None
+        with open(src, "rb") as f:
+            h.update(f.read())
+    return ent["dram_bytes_per_launch"] if h.hexdigest() == ent["sources_sha256"] else None
 
 
 # ----------------------------------------------------------- clock sampler ---
@@ -405,6 +407,7 @@ def main():
         secondary["llama3_8b_block_prefill_b4s2048"] = bench_block_shape(
             lb, torch, dev, stream, dict(SHAPE, B=4, S=2048), args, weights=w)
         secondary["llama4_scout_shaped_moe_block"] = bench_moe(lb, torch, dev, stream, args)
+        secondary["standalone_ops"] = bench_standalone_ops(lb, torch, dev, stream, args, peaks)
     stack = None
     if not args.no_stack:
         del w
@@ -570,6 +573,66 @@ def bench_moe(lb, torch, dev, stream, args, B=1, S=8192):
             "ms_per_step": ms, "tokens_per_s": T / (ms / 1e3), "tflops": (lin + att) / (ms / 1e3) / 1e12,
             "rows_per_expert": load, "steps": steps, "kernels_per_step": per_forward,
             "gpu_launches": per_forward * steps, "device_status": status}
+
+
+def bench_standalone_ops(lb, torch, dev, stream, args, peaks):
+    """The per-step entry points whose own HBM roofline the scope table lists:
+    RMSNorm over 8192 x 4096 bf16 (read x, write the normalised rows: 134.2 MB)
+    and RoPE + KV-cache write at the prefill workload (read qkv, write rotated q,
+    rotated k and v into the cache: 201.3 MB).  Each launch is timed alone with
+    CUDA events on the launching stream, after a read of a buffer larger than L2,
+    so that the operands come from HBM and L2 holds no dirty lines (after a
+    write flush the launch would also pay for writing back up to 129 MB of the
+    flush buffer, as much as its own traffic); the median is reported."""
+    T, d, H, G, D = 8192, SHAPE["d_model"], SHAPE["n_heads"], SHAPE["n_kv_heads"], SHAPE["d_model"] // SHAPE["n_heads"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(3)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    hbm = float(peaks["hbm_gbs"])
+    n = max(min(args.steps, 50), 10)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        times = []
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for i in range(n):
+            flush_sum = flush.sum()  # reads 512 MB: evicts the operands, leaves L2 clean
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3)
+        times.sort()
+        return times[len(times) // 2]
+
+    x = torch.randn((T, d), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    gain = (1 + 0.1 * torch.randn((d,), generator=g, device=dev, dtype=torch.float32)).to(torch.bfloat16)
+    out = torch.empty_like(x)
+    n0 = lb.llama_kernel_launch_count()
+    us_norm = timed(lambda: lb.check(lb.llama_op_rmsnorm(lb.LLAMA_BF16, x, gain, out, T, d, 1e-5, stream)))
+    launches = lb.llama_kernel_launch_count() - n0
+    norm_bytes = 2.0 * T * d * 2 + d * 2
+    del x, out
+    qkv = torch.randn((T, (H + 2 * G) * D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    q_out = torch.empty((T, H * D), device=dev, dtype=torch.bfloat16)
+    kc = torch.zeros((1, G, T, D), device=dev, dtype=torch.bfloat16)
+    vc = torch.zeros((1, G, T, D), device=dev, dtype=torch.bfloat16)
+    kv = lb.make_kv_cache(kc, vc, 1, T)
+    table = torch.empty((T, D // 2, 2), device=dev, dtype=torch.float32)
+    lb.check(lb.llama_op_rope_table(table, T, D, SHAPE["rope_theta"], None, stream))
+    n0 = lb.llama_kernel_launch_count()
+    us_rope = timed(lambda: lb.check(lb.llama_op_rope_kv_write(lb.LLAMA_BF16, qkv, q_out, kv, table, T, 1, T, 0, H, G,
+                                                               D, 0, stream)))
+    launches += lb.llama_kernel_launch_count() - n0
+    rope_bytes = T * (H + 2 * G) * D * 2.0 + T * H * D * 2.0 + 2.0 * T * G * D * 2
+    torch.cuda.synchronize()
+    return {"rmsnorm_8192x4096": {"us": us_norm, "gbs": norm_bytes / us_norm / 1e3,
+                                  "hbm_frac": norm_bytes / us_norm / 1e3 / hbm, "algorithmic_bytes": norm_bytes},
+            "rope_kv_write_b1s8192": {"us": us_rope, "gbs": rope_bytes / us_rope / 1e3,
+                                      "hbm_frac": rope_bytes / us_rope / 1e3 / hbm, "algorithmic_bytes": rope_bytes},
+            "hbm_peak_gbs": hbm, "gpu_launches": launches,
+            "timing": "median of single launches, L2 flushed before each by reading a 512 MB buffer"}
 
 
 def bench_stack(lb, torch, dev, stream, args, n_layers=32, vocab=128256, S=8192):

@@ -64,6 +64,7 @@ __global__ void rmsnorm_kernel(const T *__restrict__ x, const T *__restrict__ g,
   T *orow = out + (size_t)row * d;
   const int nv = d / V;
   float ss = 0.f;
+#pragma unroll 8
   for (int i = lane; i < nv; i += 32) {
     Vec16<T> v = load16(xr + (size_t)i * V);
 #pragma unroll
@@ -74,6 +75,7 @@ __global__ void rmsnorm_kernel(const T *__restrict__ x, const T *__restrict__ g,
   }
   ss = warp_sum(ss);
   const float r = rsqrtf(ss / (float)d + eps);
+#pragma unroll 8
   for (int i = lane; i < nv; i += 32) {
     Vec16<T> v = load16(xr + (size_t)i * V);
     Vec16<T> gv = load16(g + (size_t)i * V);
@@ -92,15 +94,16 @@ cudaError_t launch_rmsnorm(const T *x, const T *g, T *out, int rows, int d, floa
   const int nv = d / Vec16<T>::N;
   const int per_lane = (nv + 31) / 32;
   count_launch();
+  // Short rows stay in registers between the two halves of the computation.
+  // Longer rows (more than four 16-byte vectors per lane) are read twice, the
+  // second time from L2: a register-resident row of 16 vectors per lane needs
+  // ~150 registers, one 256-thread CTA per SM, too few loads in flight to keep
+  // HBM busy (measured at 8192 x 4096 bf16: 32 us resident vs 28 us re-read).
   switch (per_lane) {
     case 1: rmsnorm_reg_kernel<T, 1><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
     case 2: rmsnorm_reg_kernel<T, 2><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
     case 3: rmsnorm_reg_kernel<T, 3><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
     case 4: rmsnorm_reg_kernel<T, 4><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
-    case 5: case 6: case 7: case 8:
-      rmsnorm_reg_kernel<T, 8><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
-    case 9: case 10: case 11: case 12: case 13: case 14: case 15: case 16:
-      rmsnorm_reg_kernel<T, 16><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
     default: rmsnorm_kernel<T><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
   }
   return cudaGetLastError();
@@ -294,17 +297,18 @@ cudaError_t launch_rope_table(float2 *table, int max_seq, int D, double theta, c
 // start_pos + s; v: copied into the V cache ("Full Llama 3 transformer block",
 // How it works: RoPE rotates Q and K, keys/values are written into a cache).
 template <typename T>
-__global__ void rope_kv_kernel(const T *__restrict__ qkv, T *__restrict__ q_out, T *__restrict__ kc,
-                               T *__restrict__ vc, const float2 *__restrict__ table, int ntok, int S, int start_pos,
-                               int H, int G, int D, int cache_seq, int halves) {
+__global__ void __launch_bounds__(256) rope_kv_kernel(const T *__restrict__ qkv, T *__restrict__ q_out,
+                                                      T *__restrict__ kc, T *__restrict__ vc,
+                                                      const float2 *__restrict__ table, int t0, int S,
+                                                      int start_pos, int H, int G, int D, int cache_seq, int halves) {
+  // grid: x over the 16-byte vectors of one token's row, y over tokens t0 + blockIdx.y
   constexpr int V = Vec16<T>::N;
   const int row_vecs = (H + 2 * G) * D / V;
-  const size_t total = (size_t)ntok * row_vecs;
-  const size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
-  if (idx >= total) return;
-  const int t = (int)(idx / row_vecs);
-  const int col = (int)(idx % row_vecs) * V;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= row_vecs) return;
+  const int col = c * V;
   const int head = col / D, e = col % D;
+  const int t = t0 + blockIdx.y;
   const int b = t / S, s = t % S, p = start_pos + s;
   const T *src = qkv + (size_t)t * (H + 2 * G) * D + col;
   Vec16<T> x = load16(src);
@@ -316,14 +320,20 @@ __global__ void rope_kv_kernel(const T *__restrict__ qkv, T *__restrict__ q_out,
   T *dst = head < H ? q_out + (size_t)t * H * D + head * D
                     : kc + (((size_t)b * G + (head - H)) * cache_seq + p) * D;
   if (!halves) {
-    const float2 *cs = table + (size_t)p * (D / 2) + e / 2;
+    // pairs (e + 2k, e + 2k + 1) rotate by table[p][e/2 + k]; e/2 is a multiple of V/2,
+    // so the cos/sin pairs load as 16-byte vectors
+    const float4 *cs = reinterpret_cast<const float4 *>(table + (size_t)p * (D / 2) + e / 2);
     Vec16<T> o;
 #pragma unroll
-    for (int k = 0; k < V / 2; ++k) {
-      const float2 c = cs[k];
-      const float a = x.get(2 * k), bb = x.get(2 * k + 1);
-      o.set(2 * k, a * c.x - bb * c.y);
-      o.set(2 * k + 1, a * c.y + bb * c.x);
+    for (int k = 0; k < V / 4; ++k) {
+      const float4 c4 = cs[k];
+      float a = x.get(4 * k), bb = x.get(4 * k + 1);
+      o.set(4 * k, a * c4.x - bb * c4.y);
+      o.set(4 * k + 1, a * c4.y + bb * c4.x);
+      a = x.get(4 * k + 2);
+      bb = x.get(4 * k + 3);
+      o.set(4 * k + 2, a * c4.z - bb * c4.w);
+      o.set(4 * k + 3, a * c4.w + bb * c4.z);
     }
     store16(dst + e, o);
   } else if (e < D / 2) {
@@ -332,10 +342,10 @@ __global__ void rope_kv_kernel(const T *__restrict__ qkv, T *__restrict__ q_out,
     Vec16<T> lo, hi;
 #pragma unroll
     for (int k = 0; k < V; ++k) {
-      const float2 c = cs[k];
+      const float2 cv = cs[k];
       const float a = x.get(k), bb = y.get(k);
-      lo.set(k, a * c.x - bb * c.y);
-      hi.set(k, a * c.y + bb * c.x);
+      lo.set(k, a * cv.x - bb * cv.y);
+      hi.set(k, a * cv.y + bb * cv.x);
     }
     store16(dst + e, lo);
     store16(dst + e + D / 2, hi);
@@ -346,14 +356,22 @@ template <typename T>
 cudaError_t launch_rope_kv(const T *qkv, T *q_out, T *kc, T *vc, const float2 *table, int B, int S,
                            int start_pos, int H, int G, int D, int cache_seq, int halves, cudaStream_t st) {
   constexpr int V = Vec16<T>::N;
-  const size_t total = (size_t)B * S * ((H + 2 * G) * D / V);
-  if (total == 0) return cudaSuccess;
+  const int ntok = B * S;
+  const int row_vecs = (H + 2 * G) * D / V;
+  if (ntok <= 0 || row_vecs <= 0) return cudaSuccess;
   if (halves && (D / 2) % V != 0) return cudaErrorInvalidValue;
+  if (D % V != 0 || (D / 2) % (V / 2) != 0) return cudaErrorInvalidValue;
   const int threads = 256;
-  count_launch();
-  rope_kv_kernel<T><<<(unsigned)((total + threads - 1) / threads), threads, 0, st>>>(
-      qkv, q_out, kc, vc, table, B * S, S, start_pos, H, G, D, cache_seq, halves);
-  return cudaGetLastError();
+  const unsigned gx = (unsigned)((row_vecs + threads - 1) / threads);
+  for (int t0 = 0; t0 < ntok; t0 += 65535) {  // grid y is at most 65535 tokens per launch
+    const int n = ntok - t0 < 65535 ? ntok - t0 : 65535;
+    count_launch();
+    rope_kv_kernel<T><<<dim3(gx, (unsigned)n), threads, 0, st>>>(qkv, q_out, kc, vc, table, t0, S, start_pos, H, G,
+                                                                 D, cache_seq, halves);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 // ------------------------------------------------------ SIMT attention ---
