@@ -54,7 +54,7 @@ struct GemmCfg {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
-  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int NUM_BARS = 2 * STAGES + 7;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators (128, 256 or 512: powers of two)
 };
@@ -301,6 +301,58 @@ __device__ __forceinline__ void dense_unit(const GemmArgs &args, int bn, int u, 
   w_row = nt * bn;
 }
 
+// Split-K finish of columns [c_begin, c_end) of row r of split tile `tile`
+// (N tile nt; output row mm, args.M when the row is dead): read the summed
+// partials once, clear them for the next launch (the caller is their only
+// reader and every split has added its part), run the epilogue.  The next
+// chunk's sums and residual load while this chunk runs.  Returns the row's sum
+// of squares for EPI_RESIDUAL_SQSUM.  Called from one place of the epilogue.
+template <int EPI, int BN>
+__device__ __forceinline__ float splitk_finish(const GemmArgs &args, int tile, int nt, int r, int mm, int c_begin,
+                                            int c_end) {
+  float *sums = args.part + ((size_t)tile * BM + r) * BN;
+  auto load_sums = [&](int c, float (&v)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      const float4 p4 = mm < args.M ? __ldcg(reinterpret_cast<const float4 *>(sums + c + i))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[i] = p4.x;
+      v[i + 1] = p4.y;
+      v[i + 2] = p4.z;
+      v[i + 3] = p4.w;
+    }
+  };
+  auto clear_sums = [&](int c) {
+    if (mm < args.M) {
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) __stcg(reinterpret_cast<float4 *>(sums + c + i), make_float4(0.f, 0.f, 0.f, 0.f));
+    }
+  };
+  constexpr bool kRes = EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_SQSUM;
+  float sq = 0.f;
+  float v[32], nx[32];
+  uint4 rc[4], rn[4];  // residual of the current / next chunk (residual epilogues)
+  bool vc = false, vn = false;
+  load_sums(c_begin, v);
+  clear_sums(c_begin);
+  if (kRes) load_residual32(args, mm, nt * BN + c_begin, rc, vc);
+#pragma unroll 1
+  for (int c = c_begin; c < c_end; c += 32) {
+    if (c + 32 < c_end) {
+      load_sums(c + 32, nx);
+      clear_sums(c + 32);
+      if (kRes) load_residual32(args, mm, nt * BN + c + 32, rn, vn);
+    }
+    sq += epilogue_chunk32<EPI>(v, args, mm, nt * BN + c, vc ? rc : nullptr);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = nx[i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) rc[i] = rn[i];
+    vc = vn;
+  }
+  return sq;
+}
+
 // Tiles of the grouped mode: group g has ceil(rows_g / BM) x n_tiles tiles,
 // enumerated group by group, N-tile-major within a group (the m-tiles of one
 // weight tile run back to back).
@@ -339,6 +391,7 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * G::STAGE_BYTES);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + G::NUM_BARS);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *last_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);  // shared split-K finish
 
   const uint32_t smem0 = ptx::smem_u32(smem);
   const uint32_t bar0 = ptx::smem_u32(bars);
@@ -347,6 +400,10 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
   const uint32_t fin_bar = bar0 + 8u * (2 * STAGES + 4);
+  // shared split-K finish: every epilogue warp's partial is in (4 arrivals), and
+  // the arrival count of the tile is known (1 arrival)
+  const uint32_t parts_bar = bar0 + 8u * (2 * STAGES + 5);
+  const uint32_t count_bar = bar0 + 8u * (2 * STAGES + 6);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tiles = (args.M + BM - 1) / BM, n_tiles = (args.N + BN - 1) / BN;
@@ -386,6 +443,8 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
       ptx::mbar_init(tempty_bar(a), 128);
     }
     ptx::mbar_init(fin_bar, 1);
+    ptx::mbar_init(parts_bar, 4);
+    ptx::mbar_init(count_bar, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -508,6 +567,7 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     int tcount = 0;
+    int shared_splits = 0;  // split units finished jointly so far (phase of parts_bar / count_bar)
     for (int u = blockIdx.x; u < num_units && inputs_ready; u += gridDim.x, ++tcount) {
       int a_row, w_row, m_end, nt, k0, k1, slot;
       unit_coords(u, a_row, w_row, m_end, nt, k0, k1, slot);
@@ -552,7 +612,7 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
         }
       } else {
         // split-K: add this warp's 32 x BN fp32 partial into the tile's accumulator,
-        // release TMEM, count arrivals; the last split's warp finishes the tile
+        // release TMEM, count arrivals; the last split to arrive finishes the tile
         const int tile = slot;
         const bool rows_live = a_row + q * 32 < args.M;
         float *acc_row = args.part + ((size_t)tile * BM + row) * BN;
@@ -567,61 +627,62 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
         }
         ptx::tc_fence_before();
         ptx::mbar_arrive(tempty_bar(acc));
-        if (rows_live) {
-          __threadfence();
+        // who finishes what: row fin_r of the tile (output row fin_m), columns
+        // [fin_c0, fin_c1); cnt_slot: the counter this lane returns to zero
+        bool do_fin = false;
+        int fin_r = 0, fin_m = args.M, fin_c0 = 0, fin_c1 = 0, cnt_slot = -1;
+        if (m_end - a_row > 64) {
+          // a full tile: each warp counts its own 32 rows and the last split's warp
+          // finishes them
+          if (rows_live) {
+            ptx::fence_acq_rel_gpu();
+            __syncwarp();
+            int prev = 0;
+            if (lane == 0) prev = atomicAdd(args.counters + tile * 4 + q, 1);
+            prev = __shfl_sync(0xffffffffu, prev, 0);
+            if (prev == args.splits - 1) {  // every split has added its partial
+              do_fin = true;
+              fin_r = row;
+              fin_m = m;
+              fin_c1 = BN;
+              cnt_slot = lane == 0 ? tile * 4 + q : -1;
+            }
+          }
+        } else {
+          // at most 64 live rows (the decode shapes): the tile's arrivals are
+          // counted once per CTA, and the last CTA's four epilogue warps share the
+          // finish, 16 rows x half the columns each, instead of one or two warps
+          // finishing whole 32-row slices
+          ptx::fence_acq_rel_gpu();
           __syncwarp();
-          int prev = 0;
-          if (lane == 0) prev = atomicAdd(args.counters + tile * 4 + q, 1);
-          prev = __shfl_sync(0xffffffffu, prev, 0);
-          if (prev == args.splits - 1) {  // every split has added its partial: finish the tile
-            __threadfence();
-            float sq = 0.f;
-            // the next chunk's sums are loaded while this chunk runs its epilogue
-            auto load_sums = [&](int c, float (&v)[32]) {
-#pragma unroll
-              for (int i = 0; i < 32; i += 4) {
-                const float4 p4 = m < args.M ? __ldcg(reinterpret_cast<const float4 *>(acc_row + c + i))
-                                             : make_float4(0.f, 0.f, 0.f, 0.f);
-                v[i] = p4.x;
-                v[i + 1] = p4.y;
-                v[i + 2] = p4.z;
-                v[i + 3] = p4.w;
-              }
-            };
-            // leave the scratch zero for the next launch: this warp is the only
-            // reader and every other split has already added its part
-            auto clear_sums = [&](int c) {
-              if (m < args.M) {
-#pragma unroll
-                for (int i = 0; i < 32; i += 4)
-                  __stcg(reinterpret_cast<float4 *>(acc_row + c + i), make_float4(0.f, 0.f, 0.f, 0.f));
-              }
-            };
-            constexpr bool kRes = EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_SQSUM;
-            float v[32], nx[32];
-            uint4 rc[4], rn[4];  // residual of the current / next chunk (residual epilogues)
-            bool vc = false, vn = false;
-            load_sums(0, v);
-            clear_sums(0);
-            if (kRes) load_residual32(args, m, nt * BN, rc, vc);
-#pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-              if (c + 32 < BN) {
-                load_sums(c + 32, nx);
-                clear_sums(c + 32);
-                if (kRes) load_residual32(args, m, nt * BN + c + 32, rn, vn);
-              }
-              sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + c, vc ? rc : nullptr);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = nx[i];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) rc[i] = rn[i];
-              vc = vn;
+          if (lane == 0) ptx::mbar_arrive(parts_bar);
+          const uint32_t sph = shared_splits & 1;
+          if (warp == 2) {
+            const bool in = ptx::mbar_wait(parts_bar, sph, abort_flag, args.status, DEV_TIMEOUT_EPILOGUE);
+            if (lane == 0) {
+              const int prev = in ? atomicAdd(args.counters + tile * 4, 1) : -1;
+              *last_flag = prev == args.splits - 1 ? 1 : 0;
+              ptx::mbar_arrive(count_bar);
             }
-            if (lane == 0) args.counters[tile * 4 + q] = 0;
-            if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
-              if (m < args.M) atomicAdd(args.ss_out + m, sq);
-            }
+            __syncwarp();
+          }
+          const bool known = ptx::mbar_wait(count_bar, sph, abort_flag, args.status, DEV_TIMEOUT_EPILOGUE);
+          ++shared_splits;
+          if (__all_sync(0xffffffffu, known) && *last_flag != 0) {
+            do_fin = true;
+            fin_r = (warp - 2) * 16 + (lane & 15);
+            fin_m = a_row + fin_r < m_end ? a_row + fin_r : args.M;
+            fin_c0 = (lane >> 4) * (BN / 2);
+            fin_c1 = fin_c0 + BN / 2;
+            cnt_slot = warp == 2 && lane == 0 ? tile * 4 : -1;
+          }
+        }
+        if (do_fin) {
+          ptx::fence_acq_rel_gpu();
+          const float sq = splitk_finish<EPI, BN>(args, tile, nt, fin_r, fin_m, fin_c0, fin_c1);
+          if (cnt_slot >= 0) args.counters[cnt_slot] = 0;
+          if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
+            if (fin_m < args.M) atomicAdd(args.ss_out + fin_m, sq);
           }
         }
       }

@@ -76,7 +76,7 @@ __device__ __forceinline__ void phase_arrive(const PhaseSync &s) {
   fence_proxy_async_all();
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
+    __threadfence();  // cumulative over the CTA's writes ordered before it by __syncthreads
     atomicAdd(s.arrivals, 1u);
   }
 }

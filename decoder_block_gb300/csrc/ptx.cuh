@@ -19,6 +19,11 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
+// Release/acquire fence at GPU scope: orders this thread's earlier memory
+// operations (also reductions) before its later ones as seen by other SMs.
+// Lighter than the sequentially consistent fence of __threadfence(), and enough
+// for the publish-then-count and count-then-read patterns of split reductions.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 // Ends an mbarrier's life (no pending arrivals or transactions may remain), so
 // that its shared memory can be used for something else, e.g. as another
 // barrier initialised afresh.
