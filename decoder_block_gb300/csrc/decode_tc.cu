@@ -69,6 +69,7 @@ cudaError_t attn_decode_tc_prepare(const bf16 *q, const bf16 *kc, const bf16 *vc
   a.status = status;
   a.o = o;
   a.part = reinterpret_cast<float *>(scratch.partial);
+  a.items = scratch.item_counters;
   if (a.n_split > 1 && (scratch.partial == nullptr ||
                         scratch.bytes < attn_decode_tc_scratch_bytes(B, H, a.kv_len)))
     return cudaErrorInvalidValue;

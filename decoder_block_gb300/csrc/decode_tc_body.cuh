@@ -12,8 +12,12 @@
 //                                                   query heads padded to 16)
 //   O^T[128 d x 16]        += V_tile^T . P^T       (V read as an MN-major operand)
 // Persistent CTAs (one per SM) walk work items (b, g, chunk of 512 positions):
-//   warp 0      TMA producer: Q_g (16 rows) per item, K and V tiles into a
-//               3-stage ring (tensor maps end at start_pos + 1: zeros beyond);
+//   warp 0      TMA producer: takes the next work item (from a grid-wide
+//               counter, so CTAs that stream faster take more items; or a
+//               fixed share), passes its index to the other roles next to its
+//               Q buffer (-1: no more), loads Q_g (16 rows) and the K and V
+//               tiles into a 3-stage ring (tensor maps end at start_pos + 1:
+//               zeros beyond);
 //   warp 1      tcgen05.mma issuer (double-buffered S^T, O^T per item parity);
 //   warps 2-5   one thread per position (TMEM lane): per-head max over the
 //               tile (warp shuffles + shared memory), p = 2^(s*log2e/sqrt(D) - m)
@@ -48,7 +52,8 @@ struct DtLayout {
   static constexpr int OFF_Q = OFF_V + DT_STAGES * KV_BYTES;  // 2 buffers
   static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;           // 2 buffers
   static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;          // [3 sets][4 warps][DT_N] floats
-  static constexpr int OFF_BAR = OFF_RED + 3 * 4 * DT_N * 4;
+  static constexpr int OFF_ITEM = OFF_RED + 3 * 4 * DT_N * 4;  // work item of each Q buffer (-1: no more)
+  static constexpr int OFF_BAR = OFF_ITEM + 16;
   // kv_full[3], kv_empty[3], q_full[2], q_empty[2], s_full[2], p_full[2], p_free[2], o_full[2], o_free[2], fin,
   // red_full[2] (per-tile max exchange), lred_full (per-item sum exchange)
   static constexpr int NBAR = 2 * DT_STAGES + 14 + 1 + 3;
@@ -62,6 +67,7 @@ struct DtArgs {
   int B, H, G, r, kv_len, n_split, n_items;
   float scale_log2;
   int *status;
+  int *items;  // [0] next work item, [1] CTAs finished (zero at launch, left zero); null: fixed share
 };
 
 // The 4 softmax warps exchange per-head values through shared memory; each
@@ -97,6 +103,7 @@ __device__ __forceinline__ void attn_decode_tc_run(const CUtensorMap *tmQ, const
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + L::NBAR);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   float *red = reinterpret_cast<float *>(smem + L::OFF_RED);
+  volatile int *item_slot = reinterpret_cast<volatile int *>(smem + L::OFF_ITEM);
 
   const uint32_t s0 = ptx::smem_u32(smem);
   const uint32_t b0 = ptx::smem_u32(bars);
@@ -175,11 +182,18 @@ __device__ __forceinline__ void attn_decode_tc_run(const CUtensorMap *tmQ, const
       ptx::tma_prefetch_desc(tmV);
       int tile = 0, nq = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < a.n_items && ok; it += gridDim.x, ++nq) {
-        int b, g, k0, nt;
-        item_coords(it, b, g, k0, nt);
+      for (;; ++nq) {
+        int it = a.items != nullptr ? atomicAdd(a.items, 1) : (int)blockIdx.x + nq * (int)gridDim.x;
+        if (it >= a.n_items) it = -1;
         const int qi = nq & 1;
         if (!ptx::mbar_wait(q_empty(qi), ((nq >> 1) & 1) ^ 1, abort_flag, a.status, DEV_TIMEOUT_PRODUCER)) break;
+        item_slot[qi] = it;  // published to the other roles by the q_full arrival
+        if (it < 0) {
+          ptx::mbar_arrive(q_full(qi));
+          break;
+        }
+        int b, g, k0, nt;
+        item_coords(it, b, g, k0, nt);
         ptx::mbar_arrive_expect_tx(q_full(qi), L::Q_BYTES);
         for (int at = 0; at < 2; ++at)
           ptx::tma_load_2d(s0 + L::OFF_Q + qi * L::Q_BYTES + at * (DT_N * 128), tmQ, at * 64, b * a.H + g * a.r,
@@ -198,6 +212,10 @@ __device__ __forceinline__ void attn_decode_tc_run(const CUtensorMap *tmQ, const
             ptx::tma_load_4d(s0 + L::OFF_V + st * L::KV_BYTES + at * L::ATOM, tmV, at * 64, key, g, b, kv_full(st));
           }
         }
+        if (!ok) {
+          ++nq;
+          break;
+        }
       }
       // drain the last issued loads
       int dummy = 0;
@@ -212,11 +230,13 @@ __device__ __forceinline__ void attn_decode_tc_run(const CUtensorMap *tmQ, const
       constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(DT_D, DT_N, false) | (1u << 15);
       int tile = 0, nq = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < a.n_items && ok; it += gridDim.x, ++nq) {
-        int b, g, k0, nt;
-        item_coords(it, b, g, k0, nt);
+      for (; ok; ++nq) {
         const int qi = nq & 1, ob = nq & 1;
         if (!ptx::mbar_wait(q_full(qi), (nq >> 1) & 1, abort_flag, a.status, DEV_TIMEOUT_MMA)) break;
+        const int it = item_slot[qi];
+        if (it < 0) break;  // no more work items
+        int b, g, k0, nt;
+        item_coords(it, b, g, k0, nt);
         if (!ptx::mbar_wait(o_free(ob), ((nq >> 1) & 1) ^ 1, abort_flag, a.status, DEV_TIMEOUT_MMA)) break;
         const uint32_t qbase = s0 + L::OFF_Q + qi * L::Q_BYTES;
         // S^T of tile t (global tile counter) into buffer t & 1, reading K stage t % STAGES.
@@ -282,7 +302,17 @@ __device__ __forceinline__ void attn_decode_tc_run(const CUtensorMap *tmQ, const
     }
     int tile = 0, nq = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < a.n_items && ok; it += gridDim.x, ++nq) {
+    for (; ok; ++nq) {
+      // the item of Q buffer nq & 1 (the producer's q_full arrival publishes it;
+      // waiting here never runs ahead: that buffer is refilled only after this
+      // item's last PV product, which needs this warp's P)
+      ok = ptx::mbar_wait(q_full(nq & 1), (nq >> 1) & 1, abort_flag, a.status, DEV_TIMEOUT_ATTN);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      const int it = item_slot[nq & 1];
+      if (it < 0) break;  // no more work items
       int b, g, k0, nt;
       item_coords(it, b, g, k0, nt);
       const int ob = nq & 1;
@@ -414,6 +444,14 @@ __device__ __forceinline__ void attn_decode_tc_run(const CUtensorMap *tmQ, const
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if (a.items != nullptr && threadIdx.x == 0) {
+    // every CTA's producer has taken its last item before counting itself done:
+    // the last one returns the counters to zero for the next launch
+    if (atomicAdd(a.items + 1, 1) == (int)gridDim.x - 1) {
+      atomicExch(a.items, 0);
+      atomicExch(a.items + 1, 0);
+    }
+  }
   if (sync.fused()) {  // the next phase reuses this shared memory and TMEM
     if (threadIdx.x == 0) {
       for (int i = 0; i < L::NBAR; ++i) ptx::mbar_inval(b0 + 8u * i);

@@ -343,6 +343,7 @@ llama_status alloc_workspace(const Dims &dm, int max_tokens, bool staging, Alloc
     const size_t bytes = attn_decode_scratch_bytes(max_tokens, dm.H, dm.D, dm.max_seq);
     ws->attn.partial = al.alloc(bytes);
     ws->attn.bytes = bytes;
+    ws->attn.item_counters = (int *)al.alloc(2 * sizeof(int));
     ws->gemm.part_bytes = gemm_splitk_part_bytes();
     ws->gemm.part = (float *)al.alloc(ws->gemm.part_bytes);
     ws->gemm.counter_slots = gemm_splitk_counter_slots();
@@ -353,6 +354,8 @@ llama_status alloc_workspace(const Dims &dm, int max_tokens, bool staging, Alloc
   }
   if (al.failed) return LLAMA_ERR_OOM;
   if (clear_gemm_scratch(ws->gemm) != cudaSuccess) return LLAMA_ERR_CUDA;
+  if (ws->attn.item_counters != nullptr && cudaMemset(ws->attn.item_counters, 0, 2 * sizeof(int)) != cudaSuccess)
+    return LLAMA_ERR_CUDA;
   if (dm.moe() && (cudaMemset(ws->counts, 0, (size_t)dm.E * sizeof(int)) != cudaSuccess ||
                    cudaMemset(ws->fill, 0, (size_t)dm.E * sizeof(int)) != cudaSuccess))
     return LLAMA_ERR_CUDA;
@@ -575,6 +578,8 @@ llama_status read_status(int *dev_status, int device, const Workspace *ws, const
   if (e == cudaSuccess) e = cudaMemset(dev_status, 0, sizeof(int));
   if (e == cudaSuccess && v != 0 && v != DEV_BAD_TOKEN && scratch != nullptr) {
     e = clear_gemm_scratch(*scratch);
+    if (e == cudaSuccess && ws->attn.item_counters != nullptr)
+      e = cudaMemset(ws->attn.item_counters, 0, 2 * sizeof(int));
     if (e == cudaSuccess && dm != nullptr && dm->moe()) e = cudaMemset(ws->counts, 0, (size_t)dm->E * sizeof(int));
     if (e == cudaSuccess && dm != nullptr && dm->moe()) e = cudaMemset(ws->fill, 0, (size_t)dm->E * sizeof(int));
   }

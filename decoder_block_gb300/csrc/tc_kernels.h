@@ -93,6 +93,10 @@ cudaError_t launch_interleave_rows(const bf16 *gate, const bf16 *up, bf16 *out, 
 struct AttnScratch {
   void *partial = nullptr;
   size_t bytes = 0;
+  // tensor-core decode attention: two ints, zero between launches (the last CTA
+  // of a launch returns them to zero); with them CTAs take work items as they
+  // free up instead of a fixed share.  Null: a fixed share per CTA.
+  int *item_counters = nullptr;
 };
 size_t attn_decode_scratch_bytes(int max_tokens, int H, int D, int max_seq);
 
