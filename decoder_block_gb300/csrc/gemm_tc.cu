@@ -48,8 +48,40 @@ int sm_count() {
   return n > 0 ? n : 1;
 }
 
+// Cluster split-K (the K pieces of a tile in one thread-block cluster, summed
+// through distributed shared memory) when a plan splits every tile, fits one
+// wave of one CTA per SM, and this device can hold all its clusters at once.
+// Every CTA of such a grid has exactly one unit.
+template <int EPI, int BN>
+bool cluster_split_fits(int tiles, int splits, int units) {
+  if (splits < 2 || splits > 8 || units != tiles * splits || units > sm_count()) return false;
+  static std::mutex mu;
+  static int fits[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};  // per cluster size: 0 unknown, then 1 + max clusters
+  std::lock_guard<std::mutex> lock(mu);
+  if (fits[splits] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)units);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = GemmCfg<BN>::SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_kernel<EPI, BN, false>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      clusters = 0;
+    }
+    fits[splits] = 1 + clusters;
+  }
+  return fits[splits] - 1 >= tiles;
+}
+
 template <int EPI, int BN, bool GROUPED = false>
-cudaError_t launch_cfg(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &args, cudaStream_t st) {
+cudaError_t launch_cfg(const CUtensorMap &ma, const CUtensorMap &mb, GemmArgs args, cudaStream_t st) {
   using G = GemmCfg<BN>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -59,14 +91,33 @@ cudaError_t launch_cfg(const CUtensorMap &ma, const CUtensorMap &mb, const GemmA
   });
   if (attr_err != cudaSuccess) return attr_err;
   int grid = sm_count();
+  int cluster = 1;
   if (!GROUPED) {  // grouped: the tile count is on the device; every SM takes part
     const int tiles = ((args.M + BM - 1) / BM) * ((args.N + BN - 1) / BN);
     const int units = args.split_tiles * args.splits + tiles - args.split_tiles;
     grid = units < grid ? units : grid;
+    if (args.splits > 1 && args.split_tiles == tiles && cluster_split_fits<EPI, BN>(tiles, args.splits, units)) {
+      args.cluster_split = 1;
+      cluster = args.splits;
+      grid = units;
+    }
   }
   count_launch();
-  return launch_pdl(gemm_tc_kernel<EPI, BN, GROUPED>, dim3(grid), dim3(NUM_THREADS), G::SMEM_BYTES, st, ma, mb,
-                    args);
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)cluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = G::SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = cluster > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, BN, GROUPED>, ma, mb, args);
 }
 
 template <int EPI>

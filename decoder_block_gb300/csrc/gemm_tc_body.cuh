@@ -79,6 +79,10 @@ struct GemmArgs {
   // the device (written by an earlier kernel), so the tile count is found there
   const int *group_off;
   int n_groups;
+  // cluster split-K: the grid is one unit per CTA and each cluster (of `splits`
+  // CTAs) holds the K pieces of one tile, summed through distributed shared
+  // memory instead of L2 (set by the launcher, never in a fused kernel)
+  int cluster_split;
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int &mt, int &nt) {
@@ -611,6 +615,23 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
           if (m < args.M) atomicAdd(args.ss_out + m, sq);
         }
       } else {
+        if (args.cluster_split) {
+          // cluster split-K: this CTA's only unit; its fp32 partial goes into the
+          // (now idle) stage buffers, [BN / 4][128 rows][4 columns], and the
+          // cluster sums the pieces at the end of the kernel
+#pragma unroll 1
+          for (int c = 0; c < BN; c += 32) {
+            float v[32];
+            ptx::tmem_ld32(trow + c, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              ptx::st_shared_v4(smem0 + (uint32_t)((((c >> 2) + i) * BM + row) * 16), v[4 * i], v[4 * i + 1],
+                                v[4 * i + 2], v[4 * i + 3]);
+          }
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(tempty_bar(acc));
+          continue;
+        }
         // split-K: add this warp's 32 x BN fp32 partial into the tile's accumulator,
         // release TMEM, count arrivals; the last split to arrive finishes the tile
         const int tile = slot;
@@ -687,6 +708,44 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
         }
       }
     }
+  }
+  if (!GROUPED && args.cluster_split) {
+    // Every CTA of the cluster holds one K piece of the same tile.  Once all
+    // partials are in shared memory, CTA `rank` finishes the 32-column chunks
+    // rank, rank + splits, ...: each epilogue thread (one tile row) sums the
+    // pieces in piece order (the result does not depend on timing) and runs the
+    // epilogue.  The second barrier keeps every CTA's shared memory alive until
+    // the others have read it.  Both barriers are reached by every thread.
+    ptx::cluster_sync();
+    if (warp >= 2) {
+      int a_row, w_row, nt, k0, k1, slot;
+      dense_unit(args, BN, blockIdx.x, a_row, w_row, nt, k0, k1, slot);
+      const int r = threadIdx.x - 64;  // tile row
+      const int m = a_row + r < args.M ? a_row + r : args.M;
+      const uint32_t rank = ptx::cluster_ctarank();
+      float sq = 0.f;
+      for (int ch = (int)rank; ch < BN / 32 && m < args.M; ch += args.splits) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        for (int pc = 0; pc < args.splits; ++pc) {
+          const uint32_t base = ptx::mapa_shared(smem0, (uint32_t)pc);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 p4 = ptx::ld_cluster_v4(base + (uint32_t)((((ch * 32) >> 2) + i) * BM + r) * 16);
+            v[4 * i] += p4.x;
+            v[4 * i + 1] += p4.y;
+            v[4 * i + 2] += p4.z;
+            v[4 * i + 3] += p4.w;
+          }
+        }
+        sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + ch * 32);
+      }
+      if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
+        if (m < args.M) atomicAdd(args.ss_out + m, sq);
+      }
+    }
+    ptx::cluster_sync();
   }
   ptx::tc_fence_before();
   __syncthreads();
