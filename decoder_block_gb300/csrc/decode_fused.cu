@@ -40,8 +40,9 @@ static_assert(FUSED_THREADS == NUM_THREADS && FUSED_THREADS == DT_THREADS, "phas
 constexpr uint32_t FUSED_TMEM_COLS = 512;  // the widest phase: two 256-column GEMM accumulators
 
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
-constexpr int FUSED_SMEM = cmax(cmax(GemmCfg<256>::SMEM_BYTES, GemmCfg<128>::SMEM_BYTES),
-                                cmax(GemmCfg<64>::SMEM_BYTES, DtLayout::BYTES));
+constexpr int FUSED_SMEM = cmax(cmax(cmax(GemmCfg<256>::SMEM_BYTES, GemmCfg<192>::SMEM_BYTES),
+                                     cmax(GemmCfg<128>::SMEM_BYTES, GemmCfg<64>::SMEM_BYTES)),
+                                DtLayout::BYTES);
 
 struct FusedMaps {
   CUtensorMap qkv_a, qkv_w, o_a, o_w, gu_a, gu_w, dn_a, dn_w, q, k, v;
@@ -91,6 +92,7 @@ __device__ __forceinline__ void gemm_phase(const CUtensorMap *ta, const CUtensor
                                         const PhaseSync s) {
   switch (bn) {
     case 256: gemm_tc_run<EPI, 256, false>(ta, tw, args, s); break;
+    case 192: gemm_tc_run<EPI, 192, false>(ta, tw, args, s); break;
     case 128: gemm_tc_run<EPI, 128, false>(ta, tw, args, s); break;
     default: gemm_tc_run<EPI, 64, false>(ta, tw, args, s); break;
   }

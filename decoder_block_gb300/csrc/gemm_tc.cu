@@ -124,6 +124,7 @@ template <int EPI>
 cudaError_t launch_epi(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &args, int bn, cudaStream_t st) {
   switch (bn) {
     case 256: return launch_cfg<EPI, 256>(ma, mb, args, st);
+    case 192: return launch_cfg<EPI, 192>(ma, mb, args, st);
     case 128: return launch_cfg<EPI, 128>(ma, mb, args, st);
     case 64: return launch_cfg<EPI, 64>(ma, mb, args, st);
   }
@@ -240,17 +241,20 @@ GemmPlan plan_gemm(int M, int N, int K, size_t ws_part_bytes, int ws_counter_slo
   // Few output tiles (decode: weight streaming): pick the tile width and K split
   // that minimise the per-SM load, rounds x (K steps per unit) x (shared-memory
   // fill per K step: 16 KB of A plus BN x 128 B of weights); ties go to more
-  // units (more SMs streaming weights at once).
+  // units (more SMs streaming weights at once).  192-wide tiles serve wide
+  // unsplit projections: 28672 gate/up rows make 150 of them, one per SM, where
+  // 256-wide tiles leave 40 SMs without weights to stream.
   double best = 1e30;
   int best_units = 0;
-  const int bns[3] = {256, 128, 64};
-  for (int i = 0; i < 3; ++i) {
+  const int bns[4] = {256, 192, 128, 64};
+  for (int i = 0; i < 4; ++i) {
     const int bn = bns[i];
     const int tiles = tiles_for(bn);
     for (int want = 1; want <= 16 && want <= k_steps; ++want) {
       const int kss = (k_steps + want - 1) / want;
       const int splits = (k_steps + kss - 1) / kss;
       const int units = tiles * splits;
+      if (bn == 192 && splits > 1) continue;
       if (splits > 1 && ((size_t)tiles * BM * bn * sizeof(float) > ws_part_bytes || tiles * 4 > ws_counter_slots))
         continue;
       const int rounds = (units + sms - 1) / sms;

@@ -5,8 +5,8 @@
 // the block (QKV, O, gate/up, down) and the LM head:  C = epi(A W^T), with A
 // [M,K] activations and W [N,K] nn.Linear weights, both bf16 and K-major.
 //
-// Per CTA (one per SM, 192 threads), output tiles of 128 x BN (BN = 256, 128
-// or 64, picked per shape on the host):
+// Per CTA (one per SM, 192 threads), output tiles of 128 x BN (BN = 256, 192,
+// 128 or 64, picked per shape on the host):
 //   warp 0      TMA producer: 128x64 A box + BNx64 W box per stage, 128-byte
 //               swizzle, a ring of STAGES shared-memory buffers (deeper for
 //               narrower tiles);
@@ -53,10 +53,11 @@ struct GemmCfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int STAGES = BN == 256 ? 4 : (BN == 192 ? 5 : (BN == 128 ? 6 : 8));
   static constexpr int NUM_BARS = 2 * STAGES + 7;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
-  static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators (128, 256 or 512: powers of two)
+  // two accumulators of BN columns, in a power-of-two allocation (128, 256 or 512)
+  static constexpr uint32_t TMEM_COLS = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
 };
 
 struct GemmArgs {
