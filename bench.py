@@ -559,6 +559,16 @@ def bench_moe(lb, torch, dev, stream, args, B=1, S=8192):
     per_forward = (lb.llama_kernel_launch_count() - n0) // steps
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
+    # per-step breakdown (events around each step's kernels, plain launches)
+    lb.check(lb.llama_block_profile_enable(blk, 3))
+    for _ in range(3):
+        lb.check(lb.llama_block_forward(blk, x, y, B, S, 0, kv, stream))
+    torch.cuda.synchronize()
+    _, launches, total_ms = lb.llama_block_profile_read(blk)
+    lb.llama_block_profile_disable(blk)
+    names = {5: "routing_dispatch", 6: "experts_gate_up_and_shared_gate_up", 7: "experts_down_shared_down_combine"}
+    step_ms = {names.get(i, lb.llama_profile_step_name(i)): total_ms[i] / max(launches[i], 1)
+               for i in range(len(launches)) if launches[i] > 0}
     ids = torch.empty((B * S, k), dtype=torch.int32, device=dev)
     wts = torch.empty((B * S, k), dtype=torch.float32, device=dev)
     lb.check(lb.llama_block_moe_routing(blk, ids, wts, stream))
@@ -571,7 +581,7 @@ def bench_moe(lb, torch, dev, stream, args, B=1, S=8192):
     att = 4.0 * D * H * (S * (S + 1) / 2) * B
     return {"workload": "llama4_scout_shaped_moe_block_prefill_b1s8192_e16_top1_shared",
             "ms_per_step": ms, "tokens_per_s": T / (ms / 1e3), "tflops": (lin + att) / (ms / 1e3) / 1e12,
-            "rows_per_expert": load, "steps": steps, "kernels_per_step": per_forward,
+            "rows_per_expert": load, "steps": steps, "kernels_per_step": per_forward, "step_ms": step_ms,
             "gpu_launches": per_forward * steps, "device_status": status}
 
 

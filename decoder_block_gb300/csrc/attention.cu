@@ -5,8 +5,8 @@
 // Prefill kernel (one CTA per (sequence b, KV head g, block of 2*Mq query
 // positions), 320 threads):
 //   * A 128-row query tile packs the r = H/G query heads of group g: row
-//     hh*Mq + i is head g*r + hh at position q0 + i (Mq = 128 / r rounded to a
-//     power of two).  Each K/V tile that lands in shared memory therefore
+//     hh*Mq + i is head g*r + hh at position q0 + i (Mq = 128 / r rounded down
+//     to a multiple of 8; rows past r*Mq are zero).  Each K/V tile that lands in shared memory therefore
 //     serves every query head of its group; the CTA holds two such tiles
 //     (t = 0, 1: consecutive position blocks) that ping-pong.
 //   * warp 0: TMA producer -- Q tiles once, then 128-key K and V tiles into a
@@ -442,9 +442,10 @@ cudaError_t launch_prefill(const bf16 *q, const bf16 *kc, const bf16 *vc, bf16 *
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int r = H / G;
-  int rp = 1;
-  while (rp < r) rp *= 2;
-  const int Mq = 128 / rp;
+  // positions per query tile: as many as the r heads fill of its 128 rows, a
+  // multiple of 8 so that every head's Q box starts on a 1024-byte swizzle atom
+  // (r = 3: 40 positions, 120 rows; r = 5: 24 positions, 120 rows)
+  const int Mq = (128 / r) & ~7;
   const int kv_len = start_pos + S;
   CUtensorMap mq, mk, mv;
   const uint64_t qd[4] = {(uint64_t)D, (uint64_t)H, (uint64_t)S, (uint64_t)B};

@@ -152,6 +152,11 @@ ATTN_CASES = [
     (3, 45, 7, 9, 3, 64, "bf16"),     # SmolLM2 grouping (n_rep 3), cache prefix
     (1, 200, 0, 8, 2, 128, "bf16"),   # n_rep 4, several key tiles
     (2, 130, 60, 4, 2, 128, "bf16"),  # prefix + ragged
+    (2, 70, 5, 10, 2, 128, "bf16"),   # n_rep 5: 24 positions x 5 heads per 128-row query tile
+    (1, 300, 0, 40, 8, 128, "bf16"),  # Llama-4-Scout grouping (n_rep 5), several key tiles
+    (1, 50, 0, 12, 2, 64, "bf16"),    # n_rep 6: 16 positions per tile, 32 rows left zero
+    (1, 90, 11, 14, 2, 128, "bf16"),  # n_rep 7: 16 positions, 112 live rows, cache prefix
+    (2, 100, 3, 6, 2, 64, "bf16"),    # n_rep 3: 40 positions per tile (120 rows)
     (5, 1, 300, 8, 2, 128, "bf16"),   # decode step, S = 1, two key chunks
     (3, 1, 77, 9, 3, 64, "bf16"),     # decode, one chunk, n_rep 3
     (2, 1, 1000, 32, 8, 128, "bf16"), # decode, ragged last chunk
