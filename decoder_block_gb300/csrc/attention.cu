@@ -14,9 +14,10 @@
 //     the valid cache read as zeros.
 //   * warp 1: tcgen05.mma issuer -- S_t = Q_t K^T (fp32 in TMEM), then
 //     O_t += P_t V with P_t read from TMEM and V as an MN-major smem operand.
-//   * warps 2-5 / 6-9: softmax of tile 0 / 1, one thread per row: load the
-//     S row from TMEM, causal mask j <= start_pos + position, running max
-//     (rescaling O in TMEM only when the max grows by more than 2^8),
+//   * warps 2-5 / 6-9: softmax of tile 0 / 1, one thread per row, one pass
+//     over each S row in TMEM: causal mask j <= start_pos + position, running
+//     max (rescaling only when it grows by more than 2^8; the max of each
+//     32-column chunk comes from the TMEM load's own reduction),
 //     p = 2^(s*log2e/sqrt(D) - m) on the MUFU unit, P written back to TMEM as
 //     bf16 over its own S columns; finally O / l stored as bf16.
 // Every wait is bounded; on expiry the kernel records a status code, drains,
@@ -276,77 +277,62 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         break;
       }
       ptx::tc_fence_after();
-      // Pass 1: row max over the tile, 32 columns at a time (causal predicate only
-      // on tiles that reach past some row's position).
+      // One pass over the tile, 32 columns at a time.  p = 2^(s*scale - m_run)
+      // uses the running maximum as it stands; a chunk whose own maximum exceeds
+      // it by more than 2^8 first raises it (the rescale), scaling the row sum,
+      // the P chunks already written for this tile and, once the tile is done,
+      // O.  The chunk maximum comes from the TMEM load itself; the causal
+      // predicate applies only on tiles that reach past some row's position.
+      // The P chunk of columns [c, c+32) lands in TMEM columns [c/2, c/2 + 16),
+      // which hold S values already read (columns < c + 32).
       const int key0 = j * KV_TILE;
       const bool masked = __any_sync(0xffffffffu, key0 + KV_TILE - 1 > pos);
-      float mx = -INFINITY;
-      if (masked) {
-#pragma unroll
-        for (int c = 0; c < KV_TILE; c += 32) {
-          float sv[32];
-          ptx::tmem_ld32(s_col + c, sv);
-#pragma unroll
-          for (int k = 0; k < 32; ++k) mx = fmaxf(mx, key0 + c + k > pos ? -INFINITY : sv[k]);
-        }
-      } else {
-        // four independent running maxima: the chain of dependent max operations is 4x shorter
-        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int c = 0; c < KV_TILE; c += 32) {
-          float sv[32];
-          ptx::tmem_ld32(s_col + c, sv);
-#pragma unroll
-          for (int k = 0; k < 32; k += 8) {
-            mq[0] = ptx::max3(mq[0], sv[k], sv[k + 1]);
-            mq[1] = ptx::max3(mq[1], sv[k + 2], sv[k + 3]);
-            mq[2] = ptx::max3(mq[2], sv[k + 4], sv[k + 5]);
-            mq[3] = ptx::max3(mq[3], sv[k + 6], sv[k + 7]);
-          }
-        }
-        mx = fmaxf(ptx::max3(mq[0], mq[1], mq[2]), mq[3]);
-      }
-      const float m_tile = mx * a.scale_log2;
-      const bool need = m_tile > m_run + RESCALE_THRESHOLD;
-      float alpha = 1.f;
-      if (need) {
-        alpha = ptx::ex2_approx(m_run - m_tile);
-        m_run = m_tile;
-      }
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        ok = ptx::mbar_wait(o_done(t), (j - 1) & 1, abort_flag, a.status, DEV_TIMEOUT_ATTN);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D; c += 16) {
-          float ov[16];
-          ptx::tmem_ld16(o_col + c, ov);
-          ptx::tmem_ld_wait();
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(ov[e] * alpha);
-          ptx::tmem_st16(o_col + c, w);
-        }
-      }
-      l2 = ptx::fmul2(l2, ptx::f2pack(alpha, alpha));
-      const uint64_t negm2 = ptx::f2pack(-m_run, -m_run);
-      // Pass 2: p = 2^(s*scale - m), written back as bf16 pairs.  The P chunk of
-      // columns [c, c+32) lands in TMEM columns [c/2, c/2 + 16), which only hold S
-      // values already read (columns < c + 32).
-      // p = 2^(s*scale - m) written back as bf16 pairs; the P chunk of columns
-      // [c, c+32) lands in TMEM columns [c/2, c/2 + 16): only S values already read.
+      float alpha_tile = 1.f;
+      bool rescaled = false;  // warp-uniform
 #pragma unroll
       for (int c = 0; c < KV_TILE; c += 32) {
         float sv[32];
-        ptx::tmem_ld32(s_col + c, sv);
+        float cm;
         if (masked) {
+          ptx::tmem_ld32(s_col + c, sv);
+          cm = -INFINITY;
 #pragma unroll
-          for (int k = 0; k < 32; ++k)
+          for (int k = 0; k < 32; ++k) {
             if (key0 + c + k > pos) sv[k] = -INFINITY;
+            cm = fmaxf(cm, sv[k]);
+          }
+        } else {
+          ptx::tmem_ld32_max(s_col + c, sv, cm);
         }
+        const float cms = cm * a.scale_log2;
+        const bool need = cms > m_run + RESCALE_THRESHOLD;
+        if (__any_sync(0xffffffffu, need)) {
+          float alpha = 1.f;
+          if (need) {
+            alpha = ptx::ex2_approx(m_run - cms);
+            m_run = cms;
+          }
+          l2 = ptx::fmul2(l2, ptx::f2pack(alpha, alpha));
+          alpha_tile *= alpha;
+          rescaled = true;
+          if (c > 0) {
+            // this tile's P columns written so far were scaled by the old maximum
+            ptx::tmem_st_wait();
+#pragma unroll 1
+            for (int pc = 0; pc < c / 2; pc += 16) {
+              float pv[16];
+              ptx::tmem_ld16(s_col + pc, pv);
+              uint32_t w[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const uint32_t u = __float_as_uint(pv[e]);
+                w[e] = pack2(__uint_as_float(u << 16) * alpha, __uint_as_float(u & 0xffff0000u) * alpha);
+              }
+              ptx::tmem_st16(s_col + pc, w);
+            }
+          }
+        }
+        const uint64_t negm2 = ptx::f2pack(-m_run, -m_run);
         uint32_t pk[16];
         uint64_t lc = ptx::f2pack(0.f, 0.f);  // this chunk's sum: a second, independent add chain
 #pragma unroll
@@ -367,6 +353,25 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
         l2 = ptx::fadd2(l2, lc);
         ptx::tmem_st16(s_col + c / 2, pk);
+      }
+      if (j > 0 && rescaled) {
+        // O holds the sum over earlier key tiles: wait for the last PV product
+        // into it, then scale it by this tile's factor
+        ok = ptx::mbar_wait(o_done(t), (j - 1) & 1, abort_flag, a.status, DEV_TIMEOUT_ATTN);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D; c += 16) {
+          float ov[16];
+          ptx::tmem_ld16(o_col + c, ov);
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(ov[e] * alpha_tile);
+          ptx::tmem_st16(o_col + c, w);
+        }
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();

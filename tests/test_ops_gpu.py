@@ -189,3 +189,35 @@ def test_attention(lb, B, S, start_pos, H, G, D, dtype):
     lb.check(lb.llama_op_attention(dt, qd, lb.make_kv_cache(kd, vd, B, L), o, B, S, start_pos, H, G, D, ws, nws))
     t.cuda.synchronize()
     assert_parity(to_f64(o), ref, dtype, f"attention B={B} S={S} sp={start_pos} H={H} G={G} D={D}")
+
+
+# Keys whose scale grows with their position, (1 + p/8): each 32-key chunk's
+# largest score tends to exceed the running maximum by more than 2^8 (in
+# log2 units), so the online softmax raises its maximum inside a key tile and
+# rescales the probabilities already written for that tile, the row sum and O.
+GROWING_CASES = [
+    # B, S, start_pos, H, G, D
+    (1, 200, 0, 8, 2, 128),
+    (2, 130, 60, 4, 2, 128),
+    (1, 90, 11, 14, 2, 128),
+    (3, 45, 7, 9, 3, 64),
+]
+
+
+@pytest.mark.parametrize("B,S,start_pos,H,G,D", GROWING_CASES)
+def test_attention_growing_scores(lb, B, S, start_pos, H, G, D):
+    t = torch()
+    L = start_pos + S + 5
+    ramp = (1.0 + np.arange(L, dtype=np.float32) / 8.0)[None, None, :, None]
+    q = synth.f32_to_bf16_bits(synth.normal(0, "ops/gq", (B, S, H, D)))
+    kc = synth.f32_to_bf16_bits(synth.normal(0, "ops/gk", (B, G, L, D)) * ramp)
+    vc = synth.f32_to_bf16_bits(synth.normal(0, "ops/gv", (B, G, L, D)))
+    ref = oracle.gqa_attention(synth.as_f64(q), synth.as_f64(kc), synth.as_f64(vc), start_pos)
+    qd, kd, vd = to_dev(q), to_dev(kc), to_dev(vc)
+    o = t.empty_like(qd)
+    nws = lb.llama_op_attention_workspace_bytes(lb.LLAMA_BF16, B, S, start_pos, H, D)
+    ws = t.empty(max(nws, 16), dtype=t.uint8, device="cuda")
+    lb.check(lb.llama_op_attention(lb.LLAMA_BF16, qd, lb.make_kv_cache(kd, vd, B, L), o, B, S, start_pos, H, G, D,
+                                   ws, nws))
+    t.cuda.synchronize()
+    assert_parity(to_f64(o), ref, "bf16", f"attention, growing keys, B={B} S={S} sp={start_pos} H={H} G={G} D={D}")
