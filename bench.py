@@ -36,6 +36,7 @@ METRIC = "decoder-block tokens/s (prefill) & decode µs/step; % of bf16 TC / HBM
 WORKLOAD = "llama3_8b_block_prefill_b1s8192"
 SHAPE = dict(d_model=4096, n_heads=32, n_kv_heads=8, d_ff=14336, norm_eps=1e-5, rope_theta=5e5, dtype="bf16",
              B=1, S=8192, start_pos=0, max_seq_len=8192)
+SMOLLM2_SHAPE = dict(d_model=576, n_heads=9, n_kv_heads=3, d_ff=1536, norm_eps=1e-5, rope_theta=1e5, B=8, S=1024)
 DECODE = dict(SHAPE, B=64, S=1, start_pos=4095, max_seq_len=4096)
 
 
@@ -243,6 +244,8 @@ def main():
     ap.add_argument("--no-stack", action="store_true", help="skip the 32-layer stack measurement")
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the decode step (B=64 at start_pos 4095); for profiler captures")
+    ap.add_argument("--smollm2-only", action="store_true",
+                    help="time only the SmolLM2-shaped block (B=8, S=1024, d_model 576); for profiler captures")
     ap.add_argument("--seq", type=int, default=8192,
                     help="prefill length S (default 8192; smaller values are for profiler captures)")
     args = ap.parse_args()
@@ -268,6 +271,14 @@ def main():
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
 
+    if args.smollm2_only:
+        sm = bench_block_shape(lb, torch, dev, stream, SMOLLM2_SHAPE, args)
+        if rank == 0:
+            print(json.dumps({"metric": "SmolLM2-shaped block tokens/s", "value": sm["tokens_per_s"], "unit": "tokens/s",
+                              "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                              "dtype": "bf16", "data": "synthetic",
+                              "config": {"workload": "smollm2_135m_block_b8s1024"}, "smollm2": sm}), flush=True)
+        return 0
     # ---- inputs (seeded synthetic, the same recipe as the parity tests) ----
     w_np = synth.block_weights(SHAPE)
     w = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(dev) for k, v in w_np.items()}
@@ -401,9 +412,7 @@ def main():
 
     secondary = {}
     if not args.no_secondary:
-        secondary["smollm2_135m_block_b8s1024"] = bench_block_shape(
-            lb, torch, dev, stream, dict(d_model=576, n_heads=9, n_kv_heads=3, d_ff=1536, norm_eps=1e-5,
-                                         rope_theta=1e5, B=8, S=1024), args)
+        secondary["smollm2_135m_block_b8s1024"] = bench_block_shape(lb, torch, dev, stream, SMOLLM2_SHAPE, args)
         secondary["llama3_8b_block_prefill_b4s2048"] = bench_block_shape(
             lb, torch, dev, stream, dict(SHAPE, B=4, S=2048), args, weights=w)
         secondary["llama4_scout_shaped_moe_block"] = bench_moe(lb, torch, dev, stream, args)
