@@ -189,7 +189,9 @@ __device__ __forceinline__ float epilogue_chunk16(const float *v, const GemmArgs
 // Returns the row's sum-of-squares contribution (EPI_RESIDUAL_SQSUM), else 0.
 // EPI_QKV_ROPE: 32 consecutive columns of one head (D % 32 == 0), already row
 // scaled.  Interleaved pairs (2i, 2i+1) sit in adjacent registers.
-__device__ __forceinline__ void qkv_rope_chunk32(const float (&v)[32], const GemmArgs &a, int m, int n) {
+// cs: the chunk's 16 (cos, sin) pairs from load_rope32.
+__device__ __forceinline__ void qkv_rope_chunk32(const float (&v)[32], const GemmArgs &a, int m, int n,
+                                                 const float4 (&cs)[8]) {
   const QkvScatter &r = a.qkv;
   if (m >= a.M || n >= a.N) return;
   const int head = n / r.D, e = n % r.D;
@@ -197,13 +199,12 @@ __device__ __forceinline__ void qkv_rope_chunk32(const float (&v)[32], const Gem
   uint32_t w[16];
   if (head < r.H + r.G) {
     // "The Evolving Transformer 04 · LLaMA", §02 RoPE: (a cos - b sin, a sin + b cos)
-    const float4 *cs = reinterpret_cast<const float4 *>(r.table + (size_t)p * (r.D / 2) + e / 2);
     if (r.halves) {
       // pairs (i, i + D/2), i = e/2 .. e/2 + 15: first members to i, second to i + D/2
       uint32_t lo[8], hi[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const float4 c = __ldg(cs + k);
+        const float4 c = cs[k];
         const float a0 = v[4 * k], b0 = v[4 * k + 1], a1 = v[4 * k + 2], b1 = v[4 * k + 3];
         lo[k] = pack_bf16(a0 * c.x - b0 * c.y, a1 * c.z - b1 * c.w);
         hi[k] = pack_bf16(a0 * c.y + b0 * c.x, a1 * c.w + b1 * c.z);
@@ -220,7 +221,7 @@ __device__ __forceinline__ void qkv_rope_chunk32(const float (&v)[32], const Gem
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const float4 c = __ldg(cs + k);  // {cos_i, sin_i, cos_i+1, sin_i+1}
+      const float4 c = cs[k];  // {cos_i, sin_i, cos_i+1, sin_i+1}
       const float a0 = v[4 * k], b0 = v[4 * k + 1], a1 = v[4 * k + 2], b1 = v[4 * k + 3];
       w[2 * k] = pack_bf16(a0 * c.x - b0 * c.y, a0 * c.y + b0 * c.x);
       w[2 * k + 1] = pack_bf16(a1 * c.z - b1 * c.w, a1 * c.w + b1 * c.z);
@@ -243,14 +244,42 @@ __device__ __forceinline__ void qkv_rope_chunk32(const float (&v)[32], const Gem
 }
 
 template <int EPI>
-__device__ __forceinline__ float epilogue_chunk32(float (&v)[32], const GemmArgs &a, int m, int n,
-                                                  const uint4 *res = nullptr) {
-  if constexpr (EPI == EPI_STORE_ROWSCALE || EPI == EPI_SWIGLU_ROWSCALE || EPI == EPI_QKV_ROPE ||
-                EPI == EPI_F32OUT_ROWSCALE) {
-    // RMSNorm of A's row m, applied to the GEMM result (the gain is folded into W)
-    const float r = m < a.M ? rsqrtf(a.ss_in[m] * a.inv_d + a.eps) : 0.f;
+constexpr bool epi_row_scaled() {
+  return EPI == EPI_STORE_ROWSCALE || EPI == EPI_SWIGLU_ROWSCALE || EPI == EPI_QKV_ROPE || EPI == EPI_F32OUT_ROWSCALE;
+}
+
+// RMSNorm of A's row m, applied to the GEMM result by the row-scaled epilogues
+// (the gain is folded into W): rsqrt(mean of squares + eps); 1 for the others.
+// Loaded once per row, before the accumulator is ready.
+template <int EPI>
+__device__ __forceinline__ float row_scale(const GemmArgs &a, int m) {
+  if constexpr (epi_row_scaled<EPI>()) return m < a.M ? rsqrtf(a.ss_in[m] * a.inv_d + a.eps) : 0.f;
+  return 1.f;
+}
+
+// The (cos, sin) pairs of QKV columns n .. n+31 at row m's position, loaded ahead
+// of their epilogue chunk (EPI_QKV_ROPE only; value heads and dead rows load nothing).
+template <int EPI>
+__device__ __forceinline__ void load_rope32(const GemmArgs &a, int m, int n, float4 (&cs)[8]) {
+  if constexpr (EPI == EPI_QKV_ROPE) {
+    const QkvScatter &r = a.qkv;
+    if (m < a.M && n < a.N && n / r.D < r.H + r.G) {
+      const float4 *p = reinterpret_cast<const float4 *>(r.table + (size_t)(r.start_pos + m % r.S) * (r.D / 2) +
+                                                         (n % r.D) / 2);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] *= r;
+      for (int k = 0; k < 8; ++k) cs[k] = __ldg(p + k);
+    }
+  }
+}
+
+// rs: row_scale of row m; res: the chunk's residual from load_residual32 (or null);
+// cs: the chunk's rotation pairs from load_rope32 (EPI_QKV_ROPE).
+template <int EPI>
+__device__ __forceinline__ float epilogue_chunk32(float (&v)[32], const GemmArgs &a, int m, int n, float rs,
+                                                  const uint4 *res, const float4 (&cs)[8]) {
+  if constexpr (epi_row_scaled<EPI>()) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= rs;
   }
   if constexpr (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_ROWSCALE) {
     const int nout = a.N / 2;
@@ -266,7 +295,7 @@ __device__ __forceinline__ float epilogue_chunk32(float (&v)[32], const GemmArgs
     }
     return 0.f;
   } else if constexpr (EPI == EPI_QKV_ROPE) {
-    qkv_rope_chunk32(v, a, m, n);
+    qkv_rope_chunk32(v, a, m, n, cs);
     return 0.f;
   } else if constexpr (EPI == EPI_F32OUT_ROWSCALE) {
     epilogue_chunk16<EPI_F32OUT>(v, a, m, n);
@@ -345,22 +374,28 @@ __device__ __forceinline__ float splitk_finish(const GemmArgs &args, int tile, i
   float sq = 0.f;
   float v[32], nx[32];
   uint4 rc[4], rn[4];  // residual of the current / next chunk (residual epilogues)
+  float4 cs[8], csn[8];  // rotation pairs of the current / next chunk (EPI_QKV_ROPE)
   bool vc = false, vn = false;
+  const float rs = row_scale<EPI>(args, mm);
   load_sums(c_begin, v);
   clear_sums(c_begin);
   if (kRes) load_residual32(args, mm, nt * BN + c_begin, rc, vc);
+  load_rope32<EPI>(args, mm, nt * BN + c_begin, cs);
 #pragma unroll 1
   for (int c = c_begin; c < c_end; c += 32) {
     if (c + 32 < c_end) {
       load_sums(c + 32, nx);
       clear_sums(c + 32);
       if (kRes) load_residual32(args, mm, nt * BN + c + 32, rn, vn);
+      load_rope32<EPI>(args, mm, nt * BN + c + 32, csn);
     }
-    sq += epilogue_chunk32<EPI>(v, args, mm, nt * BN + c, vc ? rc : nullptr);
+    sq += epilogue_chunk32<EPI>(v, args, mm, nt * BN + c, rs, vc ? rc : nullptr, cs);
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = nx[i];
 #pragma unroll
     for (int i = 0; i < 4; ++i) rc[i] = rn[i];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cs[i] = csn[i];
     vc = vn;
   }
   return sq;
@@ -586,37 +621,48 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
       unit_coords(u, a_row, w_row, m_end, nt, k0, k1, slot);
       const int acc = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
+      // rows past the tile's valid range (the next group's rows, or past M) are
+      // passed as row M, which every epilogue skips
+      const int m = a_row + row < m_end ? a_row + row : args.M;
+      // A whole tile's row scale and its first chunk's residual and rotation pairs
+      // are loaded while its MMAs run: with a short K loop the epilogue is the
+      // critical path, and each of these loads would otherwise stall a chunk.
+      constexpr bool kRes = EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_SQSUM;
+      float rs = 1.f;
+      uint4 rc[4];
+      float4 cs[8];
+      bool vc = false;
+      if (slot < 0) {
+        rs = row_scale<EPI>(args, m);
+        if (kRes) load_residual32(args, m, nt * BN, rc, vc);
+        load_rope32<EPI>(args, m, nt * BN, cs);
+      }
       bool ok = ptx::mbar_wait(tfull_bar(acc), aph, abort_flag, args.status, DEV_TIMEOUT_EPILOGUE);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
       const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      // rows past the tile's valid range (the next group's rows, or past M) are
-      // passed as row M, which every epilogue skips
-      const int m = a_row + row < m_end ? a_row + row : args.M;
       if (slot < 0) {
+        // the next chunk's residual and rotation pairs load while this chunk is finished
         float sq = 0.f;
-        if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_SQSUM) {
-          // the next chunk's residual is loaded while this chunk is finished
-          uint4 rc[4], rn[4];
-          bool vc, vn = false;
-          load_residual32(args, m, nt * BN, rc, vc);
+        uint4 rn[4];
+        float4 csn[8];
+        bool vn = false;
 #pragma unroll 1
-          for (int c = 0; c < BN; c += 32) {
-            if (c + 32 < BN) load_residual32(args, m, nt * BN + c + 32, rn, vn);
-            float v[32];
-            ptx::tmem_ld32(trow + c, v);
-            sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + c, vc ? rc : nullptr);
+        for (int c = 0; c < BN; c += 32) {
+          if (c + 32 < BN) {
+            if (kRes) load_residual32(args, m, nt * BN + c + 32, rn, vn);
+            load_rope32<EPI>(args, m, nt * BN + c + 32, csn);
+          }
+          float v[32];
+          ptx::tmem_ld32(trow + c, v);
+          sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + c, rs, vc ? rc : nullptr, cs);
+          if (kRes) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) rc[i] = rn[i];
             vc = vn;
           }
-        } else {
-#pragma unroll 1
-          for (int c = 0; c < BN; c += 32) {
-            float v[32];
-            ptx::tmem_ld32(trow + c, v);
-            sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + c);
-          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) cs[i] = csn[i];
         }
         ptx::tc_fence_before();
         ptx::mbar_arrive(tempty_bar(acc));
@@ -733,7 +779,10 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
       const int m = a_row + r < args.M ? a_row + r : args.M;
       const uint32_t rank = ptx::cluster_ctarank();
       float sq = 0.f;
+      const float rs = row_scale<EPI>(args, m);
       for (int ch = (int)rank; ch < BN / 32 && m < args.M; ch += args.splits) {
+        float4 cs[8];  // issued ahead of the piece loads
+        load_rope32<EPI>(args, m, nt * BN + ch * 32, cs);
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0.f;
@@ -748,7 +797,7 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
             v[4 * i + 3] += p4.w;
           }
         }
-        sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + ch * 32);
+        sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + ch * 32, rs, nullptr, cs);
       }
       if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
         if (m < args.M) atomicAdd(args.ss_out + m, sq);
