@@ -2,8 +2,10 @@
 // ("The Evolving Transformer 04 · LLaMA", §05 GQA; "Full Llama 3 transformer
 // block", How it works: cache read with the start_pos offset mask).
 //
-// Prefill kernel (one CTA per (sequence b, KV head g, block of 2*Mq query
-// positions), 320 threads):
+// Prefill kernel (persistent, at most one CTA per SM, 320 threads; each CTA
+// loops over work items (sequence b, KV head g, block of 2*Mq query positions)
+// and the next item's Q, first K tile and first S products overlap the current
+// item's last PV products and output):
 //   * A 128-row query tile packs the r = H/G query heads of group g: row
 //     hh*Mq + i is head g*r + hh at position q0 + i (Mq = 128 / r rounded down
 //     to a multiple of 8; rows past r*Mq are zero).  Each K/V tile that lands in shared memory therefore
@@ -55,8 +57,8 @@ struct AttnLayout {
   static constexpr int OFF_K = 2 * Q_TILE;
   static constexpr int OFF_V = OFF_K + KV_STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + KV_STAGES * KV_BYTES;
-  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done[2], fin
-  static constexpr int NBAR = 1 + 4 * KV_STAGES + 6 + 1;
+  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done[2], fin, q_empty
+  static constexpr int NBAR = 1 + 4 * KV_STAGES + 6 + 1 + 1;
   // At least 116 KB so that a second CTA never shares the SM (both would need all 512 TMEM columns).
   static constexpr int BYTES_MIN = 1024 + OFF_BAR + NBAR * 8 + 16;
   static constexpr int BYTES = BYTES_MIN > 116 * 1024 ? BYTES_MIN : 116 * 1024;
@@ -97,15 +99,35 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   auto p_full = [&](int t) { return bar0 + 8u * (3 + 4 * KV_STAGES + t); };
   auto o_done = [&](int t) { return bar0 + 8u * (5 + 4 * KV_STAGES + t); };
   const uint32_t fin = bar0 + 8u * (7 + 4 * KV_STAGES);
+  const uint32_t q_empty = bar0 + 8u * (8 + 4 * KV_STAGES);  // the MMAs reading an item's Q are done
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Persistent CTAs: the CTA takes the items (b, g, block of 2*Mq positions)
+  // blockIdx.x, then one per round in snake order over the grid (rounds
+  // alternate direction), longest query blocks first, so that the CTAs' sums of
+  // key tiles even out.  Barrier phases run on across items: a role's counters
+  // (items started, key tiles issued) give every wait its parity.
   const int bg_count = a.B * a.G;
-  const int qb = a.nqb - 1 - (int)(blockIdx.x / bg_count);  // longest query blocks first
-  const int bg = (int)(blockIdx.x % bg_count);
-  const int b = bg / a.G, g = bg % a.G;
-  const int q0 = qb * 2 * a.Mq;
-  const int kv_need = min(a.start_pos + q0 + 2 * a.Mq, a.kv_len);
-  const int n_kv = (kv_need + KV_TILE - 1) / KV_TILE;
+  const int n_items = a.nqb * bg_count;
+  auto item_of = [&](int k) -> int {  // the CTA's k-th item, -1 past the last
+    const int gsz = (int)gridDim.x;
+    const int u = k * gsz + ((k & 1) ? gsz - 1 - (int)blockIdx.x : (int)blockIdx.x);
+    return u < n_items ? u : -1;
+  };
+  struct Item {
+    int b, g, q0, n_kv;
+  };
+  auto decode_item = [&](int u) {
+    Item it;
+    const int qb = a.nqb - 1 - u / bg_count;
+    const int bg = u % bg_count;
+    it.b = bg / a.G;
+    it.g = bg % a.G;
+    it.q0 = qb * 2 * a.Mq;
+    const int kv_need = min(a.start_pos + it.q0 + 2 * a.Mq, a.kv_len);
+    it.n_kv = (kv_need + KV_TILE - 1) / KV_TILE;
+    return it;
+  };
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
@@ -121,6 +143,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       ptx::mbar_init(o_done(t), 1);
     }
     ptx::mbar_init(fin, 1);
+    ptx::mbar_init(q_empty, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -153,34 +176,50 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       ptx::tma_prefetch_desc(&tmK);
       ptx::tma_prefetch_desc(&tmV);
       const uint32_t qbytes = 2u * a.r * (D / 64) * a.Mq * 128u;
-      ptx::mbar_arrive_expect_tx(q_full, qbytes);
-      for (int t = 0; t < 2; ++t)
-        for (int hh = 0; hh < a.r; ++hh)
+      int items = 0;   // Q loads issued
+      int issued = 0;  // K and V loads issued over all items: 2 per key tile
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int u = item_of(k);
+        if (u < 0) break;
+        const Item it = decode_item(u);
+        // the previous item's Q stays until its last S product is done
+        if (k > 0 && !ptx::mbar_wait(q_empty, (k - 1) & 1, abort_flag, a.status, DEV_TIMEOUT_PRODUCER)) break;
+        ptx::mbar_arrive_expect_tx(q_full, qbytes);
+        for (int t = 0; t < 2; ++t)
+          for (int hh = 0; hh < a.r; ++hh)
+            for (int at = 0; at < D / 64; ++at)
+              ptx::tma_load_4d(s0 + L::OFF_Q + t * L::Q_TILE + at * L::ATOM + hh * a.Mq * 128, &tmQ, at * 64,
+                               it.g * a.r + hh, it.q0 + t * a.Mq, it.b, q_full);
+        ++items;
+        for (int j = 0; j < it.n_kv; ++j) {
+          const int jj = issued / 2;  // key tile index over all items
+          const int st = jj % KV_STAGES;
+          const uint32_t ph = (jj / KV_STAGES) & 1;
+          if (!ptx::mbar_wait(k_empty(st), ph ^ 1, abort_flag, a.status, DEV_TIMEOUT_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(k_full(st), L::KV_BYTES);
           for (int at = 0; at < D / 64; ++at)
-            ptx::tma_load_4d(s0 + L::OFF_Q + t * L::Q_TILE + at * L::ATOM + hh * a.Mq * 128, &tmQ, at * 64,
-                             g * a.r + hh, q0 + t * a.Mq, b, q_full);
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % KV_STAGES;
-        const uint32_t ph = (j / KV_STAGES) & 1;
-        if (!ptx::mbar_wait(k_empty(st), ph ^ 1, abort_flag, a.status, DEV_TIMEOUT_PRODUCER)) break;
-        ptx::mbar_arrive_expect_tx(k_full(st), L::KV_BYTES);
-        for (int at = 0; at < D / 64; ++at)
-          ptx::tma_load_4d(s0 + L::OFF_K + st * L::KV_BYTES + at * L::ATOM, &tmK, at * 64, j * KV_TILE, g, b,
-                           k_full(st));
-        if (!ptx::mbar_wait(v_empty(st), ph ^ 1, abort_flag, a.status, DEV_TIMEOUT_PRODUCER)) {
-          issued = 2 * j + 1;
-          break;
+            ptx::tma_load_4d(s0 + L::OFF_K + st * L::KV_BYTES + at * L::ATOM, &tmK, at * 64, j * KV_TILE, it.g,
+                             it.b, k_full(st));
+          ++issued;
+          if (!ptx::mbar_wait(v_empty(st), ph ^ 1, abort_flag, a.status, DEV_TIMEOUT_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(v_full(st), L::KV_BYTES);
+          for (int at = 0; at < D / 64; ++at)
+            ptx::tma_load_4d(s0 + L::OFF_V + st * L::KV_BYTES + at * L::ATOM, &tmV, at * 64, j * KV_TILE, it.g,
+                             it.b, v_full(st));
+          ++issued;
         }
-        ptx::mbar_arrive_expect_tx(v_full(st), L::KV_BYTES);
-        for (int at = 0; at < D / 64; ++at)
-          ptx::tma_load_4d(s0 + L::OFF_V + st * L::KV_BYTES + at * L::ATOM, &tmV, at * 64, j * KV_TILE, g, b,
-                           v_full(st));
-        issued = 2 * j + 2;
       }
-      // Drain: every issued copy must land before the CTA exits.
+      // Drain: every issued copy must land before the CTA exits (at most one Q
+      // load and the ring's last KV_STAGES key tiles can be outstanding).
       int dummy = 0;
-      ptx::mbar_wait(q_full, 0, &dummy, a.status, DEV_TIMEOUT_PRODUCER);
+      if (items > 0) ptx::mbar_wait(q_full, (items - 1) & 1, &dummy, a.status, DEV_TIMEOUT_PRODUCER);
       for (int j = max(0, issued / 2 - KV_STAGES); j < (issued + 1) / 2; ++j) {
         const int st = j % KV_STAGES;
         const uint32_t ph = (j / KV_STAGES) & 1;
@@ -192,8 +231,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, KV_TILE, false);
       constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, true);
-      bool ok = ptx::mbar_wait(q_full, 0, abort_flag, a.status, DEV_TIMEOUT_MMA);
-      // S_t(j) = Q_t K(j)^T into TMEM columns t*128 (P_t later overwrites them as bf16).
+      // S_t(j) = Q_t K(j)^T into TMEM columns t*128 (P_t later overwrites them as bf16);
+      // j counts key tiles over all items (it picks the ring stage).
       auto issue_s = [&](int j, int t) {
         const uint32_t kb = s0 + L::OFF_K + (j % KV_STAGES) * L::KV_BYTES;
         const uint32_t qbase = s0 + L::OFF_Q + t * L::Q_TILE;
@@ -205,50 +244,66 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
         ptx::mma_commit(s_full(t));
       };
-      // O_t += P_t(j) V(j), P_t read from TMEM, V as an MN-major operand.
-      auto issue_pv = [&](int j, int t) {
+      // O_t += P_t(j) V(j), P_t read from TMEM, V as an MN-major operand; the item's
+      // first key tile (first = true) overwrites O.
+      auto issue_pv = [&](int j, bool first, int t) {
         const uint32_t vb = s0 + L::OFF_V + (j % KV_STAGES) * L::KV_BYTES;
 #pragma unroll
         for (int kk = 0; kk < KV_TILE / 16; ++kk) {
           // 16 keys = two 8-row groups of the V tile; V rows hold 64 consecutive d values.
           const uint64_t bdesc = ptx::smem_desc_sw128_mn(vb + kk * 16 * 128, L::ATOM, 1024);
-          ptx::mma_bf16_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, bdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_bf16_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, bdesc, idesc_pv, (!first || kk > 0) ? 1u : 0u);
         }
         ptx::mma_commit(o_done(t));
       };
       // Staggered order: S_0(j+1) is issued right after PV_0(j), so the softmax of tile 0 for
       // the next key tile overlaps the softmax of tile 1 and the tensor core alternates tiles.
-      if (ok && n_kv > 0) {
-        ok = ptx::mbar_wait(k_full(0), 0, abort_flag, a.status, DEV_TIMEOUT_MMA);
-        if (ok) {
-          ptx::tc_fence_after();
-          issue_s(0, 0);
-          issue_s(0, 1);
-          ptx::mma_commit(k_empty(0));
-        }
-      }
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int st = j % KV_STAGES;
-        const uint32_t ph = (j / KV_STAGES) & 1;
-        if (!ptx::mbar_wait(v_full(st), ph, abort_flag, a.status, DEV_TIMEOUT_MMA)) break;
-        if (!ptx::mbar_wait(p_full(0), j & 1, abort_flag, a.status, DEV_TIMEOUT_MMA)) break;
+      // The next item's first S products follow the last PV products of the current one
+      // (MMAs of one thread run in issue order), so they overlap the current item's epilogue.
+      // q_empty is committed after an item's last S products.
+      bool ok = true;
+      int jg = 0;  // key tiles consumed over all items
+      for (int k = 0; ok; ++k) {
+        const int u = item_of(k);
+        if (u < 0) break;
+        const int n_kv = decode_item(u).n_kv;
+        if (!ptx::mbar_wait(q_full, k & 1, abort_flag, a.status, DEV_TIMEOUT_MMA)) break;
+        if (!ptx::mbar_wait(k_full(jg % KV_STAGES), (jg / KV_STAGES) & 1, abort_flag, a.status, DEV_TIMEOUT_MMA))
+          break;
         ptx::tc_fence_after();
-        issue_pv(j, 0);
-        const bool more = j + 1 < n_kv;
-        if (more) {
-          const int st1 = (j + 1) % KV_STAGES;
-          if (!ptx::mbar_wait(k_full(st1), ((j + 1) / KV_STAGES) & 1, abort_flag, a.status, DEV_TIMEOUT_MMA)) break;
+        issue_s(jg, 0);
+        issue_s(jg, 1);
+        ptx::mma_commit(k_empty(jg % KV_STAGES));
+        if (n_kv == 1) ptx::mma_commit(q_empty);
+        for (int j = 0; j < n_kv; ++j) {
+          const int jj = jg + j;
+          const int st = jj % KV_STAGES;
+          const uint32_t ph = (jj / KV_STAGES) & 1;
+          ok = false;
+          if (!ptx::mbar_wait(v_full(st), ph, abort_flag, a.status, DEV_TIMEOUT_MMA)) break;
+          if (!ptx::mbar_wait(p_full(0), jj & 1, abort_flag, a.status, DEV_TIMEOUT_MMA)) break;
           ptx::tc_fence_after();
-          issue_s(j + 1, 0);
+          issue_pv(jj, j == 0, 0);
+          const bool more = j + 1 < n_kv;
+          if (more) {
+            const int st1 = (jj + 1) % KV_STAGES;
+            if (!ptx::mbar_wait(k_full(st1), ((jj + 1) / KV_STAGES) & 1, abort_flag, a.status, DEV_TIMEOUT_MMA))
+              break;
+            ptx::tc_fence_after();
+            issue_s(jj + 1, 0);
+          }
+          if (!ptx::mbar_wait(p_full(1), jj & 1, abort_flag, a.status, DEV_TIMEOUT_MMA)) break;
+          ptx::tc_fence_after();
+          issue_pv(jj, j == 0, 1);
+          ptx::mma_commit(v_empty(st));
+          if (more) {
+            issue_s(jj + 1, 1);
+            ptx::mma_commit(k_empty((jj + 1) % KV_STAGES));
+            if (j + 2 == n_kv) ptx::mma_commit(q_empty);
+          }
+          ok = true;
         }
-        if (!ptx::mbar_wait(p_full(1), j & 1, abort_flag, a.status, DEV_TIMEOUT_MMA)) break;
-        ptx::tc_fence_after();
-        issue_pv(j, 1);
-        ptx::mma_commit(v_empty(st));
-        if (more) {
-          issue_s(j + 1, 1);
-          ptx::mma_commit(k_empty((j + 1) % KV_STAGES));
-        }
+        jg += n_kv;
       }
       ptx::mma_commit(fin);
       int dummy = 0;
@@ -260,146 +315,155 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const int qq = warp & 3;
     const int row = qq * 32 + lane;
     const int hh = row / a.Mq, i = row % a.Mq;
-    const int rel = q0 + t * a.Mq + i;
-    const bool valid = hh < a.r && rel < a.S;
-    const int pos = a.start_pos + rel;
     const uint32_t lane_base = tmem + ((uint32_t)(qq * 32) << 16);
     const uint32_t s_col = lane_base + t * 128;
     const uint32_t o_col = lane_base + 256 + t * D;
-    float m_run = -INFINITY;
-    uint64_t l2 = ptx::f2pack(0.f, 0.f);  // running row sum, two partial halves
     const uint64_t scale2 = ptx::f2pack(a.scale_log2, a.scale_log2);
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      ok = ptx::mbar_wait(s_full(t), j & 1, abort_flag, a.status, DEV_TIMEOUT_ATTN);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      ptx::tc_fence_after();
-      // One pass over the tile, 32 columns at a time.  p = 2^(s*scale - m_run)
-      // uses the running maximum as it stands; a chunk whose own maximum exceeds
-      // it by more than 2^8 first raises it (the rescale), scaling the row sum,
-      // the P chunks already written for this tile and, once the tile is done,
-      // O.  The chunk maximum comes from the TMEM load itself; the causal
-      // predicate applies only on tiles that reach past some row's position.
-      // The P chunk of columns [c, c+32) lands in TMEM columns [c/2, c/2 + 16),
-      // which hold S values already read (columns < c + 32).
-      const int key0 = j * KV_TILE;
-      const bool masked = __any_sync(0xffffffffu, key0 + KV_TILE - 1 > pos);
-      float alpha_tile = 1.f;
-      bool rescaled = false;  // warp-uniform
-#pragma unroll
-      for (int c = 0; c < KV_TILE; c += 32) {
-        float sv[32];
-        float cm;
-        if (masked) {
-          ptx::tmem_ld32(s_col + c, sv);
-          cm = -INFINITY;
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            if (key0 + c + k > pos) sv[k] = -INFINITY;
-            cm = fmaxf(cm, sv[k]);
-          }
-        } else {
-          ptx::tmem_ld32_max(s_col + c, sv, cm);
-        }
-        const float cms = cm * a.scale_log2;
-        const bool need = cms > m_run + RESCALE_THRESHOLD;
-        if (__any_sync(0xffffffffu, need)) {
-          float alpha = 1.f;
-          if (need) {
-            alpha = ptx::ex2_approx(m_run - cms);
-            m_run = cms;
-          }
-          l2 = ptx::fmul2(l2, ptx::f2pack(alpha, alpha));
-          alpha_tile *= alpha;
-          rescaled = true;
-          if (c > 0) {
-            // this tile's P columns written so far were scaled by the old maximum
-            ptx::tmem_st_wait();
-#pragma unroll 1
-            for (int pc = 0; pc < c / 2; pc += 16) {
-              float pv[16];
-              ptx::tmem_ld16(s_col + pc, pv);
-              uint32_t w[16];
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const uint32_t u = __float_as_uint(pv[e]);
-                w[e] = pack2(__uint_as_float(u << 16) * alpha, __uint_as_float(u & 0xffff0000u) * alpha);
-              }
-              ptx::tmem_st16(s_col + pc, w);
-            }
-          }
-        }
-        const uint64_t negm2 = ptx::f2pack(-m_run, -m_run);
-        uint32_t pk[16];
-        uint64_t lc = ptx::f2pack(0.f, 0.f);  // this chunk's sum: a second, independent add chain
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          float x0, x1, p0, p1;
-          ptx::f2unpack(ptx::ffma2(ptx::f2pack(sv[k], sv[k + 1]), scale2, negm2), x0, x1);
-          if (k < POLY_EXP2_PER_32) {
-            ptx::exp2_poly2(x0, x1, p0, p1);  // FMA pipe
-          } else {
-            p0 = ptx::ex2_approx(x0);         // MUFU
-            p1 = ptx::ex2_approx(x1);
-          }
-          if ((k & 2) == 0)
-            l2 = ptx::fadd2(l2, ptx::f2pack(p0, p1));
-          else
-            lc = ptx::fadd2(lc, ptx::f2pack(p0, p1));
-          pk[k / 2] = pack2(p0, p1);
-        }
-        l2 = ptx::fadd2(l2, lc);
-        ptx::tmem_st16(s_col + c / 2, pk);
-      }
-      if (j > 0 && rescaled) {
-        // O holds the sum over earlier key tiles: wait for the last PV product
-        // into it, then scale it by this tile's factor
-        ok = ptx::mbar_wait(o_done(t), (j - 1) & 1, abort_flag, a.status, DEV_TIMEOUT_ATTN);
+    int jg = 0;  // key tiles of earlier items (the phase count of s_full, p_full and o_done)
+    for (int k = 0; ok; ++k) {
+      const int u = item_of(k);
+      if (u < 0) break;
+      const Item it = decode_item(u);
+      const int n_kv = it.n_kv;
+      const int rel = it.q0 + t * a.Mq + i;
+      const bool valid = hh < a.r && rel < a.S;
+      const int pos = a.start_pos + rel;
+      float m_run = -INFINITY;
+      uint64_t l2 = ptx::f2pack(0.f, 0.f);  // running row sum, two partial halves
+      for (int j = 0; j < n_kv; ++j) {
+        ok = ptx::mbar_wait(s_full(t), (jg + j) & 1, abort_flag, a.status, DEV_TIMEOUT_ATTN);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D; c += 16) {
-          float ov[16];
-          ptx::tmem_ld16(o_col + c, ov);
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(ov[e] * alpha_tile);
-          ptx::tmem_st16(o_col + c, w);
+        // One pass over the tile, 32 columns at a time.  p = 2^(s*scale - m_run)
+        // uses the running maximum as it stands; a chunk whose own maximum exceeds
+        // it by more than 2^8 first raises it (the rescale), scaling the row sum,
+        // the P chunks already written for this tile and, once the tile is done,
+        // O.  The chunk maximum comes from the TMEM load itself; the causal
+        // predicate applies only on tiles that reach past some row's position.
+        // The P chunk of columns [c, c+32) lands in TMEM columns [c/2, c/2 + 16),
+        // which hold S values already read (columns < c + 32).
+        const int key0 = j * KV_TILE;
+        const bool masked = __any_sync(0xffffffffu, key0 + KV_TILE - 1 > pos);
+        float alpha_tile = 1.f;
+        bool rescaled = false;  // warp-uniform
+  #pragma unroll
+        for (int c = 0; c < KV_TILE; c += 32) {
+          float sv[32];
+          float cm;
+          if (masked) {
+            ptx::tmem_ld32(s_col + c, sv);
+            cm = -INFINITY;
+  #pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              if (key0 + c + k > pos) sv[k] = -INFINITY;
+              cm = fmaxf(cm, sv[k]);
+            }
+          } else {
+            ptx::tmem_ld32_max(s_col + c, sv, cm);
+          }
+          const float cms = cm * a.scale_log2;
+          const bool need = cms > m_run + RESCALE_THRESHOLD;
+          if (__any_sync(0xffffffffu, need)) {
+            float alpha = 1.f;
+            if (need) {
+              alpha = ptx::ex2_approx(m_run - cms);
+              m_run = cms;
+            }
+            l2 = ptx::fmul2(l2, ptx::f2pack(alpha, alpha));
+            alpha_tile *= alpha;
+            rescaled = true;
+            if (c > 0) {
+              // this tile's P columns written so far were scaled by the old maximum
+              ptx::tmem_st_wait();
+  #pragma unroll 1
+              for (int pc = 0; pc < c / 2; pc += 16) {
+                float pv[16];
+                ptx::tmem_ld16(s_col + pc, pv);
+                uint32_t w[16];
+  #pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                  const uint32_t u = __float_as_uint(pv[e]);
+                  w[e] = pack2(__uint_as_float(u << 16) * alpha, __uint_as_float(u & 0xffff0000u) * alpha);
+                }
+                ptx::tmem_st16(s_col + pc, w);
+              }
+            }
+          }
+          const uint64_t negm2 = ptx::f2pack(-m_run, -m_run);
+          uint32_t pk[16];
+          uint64_t lc = ptx::f2pack(0.f, 0.f);  // this chunk's sum: a second, independent add chain
+  #pragma unroll
+          for (int k = 0; k < 32; k += 2) {
+            float x0, x1, p0, p1;
+            ptx::f2unpack(ptx::ffma2(ptx::f2pack(sv[k], sv[k + 1]), scale2, negm2), x0, x1);
+            if (k < POLY_EXP2_PER_32) {
+              ptx::exp2_poly2(x0, x1, p0, p1);  // FMA pipe
+            } else {
+              p0 = ptx::ex2_approx(x0);         // MUFU
+              p1 = ptx::ex2_approx(x1);
+            }
+            if ((k & 2) == 0)
+              l2 = ptx::fadd2(l2, ptx::f2pack(p0, p1));
+            else
+              lc = ptx::fadd2(lc, ptx::f2pack(p0, p1));
+            pk[k / 2] = pack2(p0, p1);
+          }
+          l2 = ptx::fadd2(l2, lc);
+          ptx::tmem_st16(s_col + c / 2, pk);
         }
+        if (j > 0 && rescaled) {
+          // O holds the sum over earlier key tiles: wait for the last PV product
+          // into it, then scale it by this tile's factor
+          ok = ptx::mbar_wait(o_done(t), (jg + j - 1) & 1, abort_flag, a.status, DEV_TIMEOUT_ATTN);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+  #pragma unroll
+          for (int c = 0; c < D; c += 16) {
+            float ov[16];
+            ptx::tmem_ld16(o_col + c, ov);
+            uint32_t w[16];
+  #pragma unroll
+            for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(ov[e] * alpha_tile);
+            ptx::tmem_st16(o_col + c, w);
+          }
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(p_full(t));
       }
-      ptx::tmem_st_wait();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(p_full(t));
-    }
-    if (ok && n_kv > 0) {
-      ok = ptx::mbar_wait(o_done(t), (n_kv - 1) & 1, abort_flag, a.status, DEV_TIMEOUT_ATTN);
-      if (__all_sync(0xffffffffu, ok)) {
-        ptx::tc_fence_after();
-        float la, lb;
-        ptx::f2unpack(l2, la, lb);
-        const float inv = 1.f / (la + lb);
-        bf16 *dst = a.o + (((size_t)b * a.S + rel) * a.H + g * a.r + hh) * D;
-#pragma unroll
-        for (int c = 0; c < D; c += 16) {
-          float ov[16];
-          ptx::tmem_ld16(o_col + c, ov);
-          ptx::tmem_ld_wait();
-          if (valid) {
-            uint4 w0 = make_uint4(pack2(ov[0] * inv, ov[1] * inv), pack2(ov[2] * inv, ov[3] * inv),
-                                  pack2(ov[4] * inv, ov[5] * inv), pack2(ov[6] * inv, ov[7] * inv));
-            uint4 w1 = make_uint4(pack2(ov[8] * inv, ov[9] * inv), pack2(ov[10] * inv, ov[11] * inv),
-                                  pack2(ov[12] * inv, ov[13] * inv), pack2(ov[14] * inv, ov[15] * inv));
-            *reinterpret_cast<uint4 *>(dst + c) = w0;
-            *reinterpret_cast<uint4 *>(dst + c + 8) = w1;
+      if (ok && n_kv > 0) {
+        ok = ptx::mbar_wait(o_done(t), (jg + n_kv - 1) & 1, abort_flag, a.status, DEV_TIMEOUT_ATTN);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+          ptx::tc_fence_after();
+          float la, lb;
+          ptx::f2unpack(l2, la, lb);
+          const float inv = 1.f / (la + lb);
+          bf16 *dst = a.o + (((size_t)it.b * a.S + rel) * a.H + it.g * a.r + hh) * D;
+  #pragma unroll
+          for (int c = 0; c < D; c += 16) {
+            float ov[16];
+            ptx::tmem_ld16(o_col + c, ov);
+            ptx::tmem_ld_wait();
+            if (valid) {
+              uint4 w0 = make_uint4(pack2(ov[0] * inv, ov[1] * inv), pack2(ov[2] * inv, ov[3] * inv),
+                                    pack2(ov[4] * inv, ov[5] * inv), pack2(ov[6] * inv, ov[7] * inv));
+              uint4 w1 = make_uint4(pack2(ov[8] * inv, ov[9] * inv), pack2(ov[10] * inv, ov[11] * inv),
+                                    pack2(ov[12] * inv, ov[13] * inv), pack2(ov[14] * inv, ov[15] * inv));
+              *reinterpret_cast<uint4 *>(dst + c) = w0;
+              *reinterpret_cast<uint4 *>(dst + c + 8) = w1;
+            }
           }
         }
       }
+      jg += n_kv;
     }
   }
   ptx::tc_fence_before();
@@ -473,7 +537,12 @@ cudaError_t launch_prefill(const bf16 *q, const bf16 *kc, const bf16 *vc, bf16 *
   args.nqb = (S + 2 * Mq - 1) / (2 * Mq);
   args.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   args.status = status;
-  const unsigned grid = (unsigned)(B * G * args.nqb);
+  // persistent: at most one CTA per SM, each looping over its items
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int items = B * G * args.nqb;
+  const unsigned grid = (unsigned)(sms > 0 && sms < items ? sms : items);
   count_launch();
   return launch_pdl(attn_prefill_kernel<D>, dim3(grid), dim3(ATT_THREADS), L::BYTES, st, mq, mk, mv, args);
 }

@@ -49,7 +49,7 @@ typedef enum {
     LLAMA_ERR_UNSUPPORTED = 5,   /* valid Llama shape this build has no kernel for */
     LLAMA_ERR_OOM = 6,           /* device allocation failed in a create call */
     LLAMA_ERR_CUDA = 7,          /* a CUDA runtime/driver call failed */
-    LLAMA_ERR_DEVICE_TIMEOUT = 8 /* a kernel's bounded wait ran out (see llama_get_device_status) */
+    LLAMA_ERR_DEVICE_TIMEOUT = 8 /* a kernel's bounded wait ran out (see llama_block_device_status) */
 } llama_status;
 
 typedef enum { LLAMA_F32 = 0, LLAMA_BF16 = 1 } llama_dtype;
