@@ -305,19 +305,19 @@ cudaError_t launch_decode_block_fused(const DecodeFusedParams &p, cudaStream_t s
   sc.cache_seq = p.cache_seq;
   sc.halves = p.halves;
   cudaError_t e = gemm_tc_prepare(p.x, p.wqkv, nullptr, nullptr, M, QKV, p.d, EPI_QKV_ROPE, p.status, &p.gemm,
-                                  &norm_x, &sc, true, &m.qkv_a, &m.qkv_w, &a.qkv, &a.bn_qkv);
+                                  &norm_x, &sc, true, &m.qkv_a, &m.qkv_w, &a.qkv, &a.bn_qkv, false);
   if (e == cudaSuccess)
     e = attn_decode_tc_prepare(p.q, p.kc, p.vc, p.o, p.B, p.start_pos, p.H, p.G, p.cache_seq, p.attn, p.status, &m.q,
                                &m.k, &m.v, &a.attn);
   if (e == cudaSuccess)
     e = gemm_tc_prepare(p.o, p.wo, p.x, p.h, M, p.d, p.H * p.D, EPI_RESIDUAL_SQSUM, p.status, &p.gemm, &norm_h,
-                        nullptr, true, &m.o_a, &m.o_w, &a.o, &a.bn_o);
+                        nullptr, true, &m.o_a, &m.o_w, &a.o, &a.bn_o, false);
   if (e == cudaSuccess)
     e = gemm_tc_prepare(p.h, p.w_gu, nullptr, p.act, M, 2 * p.F, p.d, EPI_SWIGLU_ROWSCALE, p.status, &p.gemm, &norm_h,
-                        nullptr, true, &m.gu_a, &m.gu_w, &a.gu, &a.bn_gu);
+                        nullptr, true, &m.gu_a, &m.gu_w, &a.gu, &a.bn_gu, false);
   if (e == cudaSuccess)
     e = gemm_tc_prepare(p.act, p.w_down, p.h, p.y, M, p.d, p.F, EPI_RESIDUAL, p.status, &p.gemm, nullptr, nullptr,
-                        true, &m.dn_a, &m.dn_w, &a.dn, &a.bn_dn);
+                        true, &m.dn_a, &m.dn_w, &a.dn, &a.bn_dn, false);
   if (e != cudaSuccess) return e;
   a.x = p.x;
   a.ss_x = p.ss_x;

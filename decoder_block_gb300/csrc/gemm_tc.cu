@@ -59,6 +59,9 @@ bool cluster_split_fits(int tiles, int splits, int units) {
   static int fits[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};  // per cluster size: 0 unknown, then 1 + max clusters
   std::lock_guard<std::mutex> lock(mu);
   if (fits[splits] == 0) {
+    // the query needs the kernel's shared-memory opt-in (the kernel may not have run yet)
+    cudaFuncSetAttribute(gemm_tc_kernel<EPI, BN, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         GemmCfg<BN>::SMEM_BYTES);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -78,6 +81,18 @@ bool cluster_split_fits(int tiles, int splits, int units) {
     fits[splits] = 1 + clusters;
   }
   return fits[splits] - 1 >= tiles;
+}
+
+// cluster_split_fits for a tile width chosen at run time (the fit depends on
+// the tile width's shared memory, not on the epilogue).
+bool cluster_split_fits_bn(int bn, int tiles, int splits, int units) {
+  switch (bn) {
+    case 256: return cluster_split_fits<EPI_STORE, 256>(tiles, splits, units);
+    case 192: return cluster_split_fits<EPI_STORE, 192>(tiles, splits, units);
+    case 128: return cluster_split_fits<EPI_STORE, 128>(tiles, splits, units);
+    case 64: return cluster_split_fits<EPI_STORE, 64>(tiles, splits, units);
+  }
+  return false;
 }
 
 template <int EPI, int BN, bool GROUPED = false>
@@ -193,7 +208,7 @@ cudaError_t launch_gemm_grouped(const bf16 *A, const bf16 *W, void *C, int M, in
   }
 }
 
-GemmPlan plan_gemm(int M, int N, int K, size_t ws_part_bytes, int ws_counter_slots) {
+GemmPlan plan_gemm(int M, int N, int K, size_t ws_part_bytes, int ws_counter_slots, bool allow_cluster) {
   const int sms = sm_count();
   const int m_tiles = (M + BM - 1) / BM;
   const int k_steps = (K + BK - 1) / BK;
@@ -242,8 +257,9 @@ GemmPlan plan_gemm(int M, int N, int K, size_t ws_part_bytes, int ws_counter_slo
   // that minimise the per-SM load, rounds x (K steps per unit) x (shared-memory
   // fill per K step: 16 KB of A plus BN x 128 B of weights); ties go to more
   // units (more SMs streaming weights at once).  192-wide tiles serve wide
-  // unsplit projections: 28672 gate/up rows make 150 of them, one per SM, where
-  // 256-wide tiles leave 40 SMs without weights to stream.
+  // unsplit projections (28672 gate/up rows make 150 of them, one per SM, where
+  // 256-wide tiles leave 40 SMs without weights to stream) and cluster splits
+  // (the 8B QKV projection: 32 tiles in clusters of 4).
   double best = 1e30;
   int best_units = 0;
   const int bns[4] = {256, 192, 128, 64};
@@ -254,16 +270,24 @@ GemmPlan plan_gemm(int M, int N, int K, size_t ws_part_bytes, int ws_counter_slo
       const int kss = (k_steps + want - 1) / want;
       const int splits = (k_steps + kss - 1) / kss;
       const int units = tiles * splits;
-      if (bn == 192 && splits > 1) continue;
+      // the pieces of every tile fit one wave of thread-block clusters: summed
+      // through distributed shared memory (see launch_cfg), not L2
+      const bool cluster = allow_cluster && splits > 1 && cluster_split_fits_bn(bn, tiles, splits, units);
+      if (bn == 192 && splits > 1 && !cluster) continue;
       if (splits > 1 && ((size_t)tiles * BM * bn * sizeof(float) > ws_part_bytes || tiles * 4 > ws_counter_slots))
         continue;
       const int rounds = (units + sms - 1) / sms;
       // + 12 K steps of fixed per-unit cost (pipeline fill, epilogue; measured on the
-      // decode shapes); each split piece's reduction into the tile's accumulator
-      // (L2 atomics on the same lines, then the last piece's serial finish) adds
-      // about two rows of weights' worth per piece (measured on the decode shapes:
-      // 9 pieces of a 256-wide tile lose to 4 of a 128-wide one)
-      const double cost = (double)rounds * (kss + 12) * (16.0 + bn / 8.0) + (splits > 1 ? splits * bn / 4.0 : 0.0);
+      // decode shapes).  Reductions, fitted to the 8B decode projections (M = 64):
+      // in L2, each piece's atomics on the tile's lines plus the last piece's serial
+      // finish cost about two rows of weights per piece and a fixed hand-over (9
+      // pieces of a 256-wide tile lose to 4 of a 128-wide one; 3 pieces in L2 lose
+      // to a cluster of 4 at 192 wide, 23.2 vs 21.5 us for QKV); in a cluster the
+      // cost grows with the square of its size (8 pieces of a 256-wide tile lose to
+      // 4 of a 128-wide one, 31.7 vs 30.9 us for the down projection).
+      const double red =
+          splits > 1 ? (cluster ? splits * splits * bn / 16.0 : splits * bn / 4.0 + 192.0) : 0.0;
+      const double cost = (double)rounds * (kss + 12) * (16.0 + bn / 8.0) + red;
       if (cost < best - 1e-9 || (cost <= best + 1e-9 && units > best_units && units <= sms)) {
         best = cost;
         best_units = units;
@@ -289,7 +313,8 @@ int gemm_splitk_counter_slots() { return 4 * sm_count() * 4; }
 
 cudaError_t gemm_tc_prepare(const bf16 *A, const bf16 *W, const bf16 *R, void *C, int M, int N, int K, int epi,
                             int *status, const GemmWorkspace *ws, const RowNorm *norm, const QkvScatter *scatter,
-                            bool weights_static, CUtensorMap *ma, CUtensorMap *mw, GemmArgs *out, int *bn) {
+                            bool weights_static, CUtensorMap *ma, CUtensorMap *mw, GemmArgs *out, int *bn,
+                            bool allow_cluster) {
   if (M <= 0 || N <= 0 || K <= 0 || (K & 7) != 0) return cudaErrorInvalidValue;
   if ((epi == EPI_SWIGLU || epi == EPI_SWIGLU_ROWSCALE) && (N & 31) != 0) return cudaErrorInvalidValue;
   const bool needs_norm = epi == EPI_STORE_ROWSCALE || epi == EPI_SWIGLU_ROWSCALE || epi == EPI_RESIDUAL_SQSUM ||
@@ -300,7 +325,8 @@ cudaError_t gemm_tc_prepare(const bf16 *A, const bf16 *W, const bf16 *R, void *C
         N != (scatter->H + 2 * scatter->G) * scatter->D || M % scatter->S != 0)
       return cudaErrorInvalidValue;
   }
-  const GemmPlan plan = plan_gemm(M, N, K, ws != nullptr ? ws->part_bytes : 0, ws != nullptr ? ws->counter_slots : 0);
+  const GemmPlan plan = plan_gemm(M, N, K, ws != nullptr ? ws->part_bytes : 0, ws != nullptr ? ws->counter_slots : 0,
+                                  allow_cluster);
   GemmArgs args{R, C, M, N, K, status, 1, (K + BK - 1) / BK, 0, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f,
                 {}, weights_static ? 1 : 0, nullptr, 0};
   if (scatter != nullptr) args.qkv = *scatter;

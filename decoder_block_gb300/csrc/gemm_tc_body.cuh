@@ -820,9 +820,10 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
 // Validation, tile plan (plan_gemm), arguments and tensor maps of one GEMM,
 // exactly as launch_gemm_tc launches it (arguments as there); bn receives the
 // plan's tile width.  For a caller that runs the GEMM as a phase of its own
-// kernel.  M, N > 0.
+// kernel (allow_cluster false: a phase cannot use thread-block clusters).  M, N > 0.
 cudaError_t gemm_tc_prepare(const bf16 *A, const bf16 *W, const bf16 *R, void *C, int M, int N, int K, int epi,
                             int *status, const GemmWorkspace *ws, const RowNorm *norm, const QkvScatter *scatter,
-                            bool weights_static, CUtensorMap *ma, CUtensorMap *mw, GemmArgs *args, int *bn);
+                            bool weights_static, CUtensorMap *ma, CUtensorMap *mw, GemmArgs *args, int *bn,
+                            bool allow_cluster = true);
 
 }  // namespace llama

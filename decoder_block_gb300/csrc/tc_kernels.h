@@ -36,7 +36,9 @@ struct GemmPlan {
   int ksteps_split = 0;  // BK steps per piece
   int split_tiles = 0;   // how many tiles (the last ones in raster order) are split
 };
-GemmPlan plan_gemm(int M, int N, int K, size_t ws_part_bytes, int ws_counter_slots);
+// allow_cluster: the GEMM runs as its own launch, which may group a tile's K
+// pieces into a thread-block cluster (a phase of a fused kernel cannot).
+GemmPlan plan_gemm(int M, int N, int K, size_t ws_part_bytes, int ws_counter_slots, bool allow_cluster = true);
 
 // RMSNorm statistics for the fused epilogues: ss_in (ROWSCALE modes) holds
 // sum_j A[m][j]^2 over the d normalised columns; ss_out (EPI_RESIDUAL_SQSUM)
