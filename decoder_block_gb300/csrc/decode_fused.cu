@@ -294,6 +294,7 @@ cudaError_t launch_decode_block_fused(const DecodeFusedParams &p, cudaStream_t s
   norm_h.d = p.d;
   QkvScatter sc;
   sc.table = p.rope;
+  sc.table_seq = p.rope_seq;
   sc.q = p.q;
   sc.kc = p.kc;
   sc.vc = p.vc;

@@ -264,10 +264,11 @@ __device__ __forceinline__ void load_rope32(const GemmArgs &a, int m, int n, flo
   if constexpr (EPI == EPI_QKV_ROPE) {
     const QkvScatter &r = a.qkv;
     if (m < a.M && n < a.N && n / r.D < r.H + r.G) {
-      const float4 *p = reinterpret_cast<const float4 *>(r.table + (size_t)(r.start_pos + m % r.S) * (r.D / 2) +
-                                                         (n % r.D) / 2);
+      // grouped table: pair group g of position p at float4 g * table_seq + p
+      const float4 *p = reinterpret_cast<const float4 *>(r.table) + (size_t)((n % r.D) / 4) * r.table_seq +
+                        (r.start_pos + m % r.S);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) cs[k] = __ldg(p + k);
+      for (int k = 0; k < 8; ++k) cs[k] = __ldg(p + (size_t)k * r.table_seq);
     }
   }
 }

@@ -50,6 +50,11 @@ struct RopeScaling {
 // f_i = theta^(-2i/D), stretched when sc.factor > 1; computed in fp64.
 cudaError_t launch_rope_table(float2 *table, int max_seq, int D, double theta, const RopeScaling &sc,
                               cudaStream_t st);
+// The same values grouped for the GEMM epilogue: [D/4][max_seq] float4 =
+// {cos_2g, sin_2g, cos_2g+1, sin_2g+1} at (g, p), so that the 32 rows (consecutive
+// positions) of a warp read one contiguous 512-byte run per pair group.
+cudaError_t launch_rope_table_grouped(float2 *table, int max_seq, int D, double theta, const RopeScaling &sc,
+                                      cudaStream_t st);
 
 // RoPE on q and k of qkv [T][(H + 2G) D] and the KV-cache write.
 //   q_out [T][H D] (rotated q); kc/vc [cache_batch][G][cache_seq][D].

@@ -371,6 +371,13 @@ llama_status alloc_workspace(const Dims &dm, int max_tokens, bool staging, Alloc
     }                                                \
   } while (0)
 
+// The handle's cos/sin table: grouped for the GEMM epilogue when that applies the
+// rotation (bf16, D % 32 == 0), else row-major for rope_kv_kernel.
+cudaError_t launch_rope_table_any(const Dims &dm, float2 *table) {
+  return dm.fused_qkv_rope() ? launch_rope_table_grouped(table, dm.max_seq, dm.D, dm.theta, dm.rope_scaling, nullptr)
+                             : launch_rope_table(table, dm.max_seq, dm.D, dm.theta, dm.rope_scaling, nullptr);
+}
+
 template <typename T>
 llama_status forward_simt(const Dims &dm, const Weights &w, const Workspace &ws, const float2 *rope, const T *x,
                           T *y, int B, int S, int start_pos, const llama_kv_cache *kv, cudaStream_t st) {
@@ -452,6 +459,7 @@ llama_status forward_decode_fused(const Dims &dm, const Weights &w, const Worksp
   p.ss_x = ws.ss_x;
   p.ss_h = ws.ss_h;
   p.rope = rope;
+  p.rope_seq = dm.max_seq;
   p.kc = (bf16 *)kv->k;
   p.vc = (bf16 *)kv->v;
   p.cache_seq = kv->max_seq_len;
@@ -495,6 +503,7 @@ llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, c
     // QKV projection, RoPE and the cache write in one GEMM epilogue
     QkvScatter sc;
     sc.table = rope;
+    sc.table_seq = dm.max_seq;
     sc.q = q;
     sc.kc = kc;
     sc.vc = vc;
@@ -638,7 +647,7 @@ llama_status llama_block_create(const llama_config *cfg, const llama_block_weigh
     if (b->al.failed) s = LLAMA_ERR_OOM;
   }
   if (s == LLAMA_OK) {
-    if (launch_rope_table(b->rope, dm.max_seq, dm.D, dm.theta, dm.rope_scaling, nullptr) != cudaSuccess ||
+    if (launch_rope_table_any(dm, b->rope) != cudaSuccess ||
         cudaMemset(b->status, 0, sizeof(int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
       s = LLAMA_ERR_CUDA;
   }
@@ -828,7 +837,7 @@ llama_status llama_stack_create(const llama_config *cfg, int32_t n_layers, int32
     cudaError_t err = cudaMemcpy(k->embed, embed, (size_t)vocab * dm.d * e, cudaMemcpyDeviceToDevice);
     if (err == cudaSuccess) err = cudaMemcpy(k->lm_head, lm_head, (size_t)vocab * dm.d * e, cudaMemcpyDeviceToDevice);
     if (err == cudaSuccess) err = cudaMemcpy(k->final_norm, final_norm, dm.d * e, cudaMemcpyDeviceToDevice);
-    if (err == cudaSuccess) err = launch_rope_table(k->rope, dm.max_seq, dm.D, dm.theta, dm.rope_scaling, nullptr);
+    if (err == cudaSuccess) err = launch_rope_table_any(dm, k->rope);
     if (err == cudaSuccess) err = cudaMemset(k->status, 0, sizeof(int));
     if (err == cudaSuccess) err = cudaDeviceSynchronize();
     if (err != cudaSuccess) s = LLAMA_ERR_CUDA;

@@ -266,6 +266,9 @@ __device__ double rope_frequency(int i, int D, double theta, RopeScaling sc) {
   return (1.0 - w) * f / sc.factor + w * f;
 }
 
+// grouped: pair i of position p at float2 index ((i / 2) * max_seq + p) * 2 + i % 2
+// (launch_rope_table_grouped), else at p * (D / 2) + i.
+template <bool GROUPED>
 __global__ void rope_table_kernel(float2 *table, int max_seq, int D, double theta, RopeScaling sc) {
   const int half = D / 2;
   const size_t n = (size_t)max_seq * half;
@@ -274,7 +277,8 @@ __global__ void rope_table_kernel(float2 *table, int max_seq, int D, double thet
     const double f = rope_frequency(i, D, theta, sc);
     double s, c;
     sincos((double)p * f, &s, &c);
-    table[idx] = make_float2((float)c, (float)s);
+    const size_t at = GROUPED ? ((size_t)(i / 2) * max_seq + p) * 2 + (i & 1) : idx;
+    table[at] = make_float2((float)c, (float)s);
   }
 }
 
@@ -283,7 +287,17 @@ cudaError_t launch_rope_table(float2 *table, int max_seq, int D, double theta, c
   const size_t n = (size_t)max_seq * (D / 2);
   const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
   count_launch();
-  rope_table_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(table, max_seq, D, theta, sc);
+  rope_table_kernel<false><<<blocks > 0 ? blocks : 1, 256, 0, st>>>(table, max_seq, D, theta, sc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table_grouped(float2 *table, int max_seq, int D, double theta, const RopeScaling &sc,
+                                      cudaStream_t st) {
+  if (D % 4 != 0) return cudaErrorInvalidValue;
+  const size_t n = (size_t)max_seq * (D / 2);
+  const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  count_launch();
+  rope_table_kernel<true><<<blocks > 0 ? blocks : 1, 256, 0, st>>>(table, max_seq, D, theta, sc);
   return cudaGetLastError();
 }
 

@@ -59,7 +59,8 @@ struct RowNorm {
 // so accumulator columns (2i, 2i+1) of a head hold components (i, i + D/2); the
 // pair is rotated as above and stored back at i and i + D/2 (natural order).
 struct QkvScatter {
-  const float2 *table = nullptr;
+  const float2 *table = nullptr;  // launch_rope_table_grouped layout, table_seq positions
+  int table_seq = 0;
   bf16 *q = nullptr, *kc = nullptr, *vc = nullptr;
   int S = 1, start_pos = 0, H = 0, G = 0, D = 0, cache_seq = 0, halves = 0;
 };
@@ -131,7 +132,8 @@ struct DecodeFusedParams {
   const bf16 *wqkv = nullptr, *wo = nullptr, *w_gu = nullptr, *w_down = nullptr;
   bf16 *q = nullptr, *o = nullptr, *h = nullptr, *act = nullptr;  // workspace activations
   float *ss_x = nullptr, *ss_h = nullptr;
-  const float2 *rope = nullptr;
+  const float2 *rope = nullptr;  // launch_rope_table_grouped layout, rope_seq positions
+  int rope_seq = 0;
   bf16 *kc = nullptr, *vc = nullptr;
   int cache_seq = 0;
   int B = 0, start_pos = 0, d = 0, H = 0, G = 0, D = 0, F = 0, halves = 0;
