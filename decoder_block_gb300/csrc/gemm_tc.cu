@@ -215,40 +215,48 @@ GemmPlan plan_gemm(int M, int N, int K, size_t ws_part_bytes, int ws_counter_slo
   GemmPlan p;
   auto tiles_for = [&](int bn) { return m_tiles * ((N + bn - 1) / bn); };
   if (tiles_for(256) >= sms) {
-    // Compute-bound regime: fewest waves, weighted by the narrower tiles' lower
-    // per-flop efficiency (shared-memory operand traffic per MMA).
-    const int bns[3] = {256, 128, 64};
-    const double eff[3] = {1.0, 1.12, 1.45};
+    // Compute-bound regime: the fewest waves, counting a split tail (below) as the
+    // fraction of a wave it takes, weighted by each tile width's cost per output
+    // column.  Every K step brings (128 + BN) x 128 B of operands into an SM, and
+    // that delivery, not the MMA, paces a K step (a 128 x 256 step takes about
+    // 700 cycles against 512 of MMA); per column it costs 1, 1.11, 1.33 and 2.0
+    // times the 256-wide figure for BN = 256, 192, 128, 64.  (Timestamped at the
+    // SmolLM2 shape, 64-wide tiles were worse still: 3.4 times per column.)
+    const int bns[4] = {256, 192, 128, 64};
+    const double eff[4] = {1.0, 1.11, 1.33, 2.0};
     double best = 1e30;
-    for (int i = 0; i < 3; ++i) {
-      const int waves = (tiles_for(bns[i]) + sms - 1) / sms;
-      const double cost = waves * bns[i] * eff[i];
-      if (cost < best - 1e-9) {
-        best = cost;
-        p.bn = bns[i];
-      }
-    }
-    // A short partial last wave (at most a quarter of the SMs busy) leaves most SMs
-    // idle for a whole tile time: split its tiles along K into pieces that every SM
-    // shares (run first, so their reductions overlap the full waves).  The tail then
-    // costs ceil(tail * s / sms) / s of a tile time instead of one, plus the pieces'
-    // reduction (charged as 0.05 of a tile).  Longer tails gain less than the L2
-    // reductions of their many pieces cost (measured), and so do short K loops.
-    const int tiles = tiles_for(p.bn), tail = tiles % sms;
-    if (tail > 0 && 4 * tail <= sms && k_steps >= 32 && (size_t)tail * BM * p.bn * sizeof(float) <= ws_part_bytes &&
-        tail * 4 <= ws_counter_slots) {
-      double best_tail = 1.0;
-      for (int s = 2; s <= 16 && k_steps / s >= 4; ++s) {
-        const double cost = (double)((tail * s + sms - 1) / sms) / s + 0.05;
-        if (cost < best_tail - 1e-9) {
-          best_tail = cost;
-          p.splits = s;
+    for (int i = 0; i < 4; ++i) {
+      GemmPlan c;
+      c.bn = bns[i];
+      // A short partial last wave (at most a quarter of the SMs busy) leaves most SMs
+      // idle for a whole tile time: split its tiles along K into pieces that every SM
+      // shares (run first, so their reductions overlap the full waves).  The tail then
+      // costs ceil(tail * s / sms) / s of a tile time instead of one, plus the pieces'
+      // reduction (charged as 0.05 of a tile).  Longer tails gain less than the L2
+      // reductions of their many pieces cost (measured), and so do short K loops.
+      const int tiles = tiles_for(c.bn), tail = tiles % sms;
+      double waves = (double)(tiles / sms) + (tail > 0 ? 1.0 : 0.0);
+      if (tail > 0 && 4 * tail <= sms && k_steps >= 32 &&
+          (size_t)tail * BM * c.bn * sizeof(float) <= ws_part_bytes && tail * 4 <= ws_counter_slots) {
+        double best_tail = 1.0;
+        for (int sp = 2; sp <= 16 && k_steps / sp >= 4; ++sp) {
+          const double tc = (double)((tail * sp + sms - 1) / sms) / sp + 0.05;
+          if (tc < best_tail - 1e-9) {
+            best_tail = tc;
+            c.splits = sp;
+          }
+        }
+        if (c.splits > 1) {
+          c.ksteps_split = (k_steps + c.splits - 1) / c.splits;
+          c.splits = (k_steps + c.ksteps_split - 1) / c.ksteps_split;
+          c.split_tiles = tail;
+          waves = (double)(tiles / sms) + best_tail;
         }
       }
-      if (p.splits > 1) {
-        p.ksteps_split = (k_steps + p.splits - 1) / p.splits;
-        p.splits = (k_steps + p.ksteps_split - 1) / p.ksteps_split;
-        p.split_tiles = tail;
+      const double cost = waves * c.bn * eff[i];
+      if (cost < best - 1e-9) {
+        best = cost;
+        p = c;
       }
     }
     return p;

@@ -63,7 +63,9 @@ struct GemmCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = BN == 256 ? 4 : (BN == 192 ? 5 : (BN == 128 ? 6 : 8));
   static constexpr int NUM_BARS = 2 * STAGES + 7;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+  // after the barriers and flags: the four epilogue warps' 2 KB output stages
+  static constexpr int STAGE_OUT_OFF = (STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 15) / 16 * 16;
+  static constexpr int SMEM_BYTES = 1024 + STAGE_OUT_OFF + 4 * 2048;
   // two accumulators of BN columns, in a power-of-two allocation (128, 256 or 512)
   static constexpr uint32_t TMEM_COLS = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
 };
@@ -314,6 +316,74 @@ __device__ __forceinline__ float epilogue_chunk32(float (&v)[32], const GemmArgs
     epilogue_chunk16<EPI>(v + 16, a, m, n + 16, res != nullptr ? res + 2 : nullptr);
     return 0.f;
   }
+}
+
+// Residual epilogues of whole tiles move the residual in and the result out
+// through each epilogue warp's 2 KB shared-memory stage (32 rows x 64 bytes):
+// lane l reads or writes 16-byte unit l % 4 of row 8j + l / 4, eight rows of 64
+// contiguous bytes per instruction, instead of one row per lane (32 rows per
+// instruction, which made the load/store units pace the epilogue).  Unit u of
+// row r sits at slot (u + r / 2) % 4, so that both access patterns are free of
+// bank conflicts.
+__device__ __forceinline__ int stage_slot(int r, int u) { return r * 4 + ((u + (r >> 1)) & 3); }
+
+// Residual columns n .. n+31 of rows rbase + 8j + lane / 4 (j = 0..3), unit lane % 4.
+__device__ __forceinline__ void coop_load_residual32(const GemmArgs &a, int rbase, int m_end, int n, int lane,
+                                                     uint4 (&g)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int row = rbase + 8 * j + (lane >> 2);
+    g[j] = row < m_end ? *reinterpret_cast<const uint4 *>(a.R + (size_t)row * a.N + n + 8 * (lane & 3))
+                       : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// EPI_RESIDUAL / EPI_RESIDUAL_SQSUM over the BN columns from n0 of a whole tile's
+// 32 rows from rbase (this warp's TMEM lanes at trow); every 32-column chunk lies
+// inside N and N % 8 == 0.  g: chunk 0's residual from coop_load_residual32.
+// Returns the sum of squares of this lane's row of stored values.
+template <int EPI, int BN>
+__device__ __forceinline__ float residual_tile_staged(const GemmArgs &a, uint32_t trow, uint4 *stage, int rbase,
+                                                      int m_end, int n0, int lane, uint4 (&g)[4]) {
+  float sq = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < BN; c += 32) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) stage[stage_slot(8 * j + (lane >> 2), lane & 3)] = g[j];
+    __syncwarp();
+    uint4 rc[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) rc[u] = stage[stage_slot(lane, u)];
+    if (c + 32 < BN) coop_load_residual32(a, rbase, m_end, n0 + c + 32, lane, g);  // in flight meanwhile
+    __syncwarp();
+    float v[32];
+    ptx::tmem_ld32(trow + c, v);
+    uint32_t w[16];
+    const bf16 *rb = reinterpret_cast<const bf16 *>(rc);
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      const float x0 = v[i] + __bfloat162float(rb[i]), x1 = v[i + 1] + __bfloat162float(rb[i + 1]);
+      w[i / 2] = pack_bf16(x0, x1);
+      if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
+        const float q0 = __bfloat162float(__float2bfloat16_rn(x0)), q1 = __bfloat162float(__float2bfloat16_rn(x1));
+        sq = fmaf(q0, q0, sq);
+        sq = fmaf(q1, q1, sq);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) stage[stage_slot(lane, u)] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = 8 * j + (lane >> 2);
+      const uint4 val = stage[stage_slot(r, lane & 3)];
+      if (rbase + r < m_end)
+        *reinterpret_cast<uint4 *>(reinterpret_cast<bf16 *>(a.C) + (size_t)(rbase + r) * a.N + n0 + c + 8 * (lane & 3)) =
+            val;
+    }
+    __syncwarp();
+  }
+  return sq;
 }
 
 // Work unit u of a dense (not grouped) GEMM with tile width bn: the K pieces of
@@ -615,6 +685,7 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
     if (!inputs_ready) *abort_flag = 1;
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
+    uint4 *stage_out = reinterpret_cast<uint4 *>(smem + G::STAGE_OUT_OFF + (warp - 2) * 2048);
     int tcount = 0;
     int shared_splits = 0;  // split units finished jointly so far (phase of parts_bar / count_bar)
     for (int u = blockIdx.x; u < num_units && inputs_ready; u += gridDim.x, ++tcount) {
@@ -629,20 +700,32 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
       // are loaded while its MMAs run: with a short K loop the epilogue is the
       // critical path, and each of these loads would otherwise stall a chunk.
       constexpr bool kRes = EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_SQSUM;
+      // whole 32-column chunks of a residual epilogue go through the output stage
+      const bool staged = kRes && (args.N & 7) == 0 && (nt + 1) * BN <= args.N;
       float rs = 1.f;
       uint4 rc[4];
       float4 cs[8];
       bool vc = false;
       if (slot < 0) {
         rs = row_scale<EPI>(args, m);
-        if (kRes) load_residual32(args, m, nt * BN, rc, vc);
+        if (staged)
+          coop_load_residual32(args, a_row + q * 32, m_end, nt * BN, lane, rc);
+        else if (kRes)
+          load_residual32(args, m, nt * BN, rc, vc);
         load_rope32<EPI>(args, m, nt * BN, cs);
       }
       bool ok = ptx::mbar_wait(tfull_bar(acc), aph, abort_flag, args.status, DEV_TIMEOUT_EPILOGUE);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
       const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      if (slot < 0) {
+      if (slot < 0 && staged) {
+        const float sq = residual_tile_staged<EPI, BN>(args, trow, stage_out, a_row + q * 32, m_end, nt * BN, lane, rc);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(tempty_bar(acc));
+        if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
+          if (m < args.M) atomicAdd(args.ss_out + m, sq);
+        }
+      } else if (slot < 0) {
         // the next chunk's residual and rotation pairs load while this chunk is finished
         float sq = 0.f;
         uint4 rn[4];
