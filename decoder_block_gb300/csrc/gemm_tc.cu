@@ -188,7 +188,8 @@ cudaError_t launch_gemm_grouped(const bf16 *A, const bf16 *W, void *C, int M, in
   else if (N % 64 == 0)
     bn = 64;
   if (bn == 0) return cudaErrorInvalidValue;
-  GemmArgs args{nullptr, C, M, N, K, status, 1, (K + BK - 1) / BK, 0, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f,
+  GemmArgs args{nullptr, C, M, N, K, status, 1, (K + BK - 1) / BK, 0, nullptr, nullptr, nullptr, nullptr, nullptr,
+                nullptr, 0.f, 0.f,
                 {}, 0, group_off, n_groups};
   CUtensorMap ma, mb;
   if (!make_map_2d(&ma, A, (uint64_t)M, (uint64_t)K, BM) ||
@@ -335,12 +336,15 @@ cudaError_t gemm_tc_prepare(const bf16 *A, const bf16 *W, const bf16 *R, void *C
   }
   const GemmPlan plan = plan_gemm(M, N, K, ws != nullptr ? ws->part_bytes : 0, ws != nullptr ? ws->counter_slots : 0,
                                   allow_cluster);
-  GemmArgs args{R, C, M, N, K, status, 1, (K + BK - 1) / BK, 0, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f,
+  GemmArgs args{R, C, M, N, K, status, 1, (K + BK - 1) / BK, 0, nullptr, nullptr, nullptr, nullptr, nullptr,
+                nullptr, 0.f, 0.f,
                 {}, weights_static ? 1 : 0, nullptr, 0};
   if (scatter != nullptr) args.qkv = *scatter;
   if (norm != nullptr) {
     args.ss_in = norm->ss_in;
     args.ss_out = norm->ss_out;
+    args.zero_a = norm->zero_a;
+    args.zero_b = norm->zero_b;
     args.inv_d = 1.0f / (float)norm->d;
     args.eps = norm->eps;
   }

@@ -82,6 +82,7 @@ struct GemmArgs {
   int *counters;     // split-K arrivals [tiles][4] (zero at launch; left zero at exit)
   const float *ss_in;  // ROWSCALE epilogues: per-row sum of squares of A's rows
   float *ss_out;       // EPI_RESIDUAL_SQSUM: per-row sum of squares of C (accumulated)
+  float *zero_a, *zero_b;  // EPI_RESIDUAL_SQSUM: rows cleared by N tile 0 (null: none)
   float inv_d, eps;    // RMSNorm: scale = rsqrt(ss * inv_d + eps)
   QkvScatter qkv;      // EPI_QKV_ROPE destinations
   int prefetch_w;      // W is written by no kernel: load it before the grid dependency wait
@@ -316,6 +317,13 @@ __device__ __forceinline__ float epilogue_chunk32(float (&v)[32], const GemmArgs
     epilogue_chunk16<EPI>(v + 16, a, m, n + 16, res != nullptr ? res + 2 : nullptr);
     return 0.f;
   }
+}
+
+// EPI_RESIDUAL_SQSUM: the epilogue of N tile 0 clears row m of the zero_a /
+// zero_b accumulators (one thread per row).
+__device__ __forceinline__ void clear_rows(const GemmArgs &a, int m) {
+  if (a.zero_a != nullptr) a.zero_a[m] = 0.f;
+  if (a.zero_b != nullptr) a.zero_b[m] = 0.f;
 }
 
 // Residual epilogues of whole tiles move the residual in and the result out
@@ -723,7 +731,10 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
         ptx::tc_fence_before();
         ptx::mbar_arrive(tempty_bar(acc));
         if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
-          if (m < args.M) atomicAdd(args.ss_out + m, sq);
+          if (m < args.M) {
+            atomicAdd(args.ss_out + m, sq);
+            if (nt == 0) clear_rows(args, m);
+          }
         }
       } else if (slot < 0) {
         // the next chunk's residual and rotation pairs load while this chunk is finished
@@ -751,7 +762,10 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
         ptx::tc_fence_before();
         ptx::mbar_arrive(tempty_bar(acc));
         if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
-          if (m < args.M) atomicAdd(args.ss_out + m, sq);
+          if (m < args.M) {
+            atomicAdd(args.ss_out + m, sq);
+            if (nt == 0) clear_rows(args, m);
+          }
         }
       } else {
         if (args.cluster_split) {
@@ -842,7 +856,10 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
           const float sq = splitk_finish<EPI, BN>(args, tile, nt, fin_r, fin_m, fin_c0, fin_c1);
           if (cnt_slot >= 0) args.counters[cnt_slot] = 0;
           if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
-            if (fin_m < args.M) atomicAdd(args.ss_out + fin_m, sq);
+            if (fin_m < args.M) {
+              atomicAdd(args.ss_out + fin_m, sq);
+              if (nt == 0 && fin_c0 == 0) clear_rows(args, fin_m);
+            }
           }
         }
       }
@@ -884,7 +901,10 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
         sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + ch * 32, rs, nullptr, cs);
       }
       if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
-        if (m < args.M) atomicAdd(args.ss_out + m, sq);
+        if (m < args.M) {
+          atomicAdd(args.ss_out + m, sq);
+          if (nt == 0 && rank == 0) clear_rows(args, m);
+        }
       }
     }
     ptx::cluster_sync();

@@ -26,7 +26,8 @@ enum Epilogue : int {
 };
 
 // ss[t] = sum_j x[t][j]^2 (fp32) for rows of width d; zero_out[t] = 0 when not null.
-cudaError_t launch_row_sqsum(const bf16 *x, float *ss, float *zero_out, int rows, int d, cudaStream_t st);
+cudaError_t launch_row_sqsum(const bf16 *x, float *ss, float *zero_out, int rows, int d, cudaStream_t st,
+                             float *zero_out2 = nullptr);
 
 // W[n][k] <- bf16(W[n][k] * g[k]) in place (fold an RMSNorm gain into a weight).
 cudaError_t launch_scale_columns(bf16 *W, const bf16 *g, int rows, int cols, cudaStream_t st);

@@ -100,6 +100,7 @@ struct Workspace {
   AttnScratch attn;                      // split-KV partials of the decode path
   GemmWorkspace gemm;                    // split-K partials of few-row GEMMs (decode)
   float *ss_x = nullptr, *ss_h = nullptr;  // per-row sums of squares (fused RMSNorm statistics)
+  float *ss_x2 = nullptr;                  // the other input-statistics buffer of a stack's layer chain
   // mixture of experts: router logits [T][E_pad] fp32; per (token, choice) expert id,
   // weight and row in the expert-grouped buffers; per-expert counts / offsets / fill;
   // expert inputs [T k][d], SwiGLU outputs [T k][F], outputs [T k][d]; shared expert
@@ -350,6 +351,7 @@ llama_status alloc_workspace(const Dims &dm, int max_tokens, bool staging, Alloc
     ws->gemm.counters = (int *)al.alloc((size_t)ws->gemm.counter_slots * sizeof(int));
     ws->ss_x = (float *)al.alloc(T * sizeof(float));
     ws->ss_h = (float *)al.alloc(T * sizeof(float));
+    ws->ss_x2 = (float *)al.alloc(T * sizeof(float));
     ws->fused_sync = (unsigned *)al.alloc(2 * sizeof(unsigned));
   }
   if (al.failed) return LLAMA_ERR_OOM;
@@ -480,9 +482,18 @@ llama_status forward_decode_fused(const Dims &dm, const Weights &w, const Worksp
   return LLAMA_OK;
 }
 
+// Row statistics handed from one block of a stack to the next: the down
+// projection's epilogue sums the squares of the rows of y it stores, which are
+// the next block's attention-norm statistics, so the next block skips its
+// statistics pass.  The two input buffers alternate between blocks.
+struct LayerStats {
+  float *in = nullptr;    // sums of squares of x's rows, already accumulated (null: compute them here)
+  float *next = nullptr;  // accumulate the sums of squares of y's rows here, zero on entry (null: don't)
+};
+
 llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, const float2 *rope, const bf16 *x,
                         bf16 *y, int B, int S, int start_pos, const llama_kv_cache *kv, int *status, Profiler *prof,
-                        cudaStream_t st) {
+                        cudaStream_t st, const LayerStats *ls = nullptr) {
   if (ws.decode_mode == LLAMA_DECODE_FUSED && fused_decode_eligible(dm, S))
     return forward_decode_fused(dm, w, ws, rope, x, y, B, start_pos, kv, status, st);
   const int M = B * S;
@@ -493,10 +504,13 @@ llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, c
   pf.begin_forward();
   // attention_norm statistics; the normalisation itself happens in the QKV GEMM
   pf.mark(0, 0, st);
-  LAUNCH(launch_row_sqsum(x, ws.ss_x, ws.ss_h, M, dm.d, st));
+  const bool stats_ready = ls != nullptr && ls->in != nullptr;
+  float *ss_x = stats_ready ? ls->in : ws.ss_x;
+  if (!stats_ready)  // also clears the accumulators this forward adds into
+    LAUNCH(launch_row_sqsum(x, ws.ss_x, ws.ss_h, M, dm.d, st, ls != nullptr ? ls->next : nullptr));
   pf.mark(0, 1, st);
   RowNorm norm_x;
-  norm_x.ss_in = ws.ss_x;
+  norm_x.ss_in = ss_x;
   norm_x.eps = dm.eps;
   norm_x.d = dm.d;
   if (dm.fused_qkv_rope()) {
@@ -551,17 +565,30 @@ llama_status forward_tc(const Dims &dm, const Weights &w, const Workspace &ws, c
                         &ws.gemm, &norm_h, nullptr, true));
   pf.mark(6, 1, st);
   pf.mark(7, 0, st);
-  LAUNCH(launch_gemm_tc(act, (const bf16 *)w.w_down, h, y, M, dm.d, dm.F, EPI_RESIDUAL, status, st, &ws.gemm,
-                        nullptr, nullptr, true));
+  if (ls != nullptr && ls->next != nullptr) {
+    // y's statistics for the next block; this block's input statistics and the
+    // ffn-norm accumulator are read by now and are cleared for the blocks after
+    RowNorm norm_y;
+    norm_y.ss_out = ls->next;
+    norm_y.zero_a = ss_x;
+    norm_y.zero_b = ws.ss_h;
+    norm_y.eps = dm.eps;
+    norm_y.d = dm.d;
+    LAUNCH(launch_gemm_tc(act, (const bf16 *)w.w_down, h, y, M, dm.d, dm.F, EPI_RESIDUAL_SQSUM, status, st,
+                          &ws.gemm, &norm_y, nullptr, true));
+  } else {
+    LAUNCH(launch_gemm_tc(act, (const bf16 *)w.w_down, h, y, M, dm.d, dm.F, EPI_RESIDUAL, status, st, &ws.gemm,
+                          nullptr, nullptr, true));
+  }
   pf.mark(7, 1, st);
   return LLAMA_OK;
 }
 
 llama_status forward_any(const Dims &dm, const Weights &w, const Workspace &ws, const float2 *rope, const void *x,
                          void *y, int B, int S, int start_pos, const llama_kv_cache *kv, int *status,
-                         cudaStream_t st, Profiler *prof = nullptr) {
+                         cudaStream_t st, Profiler *prof = nullptr, const LayerStats *ls = nullptr) {
   if (dm.dtype == LLAMA_BF16)
-    return forward_tc(dm, w, ws, rope, (const bf16 *)x, (bf16 *)y, B, S, start_pos, kv, status, prof, st);
+    return forward_tc(dm, w, ws, rope, (const bf16 *)x, (bf16 *)y, B, S, start_pos, kv, status, prof, st, ls);
   return forward_simt<float>(dm, w, ws, rope, (const float *)x, (float *)y, B, S, start_pos, kv, st);
 }
 
@@ -866,9 +893,19 @@ llama_status stack_layers(llama_stack *stk, const int32_t *tokens, int B, int S,
     LAUNCH(launch_embed<bf16>(tokens, (const bf16 *)stk->embed, (bf16 *)cur, M, dm.d, stk->vocab, stk->status, st));
   else
     LAUNCH(launch_embed<float>(tokens, (const float *)stk->embed, (float *)cur, M, dm.d, stk->vocab, stk->status, st));
+  // dense bf16 blocks hand their row statistics on (LayerStats); not the
+  // mixture-of-experts feed-forward nor the fused decode kernel
+  const bool chain = dm.dtype == LLAMA_BF16 && !dm.moe() &&
+                     !(stk->ws.decode_mode == LLAMA_DECODE_FUSED && fused_decode_eligible(dm, S));
+  float *stats[2] = {stk->ws.ss_x, stk->ws.ss_x2};
   for (int l = 0; l < stk->n_layers; ++l) {
-    llama_status s =
-        forward_any(dm, stk->layers[l], stk->ws, stk->rope, cur, nxt, B, S, start_pos, &kv[l], stk->status, st);
+    LayerStats ls;
+    if (chain) {
+      ls.in = l == 0 ? nullptr : stats[l & 1];
+      ls.next = l + 1 < stk->n_layers ? stats[(l + 1) & 1] : nullptr;
+    }
+    llama_status s = forward_any(dm, stk->layers[l], stk->ws, stk->rope, cur, nxt, B, S, start_pos, &kv[l],
+                                 stk->status, st, nullptr, chain ? &ls : nullptr);
     if (s != LLAMA_OK) return s;
     void *t = cur;
     cur = nxt;

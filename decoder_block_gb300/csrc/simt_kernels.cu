@@ -111,10 +111,11 @@ cudaError_t launch_rmsnorm(const T *x, const T *g, T *out, int rows, int d, floa
 
 // Sum of squares per row (the RMSNorm statistic of rows the next GEMM normalises
 // in its epilogue): one warp per row, 16-byte loads, fp32 accumulation.  Also
-// clears zero_out[row] (the accumulator a later epilogue adds into), which
-// keeps a memset out of the kernel chain.
+// clears zero_out[row] and zero_out2[row] (accumulators later epilogues add
+// into; either may be null), which keeps memsets out of the kernel chain.
 __global__ void __launch_bounds__(256) row_sqsum_kernel(const bf16 *__restrict__ x, float *__restrict__ ss,
-                                                        float *__restrict__ zero_out, int rows, int d) {
+                                                        float *__restrict__ zero_out, float *__restrict__ zero_out2,
+                                                        int rows, int d) {
   allow_dependents_launch();
   grid_dependency_wait();
   const int row = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
@@ -136,14 +137,16 @@ __global__ void __launch_bounds__(256) row_sqsum_kernel(const bf16 *__restrict__
   if (lane == 0) {
     ss[row] = acc;
     if (zero_out != nullptr) zero_out[row] = 0.f;
+    if (zero_out2 != nullptr) zero_out2[row] = 0.f;
   }
 }
 
-cudaError_t launch_row_sqsum(const bf16 *x, float *ss, float *zero_out, int rows, int d, cudaStream_t st) {
+cudaError_t launch_row_sqsum(const bf16 *x, float *ss, float *zero_out, int rows, int d, cudaStream_t st,
+                             float *zero_out2) {
   if (rows <= 0) return cudaSuccess;
   count_launch();
   return launch_pdl(row_sqsum_kernel, dim3((unsigned)(((size_t)rows * 32 + 255) / 256)), dim3(256), 0, st, x, ss,
-                    zero_out, rows, d);
+                    zero_out, zero_out2, rows, d);
 }
 
 __global__ void scale_columns_kernel(bf16 *__restrict__ W, const bf16 *__restrict__ g, int rows, int cols) {

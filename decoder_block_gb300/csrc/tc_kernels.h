@@ -46,6 +46,10 @@ GemmPlan plan_gemm(int M, int N, int K, size_t ws_part_bytes, int ws_counter_slo
 struct RowNorm {
   const float *ss_in = nullptr;
   float *ss_out = nullptr;
+  // EPI_RESIDUAL_SQSUM: rows of these arrays (either may be null) are cleared by
+  // the epilogue of N tile 0, for accumulators of later kernels whose readers
+  // have finished before this kernel starts
+  float *zero_a = nullptr, *zero_b = nullptr;
   float eps = 0.f;
   int d = 1;
 };
