@@ -86,6 +86,54 @@ __global__ void rmsnorm_kernel(const T *__restrict__ x, const T *__restrict__ g,
   }
 }
 
+// Long rows: one CTA per row, each thread holding PT of its 16-byte vectors
+// (consecutive threads, consecutive vectors) in registers between the sum of
+// squares and the scaled store, so the row is read from memory once; the
+// warps' partial sums meet in shared memory.  Small CTAs keep many rows in
+// flight per SM.
+template <typename T, int PT>
+__global__ void __launch_bounds__(256) rmsnorm_row_cta_kernel(const T *__restrict__ x, const T *__restrict__ g,
+                                                              T *__restrict__ out, int d, float eps) {
+  constexpr int V = Vec16<T>::N;
+  __shared__ float part[8];
+  const T *xr = x + (size_t)blockIdx.x * d;
+  T *orow = out + (size_t)blockIdx.x * d;
+  const int nv = d / V;
+  Vec16<T> v[PT];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < PT; ++j) {
+    const int i = threadIdx.x + j * blockDim.x;
+    if (i < nv) {
+      v[j] = load16(xr + (size_t)i * V);
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        const float f = v[j].get(k);
+        ss = fmaf(f, f, ss);
+      }
+    }
+  }
+  ss = warp_sum(ss);
+  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  if ((threadIdx.x & 31) == 0) part[warp] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < nwarps; ++w) tot += part[w];
+  // "The Evolving Transformer 04 · LLaMA", §03 RMSNorm: x * rsqrt(mean(x^2) + eps) * g
+  const float r = rsqrtf(tot / (float)d + eps);
+#pragma unroll
+  for (int j = 0; j < PT; ++j) {
+    const int i = threadIdx.x + j * blockDim.x;
+    if (i < nv) {
+      const Vec16<T> gv = load16(g + (size_t)i * V);
+      Vec16<T> o;
+#pragma unroll
+      for (int k = 0; k < V; ++k) o.set(k, v[j].get(k) * r * gv.get(k));
+      store16(orow + (size_t)i * V, o);
+    }
+  }
+}
+
 template <typename T>
 cudaError_t launch_rmsnorm(const T *x, const T *g, T *out, int rows, int d, float eps, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
@@ -94,11 +142,29 @@ cudaError_t launch_rmsnorm(const T *x, const T *g, T *out, int rows, int d, floa
   const int nv = d / Vec16<T>::N;
   const int per_lane = (nv + 31) / 32;
   count_launch();
-  // Short rows stay in registers between the two halves of the computation.
-  // Longer rows (more than four 16-byte vectors per lane) are read twice, the
-  // second time from L2: a register-resident row of 16 vectors per lane needs
-  // ~150 registers, one 256-thread CTA per SM, too few loads in flight to keep
-  // HBM busy (measured at 8192 x 4096 bf16: 32 us resident vs 28 us re-read).
+  // Short rows (up to four 16-byte vectors per lane) stay in one warp's
+  // registers between the two halves of the computation.  Longer rows take a
+  // CTA each (rmsnorm_row_cta_kernel), again read once.  A warp holding a
+  // 4096-wide row in registers needed ~150 registers and one 256-thread CTA
+  // per SM, too few loads in flight (32 us at 8192 x 4096 bf16), and reading
+  // the row twice, the second time from L2, took 26.6 us.  Rows beyond 2048
+  // vectors are read twice (rmsnorm_kernel).
+  if (per_lane > 4 && nv <= 8 * 256) {
+    // one CTA per row: 128 threads up to 512 vectors, else 256 (at most 8 vectors each)
+    const int cta = nv <= 512 ? 128 : 256;
+    const int pt = (nv + cta - 1) / cta;
+    switch (pt) {
+      case 1: rmsnorm_row_cta_kernel<T, 1><<<rows, cta, 0, st>>>(x, g, out, d, eps); break;
+      case 2: rmsnorm_row_cta_kernel<T, 2><<<rows, cta, 0, st>>>(x, g, out, d, eps); break;
+      case 3: rmsnorm_row_cta_kernel<T, 3><<<rows, cta, 0, st>>>(x, g, out, d, eps); break;
+      case 4: rmsnorm_row_cta_kernel<T, 4><<<rows, cta, 0, st>>>(x, g, out, d, eps); break;
+      case 5: rmsnorm_row_cta_kernel<T, 5><<<rows, cta, 0, st>>>(x, g, out, d, eps); break;
+      case 6: rmsnorm_row_cta_kernel<T, 6><<<rows, cta, 0, st>>>(x, g, out, d, eps); break;
+      case 7: rmsnorm_row_cta_kernel<T, 7><<<rows, cta, 0, st>>>(x, g, out, d, eps); break;
+      default: rmsnorm_row_cta_kernel<T, 8><<<rows, cta, 0, st>>>(x, g, out, d, eps); break;
+    }
+    return cudaGetLastError();
+  }
   switch (per_lane) {
     case 1: rmsnorm_reg_kernel<T, 1><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
     case 2: rmsnorm_reg_kernel<T, 2><<<blocks, threads, 0, st>>>(x, g, out, rows, d, eps); break;
