@@ -602,7 +602,10 @@ def bench_standalone_ops(lb, torch, dev, stream, args, peaks):
     CUDA events on the launching stream, after a read of a buffer larger than L2,
     so that the operands come from HBM and L2 holds no dirty lines (after a
     write flush the launch would also pay for writing back up to 129 MB of the
-    flush buffer, as much as its own traffic); the median is reported."""
+    flush buffer, as much as its own traffic).  The event durations measured here
+    fall on steps of about 2 us (2.048 us), a tenth of these launches; a launch
+    starts at a random phase of that step, so the mean over the launches is
+    reported (the median is kept beside it: it moves in whole steps)."""
     T, d, H, G, D = 8192, SHAPE["d_model"], SHAPE["n_heads"], SHAPE["n_kv_heads"], SHAPE["d_model"] // SHAPE["n_heads"]
     g = torch.Generator(device=dev)
     g.manual_seed(3)
@@ -623,13 +626,13 @@ def bench_standalone_ops(lb, torch, dev, stream, args, peaks):
             torch.cuda.synchronize()
             times.append(e0.elapsed_time(e1) * 1e3)
         times.sort()
-        return times[len(times) // 2]
+        return sum(times) / len(times), times[len(times) // 2]
 
     x = torch.randn((T, d), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
     gain = (1 + 0.1 * torch.randn((d,), generator=g, device=dev, dtype=torch.float32)).to(torch.bfloat16)
     out = torch.empty_like(x)
     n0 = lb.llama_kernel_launch_count()
-    us_norm = timed(lambda: lb.check(lb.llama_op_rmsnorm(lb.LLAMA_BF16, x, gain, out, T, d, 1e-5, stream)))
+    us_norm, med_norm = timed(lambda: lb.check(lb.llama_op_rmsnorm(lb.LLAMA_BF16, x, gain, out, T, d, 1e-5, stream)))
     launches = lb.llama_kernel_launch_count() - n0
     norm_bytes = 2.0 * T * d * 2 + d * 2
     del x, out
@@ -641,17 +644,18 @@ def bench_standalone_ops(lb, torch, dev, stream, args, peaks):
     table = torch.empty((T, D // 2, 2), device=dev, dtype=torch.float32)
     lb.check(lb.llama_op_rope_table(table, T, D, SHAPE["rope_theta"], None, stream))
     n0 = lb.llama_kernel_launch_count()
-    us_rope = timed(lambda: lb.check(lb.llama_op_rope_kv_write(lb.LLAMA_BF16, qkv, q_out, kv, table, T, 1, T, 0, H, G,
+    us_rope, med_rope = timed(lambda: lb.check(lb.llama_op_rope_kv_write(lb.LLAMA_BF16, qkv, q_out, kv, table, T, 1, T, 0, H, G,
                                                                D, 0, stream)))
     launches += lb.llama_kernel_launch_count() - n0
     rope_bytes = T * (H + 2 * G) * D * 2.0 + T * H * D * 2.0 + 2.0 * T * G * D * 2
     torch.cuda.synchronize()
-    return {"rmsnorm_8192x4096": {"us": us_norm, "gbs": norm_bytes / us_norm / 1e3,
+    return {"rmsnorm_8192x4096": {"us": us_norm, "us_median": med_norm, "gbs": norm_bytes / us_norm / 1e3,
                                   "hbm_frac": norm_bytes / us_norm / 1e3 / hbm, "algorithmic_bytes": norm_bytes},
-            "rope_kv_write_b1s8192": {"us": us_rope, "gbs": rope_bytes / us_rope / 1e3,
+            "rope_kv_write_b1s8192": {"us": us_rope, "us_median": med_rope, "gbs": rope_bytes / us_rope / 1e3,
                                       "hbm_frac": rope_bytes / us_rope / 1e3 / hbm, "algorithmic_bytes": rope_bytes},
             "hbm_peak_gbs": hbm, "gpu_launches": launches,
-            "timing": "median of single launches, L2 flushed before each by reading a 512 MB buffer"}
+            "timing": f"mean of {n} single launches (event durations come in steps of about 2 us), L2 flushed "
+                      "before each by reading a 512 MB buffer"}
 
 
 def bench_stack(lb, torch, dev, stream, args, n_layers=32, vocab=128256, S=8192):
