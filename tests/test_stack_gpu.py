@@ -110,3 +110,40 @@ def test_llama3_8b_shaped_two_layer_stack_bf16(lb):
     assert_stack_parity(logits, ref, "logits (8B-shaped layers)")
     assert_parity(caches[0][0][:, :, :S], ref_caches[0][0][:, :, :S], "bf16", "K cache layer 0")
     assert_stack_parity(caches[1][0][:, :, :S], ref_caches[1][0][:, :, :S], "K cache layer 1")
+
+
+def test_odd_layer_stack_repeated_and_continued_through_one_handle_bf16(lb):
+    """A bf16 stack hands each block's row statistics to the next through two
+    alternating buffers that the consuming epilogues clear.  With an odd layer
+    count the buffers end a forward in a different state than they start it, so
+    one handle runs the same prefill twice and then a one-token step per
+    sequence, each against the oracle."""
+    t = torch()
+    s = dict(synth.SHAPES["smollm2_135m"], max_seq_len=64)
+    B, S, L, vocab, n = 2, 40, 64, 4096, 3
+    layers, embed, head, fnorm, tokens, caches = _stack_inputs(s, n, vocab, B, S, L)
+    nxt = synth.uniform_int(0, "next_tokens", (B, 1), vocab)
+    ref, ref_caches = _oracle(s, layers, embed, head, fnorm, tokens, caches, 0)
+    ref2, _ = _oracle(s, layers, embed, head, fnorm, nxt, ref_caches, S)
+    wd = [{k: to_dev(v) for k, v in w.items()} for w in layers]
+    st, stk = lb.llama_stack_create(make_cfg(s, L), n, vocab, to_dev(embed), [lb.make_weights(w) for w in wd],
+                                    to_dev(fnorm), to_dev(head), B * S)
+    lb.check(st, "llama_stack_create")
+    try:
+        kvd = [(to_dev(k), to_dev(v)) for k, v in caches]
+        kvs = [lb.make_kv_cache(k, v, B, L) for k, v in kvd]
+        stream = t.cuda.current_stream()
+        tok = t.from_numpy(tokens).cuda()
+        for rep in range(2):
+            logits = t.empty((B, S, vocab), dtype=t.float32, device="cuda")
+            lb.check(lb.llama_stack_forward(stk, tok, B, S, 0, kvs, logits, stream))
+            t.cuda.synchronize()
+            assert lb.llama_stack_device_status(stk) == lb.LLAMA_OK
+            assert_stack_parity(logits.cpu().numpy().astype(np.float64), ref, f"prefill logits, forward {rep + 1}")
+        logits = t.empty((B, 1, vocab), dtype=t.float32, device="cuda")
+        lb.check(lb.llama_stack_forward(stk, t.from_numpy(nxt).cuda(), B, 1, S, kvs, logits, stream))
+        t.cuda.synchronize()
+        assert lb.llama_stack_device_status(stk) == lb.LLAMA_OK
+        assert_stack_parity(logits.cpu().numpy().astype(np.float64), ref2, "one-token step logits")
+    finally:
+        lb.llama_stack_destroy(stk)
