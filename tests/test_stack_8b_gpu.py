@@ -1,0 +1,107 @@
+"""Parity of the configured Llama-3-8B stack: 32 blocks, a 128256-entry
+vocabulary and an untied LM head ([EVT] §07 Assemble; [L3B] Overview, 32
+layers), through llama_stack_forward, against the fp64 oracle (GPU).
+
+The prompt is short (B = 1, S = 64) so that the oracle finishes quickly; every
+layer, the full vocabulary and the LM-head GEMM are the configured ones.  The
+weights are drawn one layer at a time: each layer's bf16 bits go to the
+device, its fp64 copy feeds the oracle (and the bf16 storage model) and is
+dropped, so host memory holds about one layer in fp64.
+
+Bars.  The first layer's cache is held to the single-block bf16 bars.  The
+logits and the last layer's cache of a 32-deep bf16 stack cannot meet those:
+rounding every stored value to bf16 (the model in _bf16_storage.py, which is
+what any bf16 tensor-core stack does) already puts the logits several percent
+from the exact result at this depth -- each block adds a fresh error of about
+0.8 % of the residual stream, and keeping the residual stream in fp32 removes
+only about a tenth of it.  So the library must land within twice the error of
+that storage model, evaluated here on the same weights and tokens.
+"""
+import numpy as np
+import pytest
+
+import _bf16_storage as bfs
+import oracle
+import synth
+from _helpers import assert_parity, make_cfg, parity_errors, to_dev, to_f64, torch
+
+pytestmark = pytest.mark.gpu
+
+N_LAYERS, VOCAB, B, S = 32, 128256, 1, 64
+
+
+@pytest.fixture(scope="module")
+def lb():
+    import decoder_block_gb300 as m
+    m.load()
+    return m
+
+
+def test_llama3_8b_stack_32_layers_full_vocabulary(lb):
+    t = torch()
+    s = dict(synth.SHAPES["llama3_8b_prefill_b1s8192"], max_seq_len=S)
+    d, G, D = s["d_model"], s["n_kv_heads"], s["d_model"] // s["n_heads"]
+    tokens = synth.uniform_int(0, "tokens", (B, S), VOCAB)
+    embed = synth.f32_to_bf16_bits(synth.normal(0, "embed", (VOCAB, d), std=0.02))
+    head = synth.f32_to_bf16_bits(synth.normal(0, "lm_head", (VOCAB, d), std=0.02))
+    fnorm = synth.f32_to_bf16_bits(synth.normal(0, "final_norm", (d,), std=0.1, mean=1.0))
+    embed64, head64, fnorm64 = synth.as_f64(embed), synth.as_f64(head), synth.as_f64(fnorm)
+
+    dev_layers = []
+    model = {}
+
+    def layers():
+        # one layer at a time: device copy for the library, fp64 copy for the
+        # oracle and the storage model
+        x_model = embed64[tokens]
+        for l in range(N_LAYERS):
+            w = synth.block_weights(s, layer=l)
+            dev_layers.append({k: to_dev(v) for k, v in w.items()})
+            w64 = {k: synth.as_f64(v) for k, v in w.items()}
+            del w
+            x_model, km, vm = bfs.block(s, w64, x_model)
+            model[l] = (km.transpose(0, 2, 1, 3), vm.transpose(0, 2, 1, 3))
+            yield w64
+        model["logits"] = bfs.logits(s, x_model, fnorm64, head64)
+
+    empty = np.zeros((B, G, S, D))
+    ref, ref_caches = oracle.stack_forward(s, layers(), embed64, fnorm64, head64, tokens, 0,
+                                           [(empty, empty)] * N_LAYERS)
+    del embed64, head64
+
+    st, stk = lb.llama_stack_create(make_cfg(s, S), N_LAYERS, VOCAB, to_dev(embed),
+                                    [lb.make_weights(w) for w in dev_layers], to_dev(fnorm), to_dev(head), B * S)
+    lb.check(st, "llama_stack_create")
+    dev_layers.clear()  # the library holds its own copies
+    try:
+        zeros = lambda: t.zeros((B, G, S, D), dtype=t.bfloat16, device="cuda")
+        kvd = [(zeros(), zeros()) for _ in range(N_LAYERS)]
+        kvs = [lb.make_kv_cache(k, v, B, S) for k, v in kvd]
+        tok = t.from_numpy(tokens).cuda()
+        logits = t.empty((B, S, VOCAB), dtype=t.float32, device="cuda")
+        lb.check(lb.llama_stack_forward(stk, tok, B, S, 0, kvs, logits, t.cuda.current_stream()))
+        t.cuda.synchronize()
+        assert lb.llama_stack_device_status(stk) == lb.LLAMA_OK
+        got = logits.cpu().numpy().astype(np.float64)
+        caches = {l: (to_f64(kvd[l][0]), to_f64(kvd[l][1])) for l in (0, N_LAYERS - 1)}
+    finally:
+        lb.llama_stack_destroy(stk)
+
+    assert np.all(np.isfinite(got))
+    fro, mx = parity_errors(got, ref)
+    fro_m, mx_m = parity_errors(model["logits"], ref)
+    fro_gm, _ = parity_errors(got, model["logits"])
+    print(f"\n32-layer 8B stack logits: rel-Frobenius {fro:.3e}, max|err|/max|ref| {mx:.3e}; "
+          f"bf16 storage model {fro_m:.3e} / {mx_m:.3e}; library vs model {fro_gm:.3e}")
+    assert fro <= 2.0 * fro_m and mx <= 2.0 * mx_m, (fro, mx, fro_m, mx_m)
+
+    k0, v0 = caches[0]
+    assert_parity(k0, ref_caches[0][0], "bf16", "layer 0 K cache")
+    assert_parity(v0, ref_caches[0][1], "bf16", "layer 0 V cache")
+    last = N_LAYERS - 1
+    for name, got_c, ref_c, model_c in (("K", caches[last][0], ref_caches[last][0], model[last][0]),
+                                        ("V", caches[last][1], ref_caches[last][1], model[last][1])):
+        f, m = parity_errors(got_c, ref_c)
+        fm, mm = parity_errors(model_c, ref_c)
+        print(f"layer {last} {name} cache: rel-Frobenius {f:.3e} (model {fm:.3e}), max {m:.3e} (model {mm:.3e})")
+        assert f <= 2.0 * fm and m <= 2.0 * mm, (name, f, m, fm, mm)

@@ -1,82 +1,60 @@
 """Derivation of the stack-logits tolerance (CPU).
 
-A bf16 tensor-core stack rounds values to bf16 wherever it stores them.  In
-this library's bf16 path those points are: the RMSNorm gains folded into the
-weights they feed (bf16(W * g), once at create time; the normalised
-activations themselves are never stored -- the row scale is applied to the
-fp32 accumulator), q and k after RoPE and v (one rounding each, from the fp32
-accumulator), P before the PV product, the attention output o, the SwiGLU
-product, and the residual stream h and y.  This test replays the oracle's
-exact arithmetic with a bf16 rounding at each of those storage points (a model
-of the storage precision, not of any kernel) and measures how far the logits
-land from the exact fp64 oracle.  For two Llama-3-8B-shaped layers that
+A bf16 tensor-core stack rounds values to bf16 wherever it stores them (the
+points are listed in _bf16_storage.py).  Replaying the oracle's exact
+arithmetic with a bf16 rounding at each of those points (a model of the
+storage precision, not of any kernel) shows how far a correct bf16 stack's
+logits land from the exact fp64 oracle.  For two Llama-3-8B-shaped layers that
 inherent error is about 1 % relative Frobenius -- above the 5e-3 bar that holds
-for a single block -- so the stack's logits are compared with
-STACK_LOGITS_FRO_REL = 2.5e-2, at least twice the emulated error; the max-error
-bar (3e-2 max|ref|) is unchanged.
+for a single block -- so multi-layer stacks of up to a few layers are compared
+with STACK_LOGITS_FRO_REL = 2.5e-2, at least twice the emulated error; the
+max-error bar (3e-2 max|ref|) is unchanged.  Keeping the residual stream in
+fp32 between the branches and blocks does not bring the error under 5e-3
+either: the rounding of the GEMM operands, of the folded weights, of q, k, v,
+P and of the SwiGLU product is what carries it.  Deeper stacks (the 32-layer
+8B stack) take their bar from the same model evaluated at their own depth
+(test_stack_8b_gpu.py).
 """
-import math
-
 import numpy as np
 
+import _bf16_storage as bfs
 import oracle
 import synth
 
 STACK_LOGITS_FRO_REL = 2.5e-2
 
 
-def _bf(a):
-    return synth.as_f64(synth.f32_to_bf16_bits(np.asarray(a, dtype=np.float32)))
-
-
-def _rms(x, g, eps):
-    return x / np.sqrt(np.mean(x * x, -1, keepdims=True) + eps) * g
-
-
-def _block_bf16_storage(cfg, w, x):
-    """The block with every stored value rounded to bf16 (start_pos = 0)."""
-    d, H, G = cfg["d_model"], cfg["n_heads"], cfg["n_kv_heads"]
-    D, r = d // H, H // G
-    B, S, _ = x.shape
-    eps = cfg["norm_eps"]
-    rs = 1.0 / np.sqrt(np.mean(x * x, -1, keepdims=True) + eps)  # RMSNorm row scale, applied after the GEMM
-    g1 = w["attn_norm"]
-    pos = np.arange(S)
-    q = _bf(oracle.rope((rs * (x @ _bf(w["wq"] * g1).T)).reshape(B, S, H, D), pos, cfg["rope_theta"]))
-    k = _bf(oracle.rope((rs * (x @ _bf(w["wk"] * g1).T)).reshape(B, S, G, D), pos, cfg["rope_theta"]))
-    v = _bf(rs * (x @ _bf(w["wv"] * g1).T)).reshape(B, S, G, D)
-    o = np.zeros((B, S, H, D))
-    vis = np.arange(S)[None, :] <= np.arange(S)[:, None]
-    for b in range(B):
-        for h in range(H):
-            sc = np.where(vis, q[b, :, h] @ k[b, :, h // r].T / math.sqrt(D), -np.inf)
-            p = np.exp(sc - sc.max(-1, keepdims=True))
-            o[b, :, h] = (_bf(p) @ v[b, :, h // r]) / p.sum(-1, keepdims=True)
-    hres = _bf(x + _bf(o.reshape(B, S, H * D)) @ w["wo"].T)
-    rs2 = 1.0 / np.sqrt(np.mean(hres * hres, -1, keepdims=True) + eps)
-    g2 = w["ffn_norm"]
-    gt, up = rs2 * (hres @ _bf(w["w_gate"] * g2).T), rs2 * (hres @ _bf(w["w_up"] * g2).T)
-    return _bf(hres + _bf(gt / (1 + np.exp(-gt)) * up) @ w["w_down"].T)
-
-
-def test_bf16_storage_error_of_a_two_layer_8b_stack_sets_the_logits_bar():
+def _two_layer_8b(residual_f32):
     s = dict(synth.SHAPES["llama3_8b_prefill_b1s8192"], max_seq_len=40)
     B, S, vocab, n = 1, 40, 2048, 2
     layers = [{k: synth.as_f64(v) for k, v in synth.block_weights(s, layer=l).items()} for l in range(n)]
-    embed = _bf(synth.normal(0, "embed", (vocab, s["d_model"]), std=0.02))
-    head = _bf(synth.normal(0, "lm_head", (vocab, s["d_model"]), std=0.02))
-    fnorm = _bf(synth.normal(0, "final_norm", (s["d_model"],), std=0.1, mean=1.0))
+    embed = bfs.bf(synth.normal(0, "embed", (vocab, s["d_model"]), std=0.02))
+    head = bfs.bf(synth.normal(0, "lm_head", (vocab, s["d_model"]), std=0.02))
+    fnorm = bfs.bf(synth.normal(0, "final_norm", (s["d_model"],), std=0.1, mean=1.0))
     tokens = synth.uniform_int(0, "tokens", (B, S), vocab)
     kc = np.zeros((B, s["n_kv_heads"], S, s["d_model"] // s["n_heads"]))
     ref, _ = oracle.stack_forward(s, layers, embed, fnorm, head, tokens, 0, [(kc, kc)] * n)
-    x = embed[tokens]
-    for w in layers:
-        x = _block_bf16_storage(s, w, x)
-    emu = _bf(_rms(x, fnorm, s["norm_eps"])) @ head.T
-    err = float(np.linalg.norm(emu - ref) / np.linalg.norm(ref))
-    print(f"emulated bf16-storage logits error: {err:.3e} relative Frobenius")
+    out = {}
+    for mode in residual_f32:
+        x = embed[tokens]
+        for w in layers:
+            x, _, _ = bfs.block(s, w, x, residual_f32=mode)
+        emu = bfs.logits(s, x, fnorm, head)
+        out[mode] = (float(np.linalg.norm(emu - ref) / np.linalg.norm(ref)),
+                     float(np.max(np.abs(emu - ref)) / np.max(np.abs(ref))))
+    return out
+
+
+def test_bf16_storage_error_of_a_two_layer_8b_stack_sets_the_logits_bar():
+    errs = _two_layer_8b((False, True))
+    err, mx = errs[False]
+    err32, _ = errs[True]
+    print(f"emulated bf16-storage logits error: {err:.3e} relative Frobenius "
+          f"({err32:.3e} with an fp32 residual stream)")
     # the storage precision alone exceeds the single-block bar ...
     assert err > 5e-3
+    # ... an fp32 residual stream does not change that ...
+    assert err32 > 5e-3
     # ... and the stack bar leaves at least a factor two above it
     assert 2.0 * err <= STACK_LOGITS_FRO_REL
-    assert float(np.max(np.abs(emu - ref)) / np.max(np.abs(ref))) < 3e-2
+    assert mx < 3e-2
