@@ -87,6 +87,8 @@ def load() -> ctypes.CDLL:
         "llama_block_device_status": (st, [c_void_p]),
         "llama_block_set_decode_mode": (st, [c_void_p, c_int32]),
         "llama_stack_set_decode_mode": (st, [c_void_p, c_int32]),
+        "llama_block_set_wait_budget": (st, [c_void_p, ctypes.c_int64]),
+        "llama_stack_set_wait_budget": (st, [c_void_p, ctypes.c_int64]),
         "llama_stack_create": (st, [POINTER(llama_config), c_int32, c_int32, c_void_p, POINTER(llama_block_weights),
                                     c_void_p, c_void_p, c_int32, POINTER(c_void_p)]),
         "llama_stack_generate": (st, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
@@ -195,6 +197,14 @@ def llama_block_set_decode_mode(blk, mode: int) -> int:
 
 def llama_stack_set_decode_mode(stk, mode: int) -> int:
     return load().llama_stack_set_decode_mode(stk, mode)
+
+
+def llama_block_set_wait_budget(blk, cycles: int) -> int:
+    return load().llama_block_set_wait_budget(blk, cycles)
+
+
+def llama_stack_set_wait_budget(stk, cycles: int) -> int:
+    return load().llama_stack_set_wait_budget(stk, cycles)
 
 
 def llama_stack_create(cfg: llama_config, n_layers, vocab, embed, layers, final_norm, lm_head, max_tokens):

@@ -218,13 +218,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       }
       // Drain: every issued copy must land before the CTA exits (at most one Q
       // load and the ring's last KV_STAGES key tiles can be outstanding).
-      int dummy = 0;
-      if (items > 0) ptx::mbar_wait(q_full, (items - 1) & 1, &dummy, a.status, DEV_TIMEOUT_PRODUCER);
+      if (items > 0) ptx::mbar_drain(q_full, (items - 1) & 1, a.status, DEV_TIMEOUT_PRODUCER);
       for (int j = max(0, issued / 2 - KV_STAGES); j < (issued + 1) / 2; ++j) {
         const int st = j % KV_STAGES;
         const uint32_t ph = (j / KV_STAGES) & 1;
-        ptx::mbar_wait(k_full(st), ph, &dummy, a.status, DEV_TIMEOUT_PRODUCER);
-        if (2 * j + 1 < issued) ptx::mbar_wait(v_full(st), ph, &dummy, a.status, DEV_TIMEOUT_PRODUCER);
+        ptx::mbar_drain(k_full(st), ph, a.status, DEV_TIMEOUT_PRODUCER);
+        if (2 * j + 1 < issued) ptx::mbar_drain(v_full(st), ph, a.status, DEV_TIMEOUT_PRODUCER);
       }
     }
   } else if (warp == 1) {
@@ -306,8 +305,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         jg += n_kv;
       }
       ptx::mma_commit(fin);
-      int dummy = 0;
-      ptx::mbar_wait(fin, 0, &dummy, a.status, DEV_TIMEOUT_MMA);
+      ptx::mbar_drain(fin, 0, a.status, DEV_TIMEOUT_MMA);
     }
   } else {
     // ---------------------------------------------------------- softmax ---
@@ -504,10 +502,9 @@ template <int D>
 cudaError_t launch_prefill(const bf16 *q, const bf16 *kc, const bf16 *vc, bf16 *o, int B, int S, int start_pos,
                            int H, int G, int cache_seq, int *status, cudaStream_t st) {
   using L = AttnLayout<D>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
+  static PerContextOnce attr;
+  const cudaError_t attr_err = attr.run([] {
+    return cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int r = H / G;

@@ -5,6 +5,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <vector>
+
 namespace llama {
 
 typedef __nv_bfloat16 bf16;
@@ -28,6 +31,32 @@ enum DeviceStatusCode : int {
 void note_cuda_error(cudaError_t e);
 // Counts one kernel launch (library-wide total, read by llama_kernel_launch_count).
 void count_launch();
+// Identifier of the CUDA context current on the calling thread, unique within
+// the process (a context created after a device reset gets a new one); 0 when
+// no context is current or the driver cannot tell.
+unsigned long long current_context_id();
+
+// Runs a per-context set-up (a kernel's shared-memory limit, a symbol's device
+// address) once in every CUDA context it is needed in: each device has its own
+// context, and a device reset replaces it.  Until the set-up has succeeded in
+// the current context it is run again on the next call.
+class PerContextOnce {
+ public:
+  template <typename F> cudaError_t run(F &&init) {
+    const unsigned long long id = current_context_id();
+    std::lock_guard<std::mutex> lock(mutex_);
+    if (id != 0)
+      for (unsigned long long done : done_)
+        if (done == id) return cudaSuccess;
+    const cudaError_t e = init();
+    if (e == cudaSuccess && id != 0) done_.push_back(id);
+    return e;
+  }
+
+ private:
+  std::mutex mutex_;
+  std::vector<unsigned long long> done_;
+};
 
 __device__ __forceinline__ void report_status(int *status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
@@ -112,5 +141,23 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // Budget for a bounded spin on an mbarrier or flag, in SM clock cycles
 // (about 2 s at 2 GHz); long enough that no legitimate wait reaches it.
 constexpr long long kWaitBudgetCycles = 4000000000LL;
+
+// A handle's device status block.  The `int *status` the kernels receive
+// points at `code` (or is null).  `wait_budget` is set from the host
+// (llama_block_set_wait_budget / llama_stack_set_wait_budget): it bounds, in
+// SM clock cycles, every wait that gives up (0 means kWaitBudgetCycles).
+// Waits that drain copies and MMAs already in flight before a CTA reuses their
+// memory or exits (ptx::mbar_drain) always use kWaitBudgetCycles.
+struct DeviceStatus {
+  int code;
+  int reserved;
+  long long wait_budget;
+};
+
+__device__ __forceinline__ long long wait_budget(const int *status) {
+  if (status == nullptr) return kWaitBudgetCycles;
+  const long long b = __ldg(&reinterpret_cast<const DeviceStatus *>(status)->wait_budget);
+  return b > 0 ? b : kWaitBudgetCycles;
+}
 
 }  // namespace llama

@@ -110,8 +110,9 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(DecArgs a) {
     ptx::bulk_load(s0 + s * L::STAGE + DEC_SUB * L::ROW, vg + (size_t)j * DEC_SUB * D, bytes, full(s));
   };
   volatile int abort_local = 0;
+  int issued = 0;  // thread 0: sub-tiles whose copies have been issued
   if (threadIdx.x == 0)
-    for (int j = 0; j < min(DEC_STAGES, n_sub); ++j) issue(j);
+    for (; issued < min(DEC_STAGES, n_sub); ++issued) issue(issued);
 
   float m_h = -INFINITY, l_h = 0.f;  // softmax state of this lane's head (lane % RP)
   float o[RP][L::EPL];
@@ -216,11 +217,19 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(DecArgs a) {
     if (lane == 0) ptx::mbar_arrive(empty(s));
     // refill this stage with sub-tile j + DEC_STAGES once every warp released it
     if (threadIdx.x == 0 && j + DEC_STAGES < n_sub) {
-      if (ptx::mbar_wait(empty(s), (j / DEC_STAGES) & 1, &abort_local, a.status, DEV_TIMEOUT_PRODUCER))
+      if (ptx::mbar_wait(empty(s), (j / DEC_STAGES) & 1, &abort_local, a.status, DEV_TIMEOUT_PRODUCER)) {
         issue(j + DEC_STAGES);
+        ++issued;
+      }
     }
   }
-  // All issued copies have been waited for by the consumers (or the wait gave up).
+  // A consumer whose wait gave up leaves copies in flight: they land before the
+  // stage buffers are reused below (or the CTA exits).  Sub-tile j + DEC_STAGES
+  // is issued only once every warp has consumed sub-tile j, so only the last
+  // DEC_STAGES issued copies can still be outstanding.
+  if (threadIdx.x == 0)
+    for (int j = max(0, issued - DEC_STAGES); j < issued; ++j)
+      ptx::mbar_drain(full(j % DEC_STAGES), (j / DEC_STAGES) & 1, a.status, DEV_TIMEOUT_ATTN);
   __syncthreads();
   // ------------------------------------------------------------- merge ---
   // Reuse the stage buffers: per warp [RP][D] o, then [RP] m and l.
@@ -275,10 +284,9 @@ __global__ void __launch_bounds__(D) attn_decode_combine(const float *__restrict
 template <int D, int RP>
 cudaError_t launch_dec(const DecArgs &base, int B, const AttnScratch &scratch, cudaStream_t st) {
   using L = DecLayout<D, RP>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_decode_kernel<D, RP>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
+  static PerContextOnce attr;
+  const cudaError_t attr_err = attr.run([] {
+    return cudaFuncSetAttribute(attn_decode_kernel<D, RP>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const size_t per_seq = (size_t)base.H * base.n_split * (D + 2) * sizeof(float);

@@ -249,14 +249,17 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
 }
 
 int fused_grid() {
+  static PerContextOnce attr;
+  if (attr.run([] {
+        return cudaFuncSetAttribute(decode_block_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    FUSED_SMEM);
+      }) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
   static std::once_flag once;
   static int grid = 0;
   std::call_once(once, [] {
-    if (cudaFuncSetAttribute(decode_block_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FUSED_SMEM) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      return;
-    }
     int dev = 0, sms = 0, coop = 0, per_sm = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -88,17 +88,17 @@ cudaError_t attn_decode_tc_prepare(const bf16 *q, const bf16 *kc, const bf16 *vc
 cudaError_t launch_attn_decode_tc(const bf16 *q, const bf16 *kc, const bf16 *vc, bf16 *o, int B, int start_pos,
                                   int H, int G, int cache_seq, const AttnScratch &scratch, int *status,
                                   cudaStream_t st) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_decode_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    DtLayout::BYTES);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(attn_decode_tc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      DtLayout::BYTES);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(attn_decode_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      DtLayout::BYTES);
+  static PerContextOnce attr;
+  const cudaError_t attr_err = attr.run([] {
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DtLayout::BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_decode_tc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               DtLayout::BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_decode_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               DtLayout::BYTES);
+    return e;
   });
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap mq, mk, mv;

@@ -218,10 +218,9 @@ __device__ __forceinline__ void attn_decode_tc_run(const CUtensorMap *tmQ, const
         }
       }
       // drain the last issued loads
-      int dummy = 0;
       for (int t = max(0, tile - DT_STAGES); t < tile; ++t)
-        ptx::mbar_wait(kv_full(t % DT_STAGES), (t / DT_STAGES) & 1, &dummy, a.status, DEV_TIMEOUT_PRODUCER);
-      if (nq > 0) ptx::mbar_wait(q_full((nq - 1) & 1), ((nq - 1) >> 1) & 1, &dummy, a.status, DEV_TIMEOUT_PRODUCER);
+        ptx::mbar_drain(kv_full(t % DT_STAGES), (t / DT_STAGES) & 1, a.status, DEV_TIMEOUT_PRODUCER);
+      if (nq > 0) ptx::mbar_drain(q_full((nq - 1) & 1), ((nq - 1) >> 1) & 1, a.status, DEV_TIMEOUT_PRODUCER);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -286,8 +285,7 @@ __device__ __forceinline__ void attn_decode_tc_run(const CUtensorMap *tmQ, const
         ptx::mma_commit(o_full(ob));
       }
       ptx::mma_commit(fin);
-      int dummy = 0;
-      ptx::mbar_wait(fin, 0, &dummy, a.status, DEV_TIMEOUT_MMA);
+      ptx::mbar_drain(fin, 0, a.status, DEV_TIMEOUT_MMA);
     }
   } else {
     // ------------------------------------------------- softmax / epilogue ---

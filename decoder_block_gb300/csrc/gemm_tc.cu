@@ -98,11 +98,10 @@ bool cluster_split_fits_bn(int bn, int tiles, int splits, int units) {
 template <int EPI, int BN, bool GROUPED = false>
 cudaError_t launch_cfg(const CUtensorMap &ma, const CUtensorMap &mb, GemmArgs args, cudaStream_t st) {
   using G = GemmCfg<BN>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<EPI, BN, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    G::SMEM_BYTES);
+  static PerContextOnce smem_limit;
+  const cudaError_t attr_err = smem_limit.run([] {
+    return cudaFuncSetAttribute(gemm_tc_kernel<EPI, BN, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                G::SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
   int grid = sm_count();

@@ -644,10 +644,8 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
         }
       }
       // Every issued copy must have landed before the CTA can exit.
-      for (int j = it - STAGES < 0 ? 0 : it - STAGES; j < it; ++j) {
-        int dummy = 0;
-        ptx::mbar_wait(full_bar(j % STAGES), (j / STAGES) & 1, &dummy, args.status, DEV_TIMEOUT_PRODUCER);
-      }
+      for (int j = it - STAGES < 0 ? 0 : it - STAGES; j < it; ++j)
+        ptx::mbar_drain(full_bar(j % STAGES), (j / STAGES) & 1, args.status, DEV_TIMEOUT_PRODUCER);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -683,8 +681,7 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
       }
       // Wait until every issued MMA has finished before TMEM / smem go away.
       ptx::mma_commit(fin_bar);
-      int dummy = 0;
-      ptx::mbar_wait(fin_bar, 0, &dummy, args.status, DEV_TIMEOUT_MMA);
+      ptx::mbar_drain(fin_bar, 0, args.status, DEV_TIMEOUT_MMA);
     }
   } else {
     // the epilogue reads R / row statistics and writes C

@@ -9,11 +9,12 @@
 // library image carries, instead of caller- or library-allocated memory.
 //
 // The array is part of the loaded library on every GPU that uses it and stays
-// resident until the process exits.  Its device address is looked up once
-// per device, on the first call made with that device current; make that
-// first call before any stream capture.  All calls share the one array, so
-// calls whose kernels could run at the same time on the GPU (different
-// streams without ordering between them) race on it.
+// resident until the process exits.  Its device address is looked up once per
+// CUDA context -- on the first call made with a device current, and again
+// after that device's context was reset -- so make the first call on each
+// device before any stream capture.  All calls share the one array, so calls
+// whose kernels could run at the same time on the GPU (different streams
+// without ordering between them) race on it.
 #include <mutex>
 
 #include "llama_ops.h"
@@ -26,24 +27,40 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_decode_scratch[LLAMA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
+// The array's device address in each CUDA context that has used it.  A
+// device reset ends the context and unloads the library image from it; the
+// context created after it has another identifier, so the address is looked
+// up again instead of reusing a stale one.
+struct ScratchAddress {
+  unsigned long long context;
+  void *ptr;
+};
+constexpr int kMaxContexts = 64;
 std::mutex g_setup_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
+ScratchAddress g_scratch[kMaxContexts] = {};
+int g_scratch_n = 0;
 
-// Device address of g_decode_scratch on the current device (set-up on first use).
+// Device address of g_decode_scratch in the current context (set-up on first use).
 llama_status scratch_address(void **out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LLAMA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return LLAMA_ERR_CUDA;
-    }
-    g_scratch_ptr[dev] = p;
+  unsigned long long ctx = current_context_id();
+  if (ctx != 0)
+    for (int i = 0; i < g_scratch_n; ++i)
+      if (g_scratch[i].context == ctx) {
+        *out = g_scratch[i].ptr;
+        return LLAMA_OK;
+      }
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return LLAMA_ERR_CUDA;
   }
-  *out = g_scratch_ptr[dev];
+  ctx = current_context_id();  // the look-up makes a context current if none was
+  if (ctx != 0) {
+    if (g_scratch_n == kMaxContexts) g_scratch_n = 0;  // many resets: start the table over
+    g_scratch[g_scratch_n++] = ScratchAddress{ctx, p};
+  }
+  *out = p;
   return LLAMA_OK;
 }
 
@@ -67,9 +84,12 @@ extern "C" llama_status llama_op_attention_decode_noalloc(const void *q, const l
   if (H % G != 0) return LLAMA_ERR_SHAPE;
   if (!attn_decode_supported(H, G, D)) return LLAMA_ERR_UNSUPPORTED;
   if (B > kv->max_batch || (long long)start_pos + 1 > kv->max_seq_len) return LLAMA_ERR_RANGE;
-  // Partials: B x H x ceil((start_pos + 1) / 256) chunks x (D + 2) floats; one kernel launch must hold them all.
-  const size_t need = (size_t)B * H * (size_t)((start_pos + 1 + 255) / 256) * (D + 2) * sizeof(float);
-  if (need > (size_t)LLAMA_NOALLOC_SCRATCH_BYTES) return LLAMA_ERR_RANGE;
+  // Partials: H x ceil((start_pos + 1) / 256) chunks x (D + 2) floats per sequence; with a single chunk the
+  // kernel writes o directly and uses none.  Batches whose partials exceed the array run in groups of
+  // sequences, one group after another on the stream, each reusing it: one sequence's partials must fit.
+  const size_t n_split = (size_t)((start_pos + 1 + 255) / 256);
+  const size_t per_seq = n_split > 1 ? (size_t)H * n_split * (D + 2) * sizeof(float) : 0;
+  if (per_seq > (size_t)LLAMA_NOALLOC_SCRATCH_BYTES) return LLAMA_ERR_RANGE;
   for (const void *p : {q, (const void *)kv->k, (const void *)kv->v, (const void *)o}) {
     llama_status c = check_ptr(p);
     if (c != LLAMA_OK) return c;

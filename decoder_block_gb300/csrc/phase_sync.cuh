@@ -44,9 +44,10 @@ __device__ __forceinline__ bool phase_wait(const PhaseSync &s, int *status) {
     return true;
   }
   const long long t0 = clock64();
+  const long long budget = wait_budget(status);
   while (ld_acquire_gpu(s.arrivals) < s.target) {
     if (*(volatile unsigned *)(s.arrivals + 1) != 0u) return false;
-    if (clock64() - t0 > kWaitBudgetCycles) {
+    if (clock64() - t0 > budget) {
       report_status(status, DEV_TIMEOUT_PHASE);
       atomicExch(s.arrivals + 1, 1u);
       return false;

@@ -83,19 +83,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Gives up when
-// *abort becomes non-zero (another role gave up) or after kWaitBudgetCycles,
+// *abort becomes non-zero (another role gave up) or after the handle's wait
+// budget (wait_budget(status), kWaitBudgetCycles unless the host set one),
 // recording `code` in the status word; returns false when it gave up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort, int *status,
                                           int code) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
+  const long long budget = wait_budget(status);
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitBudgetCycles) {
+    if (clock64() - t0 > budget) {
       *abort = 1;
       report_status(status, code);
       return false;
+    }
+  }
+}
+
+// Wait for copies or MMAs that this CTA already issued (tracked by the phase
+// with the given parity) before their memory is reused or the CTA exits.  It
+// ignores other roles giving up and is bounded by kWaitBudgetCycles whatever
+// the handle's wait budget, so that a short budget never lets a CTA leave an
+// asynchronous operation behind.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, int *status, int code) {
+  if (mbar_try_wait(bar, parity)) return;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitBudgetCycles) {
+      report_status(status, code);
+      return;
     }
   }
 }

@@ -18,10 +18,13 @@
 // QKV epilogue also applies RoPE and writes k and v into the cache (step 3 in
 // the same kernel as step 2, for d_head % 32 == 0).  The fp32 path keeps the
 // standalone steps.
+#include <cuda.h>
+
 #include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include "llama_block.h"
@@ -39,6 +42,28 @@ void note_cuda_error(cudaError_t e) { t_last_cuda_error = cudaGetErrorString(e);
 
 std::atomic<unsigned long long> g_kernel_launches{0};
 void count_launch() { g_kernel_launches.fetch_add(1, std::memory_order_relaxed); }
+
+unsigned long long current_context_id() {
+  typedef CUresult (*GetCurrent)(CUcontext *);
+  typedef CUresult (*GetId)(CUcontext, unsigned long long *);
+  static const std::pair<GetCurrent, GetId> fns = []() {
+    void *cur = nullptr, *id = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &cur, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess)
+      cur = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &id, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess)
+      id = nullptr;
+    cudaGetLastError();
+    return std::make_pair(reinterpret_cast<GetCurrent>(cur), reinterpret_cast<GetId>(id));
+  }();
+  if (fns.first == nullptr || fns.second == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long v = 0;
+  if (fns.first(&ctx) != CUDA_SUCCESS || ctx == nullptr || fns.second(ctx, &v) != CUDA_SUCCESS) return 0;
+  return v;
+}
 }  // namespace llama
 
 namespace {
@@ -118,20 +143,34 @@ struct Profiler {
   bool on = false;
   int max_forwards = 0, used = 0;
   std::vector<cudaEvent_t> ev;  // [max_forwards][LLAMA_PROFILE_STEPS][2]
+  std::vector<char> launched;   // [max_forwards][LLAMA_PROFILE_STEPS]: the step launched a kernel
   cudaEvent_t *slot = nullptr;  // events of the forward being enqueued (null: not recording)
+  char *slot_launched = nullptr;
+  unsigned long long at_begin = 0;  // library launch count at the step's first edge
   void begin_forward() {
     slot = (on && used < max_forwards) ? &ev[(size_t)used * LLAMA_PROFILE_STEPS * 2] : nullptr;
+    slot_launched = slot != nullptr ? &launched[(size_t)used * LLAMA_PROFILE_STEPS] : nullptr;
     if (slot != nullptr) ++used;
   }
+  // A step fused into another step's kernel launches nothing between its two
+  // edges; it is then left out of the per-step times.
   void mark(int step, int edge, cudaStream_t st) {
-    if (slot != nullptr) cudaEventRecord(slot[step * 2 + edge], st);
+    if (slot == nullptr) return;
+    cudaEventRecord(slot[step * 2 + edge], st);
+    const unsigned long long n = g_kernel_launches.load(std::memory_order_relaxed);
+    if (edge == 0)
+      at_begin = n;
+    else
+      slot_launched[step] = n != at_begin ? 1 : 0;
   }
   void release() {
     for (cudaEvent_t e : ev) cudaEventDestroy(e);
     ev.clear();
+    launched.clear();
     on = false;
     used = max_forwards = 0;
     slot = nullptr;
+    slot_launched = nullptr;
   }
 };
 
@@ -670,12 +709,12 @@ llama_status llama_block_create(const llama_config *cfg, const llama_block_weigh
   if (s == LLAMA_OK) s = alloc_workspace(dm, max_tokens, true, b->al, &b->ws);
   if (s == LLAMA_OK) {
     b->rope = (float2 *)b->al.alloc((size_t)dm.max_seq * (dm.D / 2) * sizeof(float2));
-    b->status = (int *)b->al.alloc(sizeof(int));
+    b->status = (int *)b->al.alloc(sizeof(DeviceStatus));
     if (b->al.failed) s = LLAMA_ERR_OOM;
   }
   if (s == LLAMA_OK) {
     if (launch_rope_table_any(dm, b->rope) != cudaSuccess ||
-        cudaMemset(b->status, 0, sizeof(int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+        cudaMemset(b->status, 0, sizeof(DeviceStatus)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
       s = LLAMA_ERR_CUDA;
   }
   if (s != LLAMA_OK) {
@@ -732,6 +771,7 @@ llama_status llama_block_profile_enable(llama_block *blk, int32_t max_forwards) 
   if (blk == nullptr || max_forwards <= 0) return LLAMA_ERR_INVALID_ARG;
   blk->prof.release();
   blk->prof.ev.resize((size_t)max_forwards * LLAMA_PROFILE_STEPS * 2);
+  blk->prof.launched.assign((size_t)max_forwards * LLAMA_PROFILE_STEPS, 0);
   for (cudaEvent_t &e : blk->prof.ev) {
     if (cudaEventCreate(&e) != cudaSuccess) {
       e = nullptr;
@@ -764,6 +804,7 @@ llama_status llama_block_profile_read(llama_block *blk, int32_t *launches, float
     for (int s = 0; s < LLAMA_PROFILE_STEPS; ++s) {
       float ms = 0.f;
       cudaEvent_t *e = &p.ev[((size_t)f * LLAMA_PROFILE_STEPS + s) * 2];
+      if (!p.launched[(size_t)f * LLAMA_PROFILE_STEPS + s]) continue;  // fused into another step's kernel
       if (cudaEventElapsedTime(&ms, e[0], e[1]) == cudaSuccess) {
         launches[s] += 1;
         total_ms[s] += ms;
@@ -819,6 +860,35 @@ llama_status llama_stack_set_decode_mode(llama_stack *stk, int32_t mode) {
   return set_decode_mode(stk->ws, stk->device, mode);
 }
 
+// Writes the wait budget (cycles, 0 = the default) of a handle's status block.
+static llama_status set_wait_budget(int *dev_status, int device, int64_t cycles) {
+  if (cycles < 0) return LLAMA_ERR_INVALID_ARG;
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return LLAMA_ERR_CUDA;
+  if (prev != device && cudaSetDevice(device) != cudaSuccess) return LLAMA_ERR_CUDA;
+  const long long v = cycles;
+  DeviceStatus *blk = reinterpret_cast<DeviceStatus *>(dev_status);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&blk->wait_budget, &v, sizeof(v), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (prev != device) cudaSetDevice(prev);
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    return LLAMA_ERR_CUDA;
+  }
+  return LLAMA_OK;
+}
+
+llama_status llama_block_set_wait_budget(llama_block *blk, int64_t cycles) {
+  if (blk == nullptr) return LLAMA_ERR_INVALID_ARG;
+  return set_wait_budget(blk->status, blk->device, cycles);
+}
+
+llama_status llama_stack_set_wait_budget(llama_stack *stk, int64_t cycles) {
+  if (stk == nullptr) return LLAMA_ERR_INVALID_ARG;
+  return set_wait_budget(stk->status, stk->device, cycles);
+}
+
 llama_status llama_block_device_status(llama_block *blk) {
   if (blk == nullptr) return LLAMA_ERR_INVALID_ARG;
   return read_status(blk->status, blk->device, &blk->ws, &blk->dm);
@@ -857,7 +927,7 @@ llama_status llama_stack_create(const llama_config *cfg, int32_t n_layers, int32
     k->xn = k->al.alloc((size_t)max_tokens * dm.d * e);
     k->next_tok = (int32_t *)k->al.alloc((size_t)max_tokens * sizeof(int32_t));
     k->rope = (float2 *)k->al.alloc((size_t)dm.max_seq * (dm.D / 2) * sizeof(float2));
-    k->status = (int *)k->al.alloc(sizeof(int));
+    k->status = (int *)k->al.alloc(sizeof(DeviceStatus));
     if (k->al.failed) s = LLAMA_ERR_OOM;
   }
   if (s == LLAMA_OK) {
@@ -865,7 +935,7 @@ llama_status llama_stack_create(const llama_config *cfg, int32_t n_layers, int32
     if (err == cudaSuccess) err = cudaMemcpy(k->lm_head, lm_head, (size_t)vocab * dm.d * e, cudaMemcpyDeviceToDevice);
     if (err == cudaSuccess) err = cudaMemcpy(k->final_norm, final_norm, dm.d * e, cudaMemcpyDeviceToDevice);
     if (err == cudaSuccess) err = launch_rope_table_any(dm, k->rope);
-    if (err == cudaSuccess) err = cudaMemset(k->status, 0, sizeof(int));
+    if (err == cudaSuccess) err = cudaMemset(k->status, 0, sizeof(DeviceStatus));
     if (err == cudaSuccess) err = cudaDeviceSynchronize();
     if (err != cudaSuccess) s = LLAMA_ERR_CUDA;
   }

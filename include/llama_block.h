@@ -235,8 +235,11 @@ unsigned long long llama_kernel_launch_count(void);
  * forward call records a CUDA event pair on its stream around each step's
  * kernel launch, for up to max_forwards calls (events are created here;
  * synchronous).  llama_block_profile_read synchronises the device, writes for
- * each step s in [0, LLAMA_PROFILE_STEPS) the number of launches timed and
- * their total milliseconds, then clears the record.  Steps: 0 attention_norm,
+ * each step s in [0, LLAMA_PROFILE_STEPS) the number of forwards in which the
+ * step launched a kernel of its own and the total milliseconds of those, then
+ * clears the record; a step fused into another step's kernel (RoPE + KV write
+ * in the QKV epilogue, ffn_norm in the O and gate/up epilogues) reads 0
+ * launches.  Steps: 0 attention_norm,
  * 1 QKV projection, 2 RoPE + KV write, 3 attention, 4 O projection + residual,
  * 5 ffn_norm, 6 gate/up + SwiGLU, 7 down projection + residual. */
 #define LLAMA_PROFILE_STEPS 8
@@ -269,6 +272,25 @@ llama_status llama_stack_set_decode_mode(llama_stack *stk, int32_t mode);
  * was written as zeros), LLAMA_ERR_CUDA when the read itself failed. */
 llama_status llama_block_device_status(llama_block *blk);
 llama_status llama_stack_device_status(llama_stack *stk);
+
+/* Bound, in SM clock cycles, on every wait of this handle's kernels that gives
+ * up (mbarrier waits of the tensor-core kernels, the fused decode kernel's
+ * phase barriers, the split-KV decode kernel's stage waits); 0 restores the
+ * default, about 4e9 cycles (2 s at 2 GHz), which no legitimate wait reaches.
+ * A wait that runs out records LLAMA_ERR_DEVICE_TIMEOUT in the status word
+ * (llama_block_device_status), makes the kernel's other roles give up too, and
+ * the kernel returns once the copies and MMAs it had issued have completed --
+ * those waits keep the default bound -- and its tensor memory is freed; the
+ * outputs of that forward are undefined, the context stays usable, and
+ * reading the status resets the handle's scratch for the next forward.  This
+ * is a fault-injection and diagnosis knob (a short budget makes ordinary
+ * waits give up); the library itself never sets it.  Synchronises the
+ * device; do not call it while a forward of the handle is in flight.
+ * LLAMA_ERR_INVALID_ARG for a null handle or a negative budget.
+ * The pages have no counterpart: it serves the bounded-wait failure
+ * detection of the kernels. */
+llama_status llama_block_set_wait_budget(llama_block *blk, int64_t cycles);
+llama_status llama_stack_set_wait_budget(llama_stack *stk, int64_t cycles);
 
 #ifdef __cplusplus
 }

@@ -80,16 +80,25 @@ llama_status llama_op_rope_kv_write(int32_t dtype, const void *qkv, void *q_out,
  * LLAMA_NOALLOC_SCRATCH_BYTES that is part of the library image on every GPU
  * that loads it, held until the process exits; no cudaMalloc / cudaFree or
  * allocating library routine is called.
- *   - Limit: B * H * ceil((start_pos + 1) / 256) * (D + 2) * 4 bytes must not
- *     exceed LLAMA_NOALLOC_SCRATCH_BYTES, else LLAMA_ERR_RANGE (nothing runs).
- *     32 MiB covers, e.g., B = 64, H = 32, D = 128 up to 8192 cached positions.
+ *   - Limit: one sequence's partials, H * ceil((start_pos + 1) / 256) *
+ *     (D + 2) * 4 bytes, must fit in LLAMA_NOALLOC_SCRATCH_BYTES, else
+ *     LLAMA_ERR_RANGE (nothing runs); a single chunk (start_pos < 256) needs
+ *     none.  Batches whose partials do not fit run in groups of sequences, one
+ *     group after another on the stream, each reusing the array.  With
+ *     H = 32 and D = 128 a sequence needs 16,640 bytes per 256 positions:
+ *     32 MiB holds one sequence of up to 516,096 cached positions, and B = 64
+ *     sequences of 4096 positions in one group.
  *   - D in {64, 128}, n_heads / n_kv_heads <= 8 (LLAMA_ERR_UNSUPPORTED otherwise).
  *   - The first call on a device looks up the array's device address (a
- *     one-time set-up per device, done with that device current); make that
- *     first call before any stream capture.
+ *     one-time set-up per CUDA context, done with that device current, and
+ *     done again after the device's context was reset); make that first call
+ *     before any stream capture.
  *   - All calls share the array and every call overwrites the partials it
  *     reads, so nothing needs clearing; calls that may run at the same time on
- *     the GPU (unordered streams) race on the array and must be avoided. */
+ *     the GPU (unordered streams) race on the array and must be avoided.
+ *   - The kernel's bounded waits (2 s, never reached in normal operation)
+ *     have no status word to report to here: if one ran out, the call still
+ *     returns LLAMA_OK and o is undefined. */
 #define LLAMA_NOALLOC_SCRATCH_BYTES (32u << 20)
 llama_status llama_op_attention_decode_noalloc(const void *q, const llama_kv_cache *kv, void *o, int32_t B,
                                                int32_t start_pos, int32_t H, int32_t G, int32_t D,

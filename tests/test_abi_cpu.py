@@ -105,3 +105,5 @@ def test_null_arguments_are_rejected(lib):
                                   4, 2, 64) == lib.LLAMA_ERR_RANGE
     assert lib.llama_op_attention_workspace_bytes(lib.LLAMA_BF16, 64, 1, 4095, 32, 128) == 64 * 32 * 16 * 130 * 4
     assert lib.llama_op_attention_workspace_bytes(lib.LLAMA_BF16, 64, 8, 0, 32, 128) == 0
+    assert lib.llama_block_set_wait_budget(None, 0) == lib.LLAMA_ERR_INVALID_ARG
+    assert lib.llama_stack_set_wait_budget(None, 100) == lib.LLAMA_ERR_INVALID_ARG
