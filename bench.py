@@ -321,6 +321,8 @@ def main():
                     help="time only the decode step (B=64 at start_pos 4095); for profiler captures")
     ap.add_argument("--smollm2-only", action="store_true",
                     help="time only the SmolLM2-shaped block (B=8, S=1024, d_model 576); for profiler captures")
+    ap.add_argument("--standalone-only", action="store_true",
+                    help="time only the standalone RMSNorm and RoPE + KV-write launches; for profiler captures")
     ap.add_argument("--seq", type=int, default=8192,
                     help="prefill length S (default 8192; smaller values are for profiler captures)")
     args = ap.parse_args()
@@ -346,6 +348,15 @@ def main():
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
 
+    if args.standalone_only:
+        ops = bench_standalone_ops(lb, torch, dev, stream, args, measured_peaks()[0])
+        if rank == 0:
+            print(json.dumps({"metric": "standalone RMSNorm and RoPE + KV write, % of HBM", "value":
+                              ops["rmsnorm_8192x4096"]["hbm_frac"], "unit": "fraction of measured HBM GB/s",
+                              "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                              "dtype": "bf16", "data": "synthetic", "config": {"workload": "standalone_ops_8192x4096"},
+                              "standalone_ops": ops}), flush=True)
+        return 0
     if args.smollm2_only:
         sm = bench_block_shape(lb, torch, dev, stream, SMOLLM2_SHAPE, args)
         if rank == 0:
