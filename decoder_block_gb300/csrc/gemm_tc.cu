@@ -6,6 +6,11 @@
 
 #include "gemm_tc_body.cuh"
 
+// 256 x 256 tiles on CTA pairs for large compute-bound GEMMs (tuning define: 0 keeps every GEMM on single CTAs).
+#ifndef LLAMA_GEMM_PAIRS
+#define LLAMA_GEMM_PAIRS 1
+#endif
+
 namespace llama {
 namespace {
 
@@ -14,6 +19,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ GemmArgs args) {
   gemm_tc_run<EPI, BN, GROUPED>(&tmA, &tmB, args, PhaseSync{});
+}
+
+// Whole 256 x 256 tiles on CTA pairs (launched in clusters of two; cta_group::2
+// MMAs issued by the even CTA of each pair).
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ GemmArgs args) {
+  gemm_tc_run<EPI, 256, false, true>(&tmA, &tmB, args, PhaseSync{});
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
@@ -132,6 +146,67 @@ cudaError_t launch_cfg(const CUtensorMap &ma, const CUtensorMap &mb, GemmArgs ar
   cfg.attrs = attr;
   cfg.numAttrs = cluster > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, BN, GROUPED>, ma, mb, args);
+}
+
+// How many clusters of two pair-kernel CTAs the device holds at once (0 when
+// the query fails); the pair grid is at most that many pairs, every pair
+// resident for the whole launch.
+template <int EPI>
+int pair_slots() {
+  static std::mutex mu;
+  static int slots = -1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (slots < 0) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(sm_count() & ~1));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = GemmCfg<256, true>::SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_pair_kernel<EPI>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      clusters = 0;
+    }
+    slots = clusters;
+  }
+  return slots;
+}
+
+template <int EPI>
+cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &args, cudaStream_t st) {
+  using G = GemmCfg<256, true>;
+  static PerContextOnce smem_limit;
+  const cudaError_t attr_err = smem_limit.run([] {
+    return cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                G::SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const int tiles = ((args.M + 2 * BM - 1) / (2 * BM)) * ((args.N + 255) / 256);
+  int pairs = pair_slots<EPI>();
+  if (pairs <= 0) return cudaErrorInvalidConfiguration;
+  pairs = tiles < pairs ? tiles : pairs;
+  count_launch();
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * pairs));
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = G::SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<EPI>, ma, mb, args);
 }
 
 template <int EPI>
@@ -371,6 +446,26 @@ cudaError_t launch_gemm_tc(const bf16 *A, const bf16 *W, const bf16 *R, void *C,
   const cudaError_t e = gemm_tc_prepare(A, W, R, C, M, N, K, epi, status, ws, norm, scatter, weights_static, &ma, &mb,
                                         &args, &bn);
   if (e != cudaSuccess) return e;
+  // Compute-bound GEMMs whose plan takes 256-wide tiles run on CTA pairs when
+  // there is at least one wave of 256 x 256 tiles: whole tiles, no K splits.
+  const bool pair_epi = epi == EPI_QKV_ROPE || epi == EPI_RESIDUAL_SQSUM || epi == EPI_SWIGLU_ROWSCALE ||
+                        epi == EPI_RESIDUAL || epi == EPI_F32OUT;
+  if (LLAMA_GEMM_PAIRS && pair_epi && bn == 256 &&
+      2 * ((M + 2 * BM - 1) / (2 * BM)) * ((N + 255) / 256) >= sm_count()) {
+    args.splits = 1;
+    args.split_tiles = 0;
+    args.ksteps_split = (K + BK - 1) / BK;
+    args.part = nullptr;
+    args.counters = nullptr;
+    if (!make_map_2d(&mb, W, (uint64_t)N, (uint64_t)K, 128)) return cudaErrorInvalidValue;
+    switch (epi) {
+      case EPI_QKV_ROPE: return launch_pair<EPI_QKV_ROPE>(ma, mb, args, st);
+      case EPI_RESIDUAL_SQSUM: return launch_pair<EPI_RESIDUAL_SQSUM>(ma, mb, args, st);
+      case EPI_SWIGLU_ROWSCALE: return launch_pair<EPI_SWIGLU_ROWSCALE>(ma, mb, args, st);
+      case EPI_RESIDUAL: return launch_pair<EPI_RESIDUAL>(ma, mb, args, st);
+      case EPI_F32OUT: return launch_pair<EPI_F32OUT>(ma, mb, args, st);
+    }
+  }
   switch (epi) {
     case EPI_STORE: return launch_epi<EPI_STORE>(ma, mb, args, bn, st);
     case EPI_RESIDUAL: return launch_epi<EPI_RESIDUAL>(ma, mb, args, bn, st);

@@ -55,14 +55,17 @@ constexpr int NUM_THREADS = 192;
 #endif
 constexpr int GROUP_M = LLAMA_GEMM_GROUP_M;
 
-template <int BN_>
+// PAIR_: the tile is computed by a CTA pair (cta_group::2 MMAs, M = 256): each
+// CTA holds 128 rows of A and half of the BN weight rows per stage.
+template <int BN_, bool PAIR_ = false>
 struct GemmCfg {
   static constexpr int BN = BN_;
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_ROWS = PAIR_ ? BN / 2 : BN;  // weight rows this CTA loads per stage
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 256 ? 4 : (BN == 192 ? 5 : (BN == 128 ? 6 : 8));
-  static constexpr int NUM_BARS = 2 * STAGES + 7;
+  static constexpr int STAGES = PAIR_ ? 6 : (BN == 256 ? 4 : (BN == 192 ? 5 : (BN == 128 ? 6 : 8)));
+  static constexpr int NUM_BARS = 2 * STAGES + 8;
   // after the barriers and flags: the four epilogue warps' 2 KB output stages
   static constexpr int STAGE_OUT_OFF = (STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + 15) / 16 * 16;
   static constexpr int SMEM_BYTES = 1024 + STAGE_OUT_OFF + 4 * 2048;
@@ -508,10 +511,23 @@ struct GroupedTiles {
 
 // The GEMM of one launch (or one phase of a fused kernel, see phase_sync.cuh):
 // every CTA of the grid runs this with its 192 threads.
-template <int EPI, int BN, bool GROUPED>
+//
+// PAIR: whole 256 x 256 tiles computed by the two CTAs of a cluster (launched
+// with cluster size 2, never as a phase of a fused kernel).  CTA r loads rows
+// r*128 .. r*128+127 of the tile's A rows and of its 256 weight rows into its
+// own shared memory; both CTAs' copies complete on the even (leader) CTA's
+// full barriers, whose MMA thread issues cta_group::2 MMAs that read both CTAs'
+// operands and write 128 accumulator rows into each CTA's tensor memory.  Its
+// commits arrive on the stage-empty and accumulator-full barriers of both CTAs;
+// each CTA's epilogue drains its own accumulator rows and hands the
+// accumulator back to the leader.  A CTA that gives up also raises its peer's
+// abort flag.  Per K step each SM now brings in 32 KB of operands instead of
+// 48 KB for the same MMA work.
+template <int EPI, int BN, bool GROUPED, bool PAIR = false>
 __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtensorMap *tmB, const GemmArgs &args,
                                             const PhaseSync sync) {
-  using G = GemmCfg<BN>;
+  static_assert(!PAIR || (BN == 256 && !GROUPED), "CTA pairs compute dense 256 x 256 tiles");
+  using G = GemmCfg<BN, PAIR>;
   constexpr int STAGES = G::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -519,6 +535,7 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + G::NUM_BARS);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *last_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);  // shared split-K finish
+  volatile uint32_t *peer_fills = tmem_slot + 3;  // PAIR: fills the peer's producer issued (exchange at exit)
 
   const uint32_t smem0 = ptx::smem_u32(smem);
   const uint32_t bar0 = ptx::smem_u32(bars);
@@ -531,14 +548,25 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
   // the arrival count of the tile is known (1 arrival)
   const uint32_t parts_bar = bar0 + 8u * (2 * STAGES + 5);
   const uint32_t count_bar = bar0 + 8u * (2 * STAGES + 6);
+  const uint32_t xchg_bar = bar0 + 8u * (2 * STAGES + 7);  // PAIR: the peer's fill count has arrived
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tiles = (args.M + BM - 1) / BM, n_tiles = (args.N + BN - 1) / BN;
+  // PAIR: this CTA's rank in the pair; units are distributed over pairs
+  const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+  const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int unit_stride = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  // the leader's copy of one of this CTA's barriers (PAIR), and raising the peer's abort flag
+  auto leader = [&](uint32_t bar) { return ptx::mapa_shared(bar, 0); };
+  auto abort_peer = [&]() {
+    if constexpr (PAIR) ptx::st_cluster_u32(ptx::mapa_shared(ptx::smem_u32((const void *)abort_flag), rank ^ 1u), 1u);
+  };
+  const int m_tiles = PAIR ? (args.M + 2 * BM - 1) / (2 * BM) : (args.M + BM - 1) / BM;
+  const int n_tiles = (args.N + BN - 1) / BN;
   const int k_steps = (args.K + BK - 1) / BK;
   const GroupedTiles gt{args.group_off, args.n_groups, n_tiles};
   if constexpr (GROUPED) grid_dependency_wait();  // every role reads the group offsets
   const int num_tiles = m_tiles * n_tiles;
-  const int split_units = GROUPED ? 0 : args.split_tiles * args.splits;
+  const int split_units = (GROUPED || PAIR) ? 0 : args.split_tiles * args.splits;
   const int num_units = GROUPED ? gt.count() : split_units + (num_tiles - args.split_tiles);
   // unit -> first A row, first W row, end of the valid A rows, N tile, K range in BK steps.
   // Units [0, split_units) are the K pieces of the last split_tiles tiles (spread over
@@ -551,6 +579,15 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
       a_row = args.group_off[g] + mt * BM;
       m_end = min(args.group_off[g + 1], args.M);  // never past A, whatever the offsets say
       w_row = g * args.N + nt * BN;
+      k0 = 0;
+      k1 = k_steps;
+      slot = -1;
+    } else if constexpr (PAIR) {
+      int mt;
+      tile_coords(u, m_tiles, n_tiles, mt, nt);
+      a_row = mt * 2 * BM + (int)rank * BM;
+      w_row = nt * BN + (int)rank * (BN / 2);
+      m_end = args.M;
       k0 = 0;
       k1 = k_steps;
       slot = -1;
@@ -567,24 +604,33 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(tfull_bar(a), 1);
-      ptx::mbar_init(tempty_bar(a), 128);
+      ptx::mbar_init(tempty_bar(a), PAIR ? 8 : 128);  // PAIR: one arrival per epilogue warp of both CTAs
     }
     ptx::mbar_init(fin_bar, 1);
     ptx::mbar_init(parts_bar, 4);
     ptx::mbar_init(count_bar, 1);
+    ptx::mbar_init(xchg_bar, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 1 && !sync.fused()) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), G::TMEM_COLS);
-    ptx::tmem_relinquish();
+    if constexpr (PAIR) {
+      ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), G::TMEM_COLS);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(tmem_slot), G::TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(tmA);
     ptx::tma_prefetch_desc(tmB);
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    ptx::cluster_sync();  // both CTAs' barriers exist before either signals the other's
+  else
+    __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = sync.fused() ? sync.tmem : *tmem_slot;
 
@@ -593,15 +639,30 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
     if (lane == 0) {
       // The weights of the first unit's first stages depend on no earlier
       // kernel: request them before waiting for the activations.
+      // PAIR: both CTAs' copies complete on the leader's full barriers; the
+      // leader alone arrives there, expecting both CTAs' bytes
+      auto expect = [&](int s) {
+        if constexpr (PAIR) {
+          if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * G::STAGE_BYTES);
+        } else {
+          ptx::mbar_arrive_expect_tx(full_bar(s), G::STAGE_BYTES);
+        }
+      };
+      auto load = [&](uint32_t dst, const CUtensorMap *map, int x, int y, int s) {
+        if constexpr (PAIR)
+          ptx::tma_load_2d_pair(dst, map, x, y, leader(full_bar(s)));
+        else
+          ptx::tma_load_2d(dst, map, x, y, full_bar(s));
+      };
       int pre = 0;
-      if (!GROUPED && args.prefetch_w && (int)blockIdx.x < num_units) {
+      if (!GROUPED && args.prefetch_w && unit0 < num_units) {
         int a_row, w_row, m_end, nt, k0, k1, slot;
-        unit_coords(blockIdx.x, a_row, w_row, m_end, nt, k0, k1, slot);
+        unit_coords(unit0, a_row, w_row, m_end, nt, k0, k1, slot);
         pre = min(STAGES, k1 - k0);
         for (int i = 0; i < pre; ++i) {
           const uint32_t sb = smem0 + i * G::STAGE_BYTES + G::A_BYTES;
-          ptx::mbar_arrive_expect_tx(full_bar(i), G::STAGE_BYTES);
-          ptx::tma_load_2d(sb, tmB, (k0 + i) * BK, w_row, full_bar(i));
+          expect(i);
+          load(sb, tmB, (k0 + i) * BK, w_row, i);
         }
       }
       int it = 0;
@@ -614,14 +675,13 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
           ok = false;
           if (pre > 0) {
             int a_row, w_row, m_end, nt, k0, k1, slot;
-            unit_coords(blockIdx.x, a_row, w_row, m_end, nt, k0, k1, slot);
-            for (int i = 0; i < pre; ++i) ptx::tma_load_2d(smem0 + i * G::STAGE_BYTES, tmA, (k0 + i) * BK, a_row,
-                                                           full_bar(i));
+            unit_coords(unit0, a_row, w_row, m_end, nt, k0, k1, slot);
+            for (int i = 0; i < pre; ++i) load(smem0 + i * G::STAGE_BYTES, tmA, (k0 + i) * BK, a_row, i);
           }
           it = pre;
         }
       }
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      for (int u = unit0; u < num_units && ok; u += unit_stride) {
         int a_row, w_row, m_end, nt, k0, k1, slot;
         unit_coords(u, a_row, w_row, m_end, nt, k0, k1, slot);
         for (int k = k0; k < k1; ++k) {
@@ -629,41 +689,73 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
           const uint32_t ph = (it / STAGES) & 1;
           const uint32_t sa = smem0 + s * G::STAGE_BYTES, sb = sa + G::A_BYTES;
           if (it < pre) {  // stage s is fresh and its weights are already on the way
-            ptx::tma_load_2d(sa, tmA, k * BK, a_row, full_bar(s));
+            load(sa, tmA, k * BK, a_row, s);
             ++it;
             continue;
           }
           if (!ptx::mbar_wait(empty_bar(s), ph ^ 1, abort_flag, args.status, DEV_TIMEOUT_PRODUCER)) {
+            abort_peer();
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(full_bar(s), G::STAGE_BYTES);
-          ptx::tma_load_2d(sa, tmA, k * BK, a_row, full_bar(s));
-          ptx::tma_load_2d(sb, tmB, k * BK, w_row, full_bar(s));
+          expect(s);
+          load(sa, tmA, k * BK, a_row, s);
+          load(sb, tmB, k * BK, w_row, s);
           ++it;
         }
       }
       // Every issued copy must have landed before the CTA can exit.
-      for (int j = it - STAGES < 0 ? 0 : it - STAGES; j < it; ++j)
-        ptx::mbar_drain(full_bar(j % STAGES), (j / STAGES) & 1, args.status, DEV_TIMEOUT_PRODUCER);
+      if constexpr (PAIR) {
+        // A fill completes on the leader's barrier only once the leader has
+        // arrived for it and both CTAs' bytes have landed.  The producers
+        // exchange their fill counts; for fills that only the other one issued
+        // (this one gave up earlier) this one supplies its missing part -- the
+        // leader its arrival (expecting the peer's bytes only), the peer its
+        // bytes' worth of transaction count -- so that every issued copy can
+        // complete.  A producer runs at most STAGES fills ahead of the fills
+        // the MMAs have consumed, so the leader then waits for the last STAGES
+        // fills, and the exit barrier keeps the peer alive until it has.
+        ptx::st_cluster_u32(ptx::mapa_shared(ptx::smem_u32((const void *)peer_fills), rank ^ 1u), (uint32_t)it);
+        ptx::mbar_arrive_cluster(ptx::mapa_shared(xchg_bar, rank ^ 1u));
+        int other = it;
+        if (ptx::mbar_wait_cluster(xchg_bar, 0, args.status, DEV_TIMEOUT_PRODUCER)) other = (int)*peer_fills;
+        for (int j = it; j < other; ++j) {
+          if (rank == 0)
+            ptx::mbar_arrive_expect_tx(full_bar(j % STAGES), G::STAGE_BYTES);
+          else
+            ptx::mbar_complete_tx_cluster(leader(full_bar(j % STAGES)), G::STAGE_BYTES);
+        }
+        if (rank == 0) {
+          const int hi = max(it, other);
+          for (int j = max(0, hi - STAGES); j < hi; ++j)
+            ptx::mbar_drain(full_bar(j % STAGES), (j / STAGES) & 1, args.status, DEV_TIMEOUT_PRODUCER);
+        }
+      } else {
+        for (int j = it - STAGES < 0 ? 0 : it - STAGES; j < it; ++j)
+          ptx::mbar_drain(full_bar(j % STAGES), (j / STAGES) & 1, args.status, DEV_TIMEOUT_PRODUCER);
+      }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+    if (lane == 0 && (!PAIR || rank == 0)) {  // PAIR: the leader issues the pair's MMAs
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
       int it = 0, tcount = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++tcount) {
+      for (int u = unit0; u < num_units && ok; u += unit_stride, ++tcount) {
         int a_row, w_row, m_end, nt, k0, k1, slot;
         unit_coords(u, a_row, w_row, m_end, nt, k0, k1, slot);
         const int acc = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
-        if (!ptx::mbar_wait(tempty_bar(acc), aph ^ 1, abort_flag, args.status, DEV_TIMEOUT_MMA)) break;
+        if (!ptx::mbar_wait(tempty_bar(acc), aph ^ 1, abort_flag, args.status, DEV_TIMEOUT_MMA)) {
+          abort_peer();
+          break;
+        }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int k = k0; k < k1; ++k) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!ptx::mbar_wait(full_bar(s), ph, abort_flag, args.status, DEV_TIMEOUT_MMA)) {
+            abort_peer();
             ok = false;
             break;
           }
@@ -671,16 +763,32 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
           const uint32_t sa = smem0 + s * G::STAGE_BYTES, sb = sa + G::A_BYTES;
           const uint64_t adesc = ptx::smem_desc_sw128(sa), bdesc = ptx::smem_desc_sw128(sb);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            ptx::mma_bf16_ss(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
-                             (k > k0 || kk != 0) ? 1u : 0u);
-          ptx::mma_commit(empty_bar(s));
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            if constexpr (PAIR)
+              ptx::mma_bf16_ss_pair(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
+                                    (k > k0 || kk != 0) ? 1u : 0u);
+            else
+              ptx::mma_bf16_ss(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
+                               (k > k0 || kk != 0) ? 1u : 0u);
+          }
+          if constexpr (PAIR)
+            ptx::mma_commit_pair(empty_bar(s), 3);  // frees stage s in both CTAs
+          else
+            ptx::mma_commit(empty_bar(s));
           ++it;
         }
-        if (ok) ptx::mma_commit(tfull_bar(acc));
+        if (ok) {
+          if constexpr (PAIR)
+            ptx::mma_commit_pair(tfull_bar(acc), 3);
+          else
+            ptx::mma_commit(tfull_bar(acc));
+        }
       }
       // Wait until every issued MMA has finished before TMEM / smem go away.
-      ptx::mma_commit(fin_bar);
+      if constexpr (PAIR)
+        ptx::mma_commit_pair(fin_bar, 1);
+      else
+        ptx::mma_commit(fin_bar);
       ptx::mbar_drain(fin_bar, 0, args.status, DEV_TIMEOUT_MMA);
     }
   } else {
@@ -693,7 +801,18 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
     uint4 *stage_out = reinterpret_cast<uint4 *>(smem + G::STAGE_OUT_OFF + (warp - 2) * 2048);
     int tcount = 0;
     int shared_splits = 0;  // split units finished jointly so far (phase of parts_bar / count_bar)
-    for (int u = blockIdx.x; u < num_units && inputs_ready; u += gridDim.x, ++tcount) {
+    // the accumulator's rows are read: hand it back to the MMA thread (PAIR: one
+    // arrival per warp on the leader's barrier)
+    auto release_acc = [&](int acc) {
+      ptx::tc_fence_before();
+      if constexpr (PAIR) {
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_remote(leader(tempty_bar(acc)));
+      } else {
+        ptx::mbar_arrive(tempty_bar(acc));
+      }
+    };
+    for (int u = unit0; u < num_units && inputs_ready; u += unit_stride, ++tcount) {
       int a_row, w_row, m_end, nt, k0, k1, slot;
       unit_coords(u, a_row, w_row, m_end, nt, k0, k1, slot);
       const int acc = tcount & 1;
@@ -720,13 +839,15 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
         load_rope32<EPI>(args, m, nt * BN, cs);
       }
       bool ok = ptx::mbar_wait(tfull_bar(acc), aph, abort_flag, args.status, DEV_TIMEOUT_EPILOGUE);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      if (!__all_sync(0xffffffffu, ok)) {
+        abort_peer();
+        break;
+      }
       ptx::tc_fence_after();
       const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       if (slot < 0 && staged) {
         const float sq = residual_tile_staged<EPI, BN>(args, trow, stage_out, a_row + q * 32, m_end, nt * BN, lane, rc);
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(tempty_bar(acc));
+        release_acc(acc);
         if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
           if (m < args.M) {
             atomicAdd(args.ss_out + m, sq);
@@ -756,8 +877,7 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
 #pragma unroll
           for (int i = 0; i < 8; ++i) cs[i] = csn[i];
         }
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(tempty_bar(acc));
+        release_acc(acc);
         if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
           if (m < args.M) {
             atomicAdd(args.ss_out + m, sq);
@@ -862,7 +982,7 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
       }
     }
   }
-  if (!GROUPED && args.cluster_split) {
+  if (!GROUPED && !PAIR && args.cluster_split) {
     // Every CTA of the cluster holds one K piece of the same tile.  Once all
     // partials are in shared memory, CTA `rank` finishes the 32-column chunks
     // rank, rank + splits, ...: each epilogue thread (one tile row) sums the
@@ -907,14 +1027,20 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
     ptx::cluster_sync();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    ptx::cluster_sync();  // neither CTA leaves while the pair's MMAs or copies may still use its memory
+  else
+    __syncthreads();
   if (sync.fused()) {  // the next phase reuses this shared memory and TMEM
     if (threadIdx.x == 0) {
       for (int i = 0; i < G::NUM_BARS; ++i) ptx::mbar_inval(bar0 + 8u * i);
     }
   } else if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, G::TMEM_COLS);
+    if constexpr (PAIR)
+      ptx::tmem_dealloc_pair(tmem_base, G::TMEM_COLS);
+    else
+      ptx::tmem_dealloc(tmem_base, G::TMEM_COLS);
   }
 }
 
