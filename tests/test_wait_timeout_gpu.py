@@ -9,8 +9,11 @@ other roles give up too, and it returns once the copies and MMAs it had issued
 have landed and its tensor memory is freed.  The test checks that the host
 reads LLAMA_ERR_DEVICE_TIMEOUT (once: reading clears it), that the CUDA
 context is still usable, and that the same handle with the default budget, and
-a fresh handle, then match the fp64 oracle.  Nothing here faults or traps.
+a fresh handle, then match the fp64 oracle.  A Llama-3-8B-shaped prefill
+does the same through the GEMMs that run on CTA pairs.  Nothing here faults
+or traps.
 """
+import numpy as np
 import pytest
 
 import oracle
@@ -88,3 +91,30 @@ def test_stack_wait_budget_setter(lb):
         t.cuda.synchronize()
     finally:
         lb.llama_stack_destroy(stk)
+
+
+def test_wait_that_runs_out_in_cta_pair_gemms(lb):
+    """The same on a Llama-3-8B-shaped prefill (B = 1, S = 2048), whose four
+    GEMMs run as 256 x 256 tiles on CTA pairs: a wait that gives up in one CTA
+    of a pair makes its peer give up too, the pair settles the copies either
+    producer issued before both leave, and the handle recovers."""
+    s = dict(synth.SHAPES["llama3_8b_prefill_b4s2048"], B=1)
+    B, S = 1, 2048
+    w = synth.block_weights(s)
+    x = synth.block_activations(s, B=B, S=S)
+    kc, vc = synth.kv_cache(s, max_batch=B, max_seq_len=S)
+    rows = [(0, 0), (0, 127), (0, 128), (0, 255), (0, 256), (0, 1023), (0, 2047)]
+    yr, kr, vr = oracle.block_forward_rows(s, f64_weights(w), synth.as_f64(x), 0, synth.as_f64(kc),
+                                           synth.as_f64(vc), rows)
+    with GpuBlock(s, w, B * S) as blk:
+        lb.check(lb.llama_block_set_wait_budget(blk.h, 1), "set a one-cycle wait budget")
+        _forward(blk, x, kc, vc, B, S)
+        assert lb.llama_block_device_status(blk.h) == lb.LLAMA_ERR_DEVICE_TIMEOUT
+        lb.check(lb.llama_block_set_wait_budget(blk.h, 0), "restore the default budget")
+        yd, kd, vd = _forward(blk, x, kc, vc, B, S)
+        assert lb.llama_block_device_status(blk.h) == lb.LLAMA_OK
+    y = to_f64(yd)
+    ys = np.stack([y[b, t] for b, t in rows])
+    assert_parity(ys, yr, "bf16", "y (sampled rows) after the timeout")
+    assert_parity(to_f64(kd)[:, :, :S], kr, "bf16", "K cache after the timeout")
+    assert_parity(to_f64(vd)[:, :, :S], vr, "bf16", "V cache after the timeout")
