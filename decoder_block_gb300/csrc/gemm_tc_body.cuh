@@ -54,6 +54,12 @@ constexpr int NUM_THREADS = 192;
 #define LLAMA_GEMM_GROUP_M 32
 #endif
 constexpr int GROUP_M = LLAMA_GEMM_GROUP_M;
+// CTA pairs: 256-row tiles, so the same 4096 rows of A per group are 16 tiles
+// tall.  (Tuning define.)
+#ifndef LLAMA_GEMM_PAIR_GROUP_M
+#define LLAMA_GEMM_PAIR_GROUP_M 16
+#endif
+constexpr int PAIR_GROUP_M = LLAMA_GEMM_PAIR_GROUP_M;
 
 // PAIR_: the tile is computed by a CTA pair (cta_group::2 MMAs, M = 256): each
 // CTA holds 128 rows of A and half of the BN weight rows per stage.
@@ -100,11 +106,12 @@ struct GemmArgs {
   int cluster_split;
 };
 
-__device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int &mt, int &nt) {
-  const int per_group = GROUP_M * n_tiles;
+__device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int &mt, int &nt,
+                                            int group_m = GROUP_M) {
+  const int per_group = group_m * n_tiles;
   const int g = tile / per_group;
-  const int first = g * GROUP_M;
-  const int gm = min(m_tiles - first, GROUP_M);
+  const int first = g * group_m;
+  const int gm = min(m_tiles - first, group_m);
   const int local = tile % per_group;
   mt = first + local % gm;
   nt = local / gm;
@@ -584,7 +591,7 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
       slot = -1;
     } else if constexpr (PAIR) {
       int mt;
-      tile_coords(u, m_tiles, n_tiles, mt, nt);
+      tile_coords(u, m_tiles, n_tiles, mt, nt, PAIR_GROUP_M);
       a_row = mt * 2 * BM + (int)rank * BM;
       w_row = nt * BN + (int)rank * (BN / 2);
       m_end = args.M;

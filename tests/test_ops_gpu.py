@@ -30,6 +30,7 @@ GEMM_SHAPES = [
     (257, 264, 136),
     (64, 6144, 4096),    # decode-sized M, Llama-3-8B QKV
     (1000, 1536, 512),
+    (2000, 4000, 4104),  # CTA-pair tiles (residual and fp32 epilogues): ragged M, N and K
 ]
 
 
