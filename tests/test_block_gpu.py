@@ -126,6 +126,30 @@ def test_llama3_8b_prefill_full_size_sampled(name):
     assert_parity(vg[:, :, :S], vr, "bf16", "V cache (all written positions)")
 
 
+def test_llama3_8b_ragged_prefill_on_cta_pairs():
+    """B=2, S=2250 (4500 rows: the last 256-row pair tile has 148 live rows, 20 of them in its second
+    CTA) at start_pos 100 over a filled cache prefix: all four GEMMs run on CTA pairs.  Sampled rows
+    at both ends of that tile, every written K/V element, and the prefix bit for bit."""
+    s = dict(synth.SHAPES["llama3_8b_prefill_b4s2048"], B=2, S=2250, max_seq_len=2400)
+    B, S, sp = 2, 2250, 100
+    w = synth.block_weights(s)
+    x = synth.block_activations(s, tag="ragged_pairs", B=B, S=S)
+    kc, vc = synth.kv_cache(s, max_batch=B, max_seq_len=2400, fill_upto=sp)
+    y, kg, vg = _run(s, w, x, kc, vc, B, S, sp)
+    rows = sorted({(0, 0), (0, 2249), (1, 0), (1, 2101), (1, 2102), (1, 2229), (1, 2230), (1, 2249)} |
+                  set(_sample_rows(B, S, n_random=6, seed=3)))
+    yr, kr, vr = oracle.block_forward_rows(s, f64_weights(w), synth.as_f64(x), sp, synth.as_f64(kc),
+                                           synth.as_f64(vc), rows)
+    ys = np.stack([y[b, t] for b, t in rows])
+    xs = np.stack([synth.as_f64(x)[b, t] for b, t in rows])
+    assert_parity(ys, yr, "bf16", "y (sampled rows)")
+    assert_branch_parity(ys, yr, xs, "y - x (sampled rows)")
+    assert_parity(kg[:, :, sp:sp + S], kr, "bf16", "K cache (all written positions)")
+    assert_parity(vg[:, :, sp:sp + S], vr, "bf16", "V cache (all written positions)")
+    np.testing.assert_array_equal(kg[:, :, :sp], synth.as_f64(kc)[:, :, :sp])
+    np.testing.assert_array_equal(kg[:, :, sp + S:], synth.as_f64(kc)[:, :, sp + S:])
+
+
 def test_llama3_8b_decode_full_size():
     s = synth.SHAPES["llama3_8b_decode_b64"]
     B, S, sp = s["B"], s["S"], s["start_pos"]

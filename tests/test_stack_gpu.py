@@ -112,6 +112,24 @@ def test_llama3_8b_shaped_two_layer_stack_bf16(lb):
     assert_stack_parity(caches[1][0][:, :, :S], ref_caches[1][0][:, :, :S], "K cache layer 1")
 
 
+def test_llama3_8b_shaped_three_layer_stack_on_cta_pairs_bf16(lb):
+    """Three Llama-3-8B-shaped layers over a 2048-token prompt: every projection and the LM head
+    (vocabulary 32768) run on CTA pairs, and the down projections' epilogues hand the next block's
+    row statistics on through the alternating buffers."""
+    s = dict(synth.SHAPES["llama3_8b_prefill_b1s8192"], max_seq_len=2048)
+    B, S, L, vocab, n = 1, 2048, 2048, 32768, 3
+    args = _stack_inputs(s, n, vocab, B, S, L)
+    logits, caches, status = _run_stack(lb, s, *args, B, S, 0, L)
+    assert status == lb.LLAMA_OK
+    ref, ref_caches = _oracle(s, *args, 0)
+    assert_stack_parity(logits, ref, "logits (8B-shaped layers, S=2048)")
+    assert_parity(caches[0][0], ref_caches[0][0], "bf16", "K cache layer 0")
+    assert_parity(caches[0][1], ref_caches[0][1], "bf16", "V cache layer 0")
+    for l in (1, 2):
+        assert_stack_parity(caches[l][0], ref_caches[l][0], f"K cache layer {l}")
+        assert_stack_parity(caches[l][1], ref_caches[l][1], f"V cache layer {l}")
+
+
 def test_odd_layer_stack_repeated_and_continued_through_one_handle_bf16(lb):
     """A bf16 stack hands each block's row statistics to the next through two
     alternating buffers that the consuming epilogues clear.  With an odd layer
