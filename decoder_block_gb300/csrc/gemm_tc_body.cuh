@@ -18,6 +18,8 @@
 //               SiLU(gate) * up / fp32 out / RMSNorm row scale / RoPE and
 //               KV-cache scatter) and store to global memory, then
 //               hand the accumulator back -- overlapping the next tile's K loop.
+// Large compute-bound GEMMs run the PAIR variant instead (gemm_tc_run below):
+// 256 x 256 tiles on the two CTAs of a cluster with cta_group::2 MMAs.
 // Split-K (for few output tiles, e.g. the decode step's M = 64 rows, so that
 // every SM streams a share of the weights): a work unit is (tile, K split);
 // each epilogue warp adds its 32-row fp32 partial into the tile's fp32
@@ -30,8 +32,9 @@
 // create, by no kernel of a forward) the producer requests the first stages'
 // weights before it waits for the previous kernel (phase); everything else
 // (activations, residuals, row statistics, outputs) is touched after the wait.
-// Every mbarrier wait is bounded (clock budget); on expiry the kernel records a
-// status code, drains in-flight copies and MMAs, frees TMEM and returns.
+// Every mbarrier wait is bounded (the handle's wait budget); on expiry the
+// kernel records a status code, drains in-flight copies and MMAs (waits bounded
+// by the default budget), frees TMEM and returns.
 #pragma once
 
 #include <cuda.h>
