@@ -23,11 +23,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // Whole 256 x 256 tiles on CTA pairs (launched in clusters of two; cta_group::2
 // MMAs issued by the even CTA of each pair).
-template <int EPI>
+template <int EPI, bool GROUPED = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ GemmArgs args) {
-  gemm_tc_run<EPI, 256, false, true>(&tmA, &tmB, args, PhaseSync{});
+  gemm_tc_run<EPI, 256, GROUPED, true>(&tmA, &tmB, args, PhaseSync{});
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
@@ -150,11 +150,19 @@ cudaError_t launch_cfg(const CUtensorMap &ma, const CUtensorMap &mb, GemmArgs ar
 
 // How many clusters of two pair-kernel CTAs the device holds at once (0 when
 // the query fails); the pair grid is at most that many pairs, every pair
-// resident for the whole launch.
-template <int EPI>
+// resident for the whole launch.  Every pair kernel has the same shared memory
+// and thread count, so one of them answers for all.
 int pair_slots() {
   static std::mutex mu;
   static int slots = -1;
+  static PerContextOnce smem_limit;
+  if (smem_limit.run([] {
+        return cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI_RESIDUAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    GemmCfg<256, true>::SMEM_BYTES);
+      }) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
   std::lock_guard<std::mutex> lock(mu);
   if (slots < 0) {
     cudaLaunchConfig_t cfg = {};
@@ -169,7 +177,7 @@ int pair_slots() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_pair_kernel<EPI>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_pair_kernel<EPI_RESIDUAL>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       clusters = 0;
     }
@@ -178,19 +186,22 @@ int pair_slots() {
   return slots;
 }
 
-template <int EPI>
+// GROUPED: the tile count is on the device; every pair takes part.
+template <int EPI, bool GROUPED = false>
 cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const GemmArgs &args, cudaStream_t st) {
   using G = GemmCfg<256, true>;
   static PerContextOnce smem_limit;
   const cudaError_t attr_err = smem_limit.run([] {
-    return cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(gemm_tc_pair_kernel<EPI, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 G::SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const int tiles = ((args.M + 2 * BM - 1) / (2 * BM)) * ((args.N + 255) / 256);
-  int pairs = pair_slots<EPI>();
+  int pairs = pair_slots();
   if (pairs <= 0) return cudaErrorInvalidConfiguration;
-  pairs = tiles < pairs ? tiles : pairs;
+  if (!GROUPED) {
+    const int tiles = ((args.M + 2 * BM - 1) / (2 * BM)) * ((args.N + 255) / 256);
+    pairs = tiles < pairs ? tiles : pairs;
+  }
   count_launch();
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -206,7 +217,7 @@ cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const Gemm
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<EPI>, ma, mb, args);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<EPI, GROUPED>, ma, mb, args);
 }
 
 template <int EPI>
@@ -266,6 +277,15 @@ cudaError_t launch_gemm_grouped(const bf16 *A, const bf16 *W, void *C, int M, in
                 nullptr, 0.f, 0.f,
                 {}, 0, group_off, n_groups};
   CUtensorMap ma, mb;
+  // Many rows (at least a wave of 256 x 256 tiles, counted as if in one
+  // group) and 256 dividing N: 256-row tiles per group on CTA pairs.
+  if (LLAMA_GEMM_PAIRS && N % 256 == 0 && 2 * ((M + 2 * BM - 1) / (2 * BM)) * (N / 256) >= sm_count()) {
+    if (!make_map_2d(&ma, A, (uint64_t)M, (uint64_t)K, BM) ||
+        !make_map_2d(&mb, W, (uint64_t)N * n_groups, (uint64_t)K, 128))
+      return cudaErrorInvalidValue;
+    return epi == EPI_STORE ? launch_pair<EPI_STORE, true>(ma, mb, args, st)
+                            : launch_pair<EPI_SWIGLU, true>(ma, mb, args, st);
+  }
   if (!make_map_2d(&ma, A, (uint64_t)M, (uint64_t)K, BM) ||
       !make_map_2d(&mb, W, (uint64_t)N * n_groups, (uint64_t)K, bn))
     return cudaErrorInvalidValue;

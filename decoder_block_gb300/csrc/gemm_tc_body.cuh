@@ -496,17 +496,18 @@ __device__ __forceinline__ float splitk_finish(const GemmArgs &args, int tile, i
 // Tiles of the grouped mode: group g has ceil(rows_g / BM) x n_tiles tiles,
 // enumerated group by group, N-tile-major within a group (the m-tiles of one
 // weight tile run back to back).
+// tile_rows: BM, or 2 * BM for 256-row tiles on CTA pairs.
 struct GroupedTiles {
   const int *off;
-  int n_groups, n_tiles;
+  int n_groups, n_tiles, tile_rows;
   __device__ int count() const {
     int t = 0;
-    for (int g = 0; g < n_groups; ++g) t += (off[g + 1] - off[g] + BM - 1) / BM * n_tiles;
+    for (int g = 0; g < n_groups; ++g) t += (off[g + 1] - off[g] + tile_rows - 1) / tile_rows * n_tiles;
     return t;
   }
   __device__ void coords(int u, int &g, int &mt, int &nt) const {
     for (g = 0; g < n_groups; ++g) {
-      const int mtg = (off[g + 1] - off[g] + BM - 1) / BM;
+      const int mtg = (off[g + 1] - off[g] + tile_rows - 1) / tile_rows;
       if (u < mtg * n_tiles) {
         nt = u / mtg;
         mt = u % mtg;
@@ -523,7 +524,8 @@ struct GroupedTiles {
 // every CTA of the grid runs this with its 192 threads.
 //
 // PAIR: whole 256 x 256 tiles computed by the two CTAs of a cluster (launched
-// with cluster size 2, never as a phase of a fused kernel).  CTA r loads rows
+// with cluster size 2, never as a phase of a fused kernel; dense, or grouped
+// with 256-row tiles per group).  CTA r loads rows
 // r*128 .. r*128+127 of the tile's A rows and of its 256 weight rows into its
 // own shared memory; both CTAs' copies complete on the even (leader) CTA's
 // full barriers, whose MMA thread issues cta_group::2 MMAs that read both CTAs'
@@ -536,7 +538,7 @@ struct GroupedTiles {
 template <int EPI, int BN, bool GROUPED, bool PAIR = false>
 __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtensorMap *tmB, const GemmArgs &args,
                                             const PhaseSync sync) {
-  static_assert(!PAIR || (BN == 256 && !GROUPED), "CTA pairs compute dense 256 x 256 tiles");
+  static_assert(!PAIR || BN == 256, "CTA pairs compute 256 x 256 tiles");
   using G = GemmCfg<BN, PAIR>;
   constexpr int STAGES = G::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -573,7 +575,7 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
   const int m_tiles = PAIR ? (args.M + 2 * BM - 1) / (2 * BM) : (args.M + BM - 1) / BM;
   const int n_tiles = (args.N + BN - 1) / BN;
   const int k_steps = (args.K + BK - 1) / BK;
-  const GroupedTiles gt{args.group_off, args.n_groups, n_tiles};
+  const GroupedTiles gt{args.group_off, args.n_groups, n_tiles, PAIR ? 2 * BM : BM};
   if constexpr (GROUPED) grid_dependency_wait();  // every role reads the group offsets
   const int num_tiles = m_tiles * n_tiles;
   const int split_units = (GROUPED || PAIR) ? 0 : args.split_tiles * args.splits;
@@ -586,9 +588,9 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
     if constexpr (GROUPED) {
       int g, mt;
       gt.coords(u, g, mt, nt);
-      a_row = args.group_off[g] + mt * BM;
+      a_row = args.group_off[g] + (PAIR ? mt * 2 * BM + (int)rank * BM : mt * BM);
       m_end = min(args.group_off[g + 1], args.M);  // never past A, whatever the offsets say
-      w_row = g * args.N + nt * BN;
+      w_row = g * args.N + nt * BN + (PAIR ? (int)rank * (BN / 2) : 0);
       k0 = 0;
       k1 = k_steps;
       slot = -1;

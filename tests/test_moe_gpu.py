@@ -99,6 +99,18 @@ def test_moe_block_prefill(lb, name):
         assert np.bincount(ids.ravel(), minlength=shape["n_experts"]).max() > 128
 
 
+def test_moe_block_prefill_on_cta_pairs(lb):
+    """8192 routed rows (4096 tokens, top-2 of 8 experts): the experts' grouped GEMMs run 256-row tiles
+    per expert on CTA pairs (rows past an expert's range inside a tile are computed and not stored),
+    and so do the shared expert's GEMMs."""
+    shape = dict(BASE, d_model=1024, n_heads=8, n_kv_heads=2, rope_theta=5e5, d_ff=1024, n_experts=8, top_k=2,
+                 d_ff_shared=1024, max_seq_len=2048)
+    B, S = 2, 2048
+    ids = _check(shape, B, S, 0, S, 0, "moe_pairs", lb)
+    counts = np.bincount(ids.ravel(), minlength=shape["n_experts"])
+    assert counts.sum() == B * S * 2 and counts.max() > 512  # experts span several 256-row tiles
+
+
 @pytest.mark.parametrize("name", ["small_shared", "d128_heads_shared"])
 def test_moe_block_decode(lb, name):
     _check(MOE_SHAPES[name], 4, 1, 37, 48, 37, "moe_dec_" + name, lb)
