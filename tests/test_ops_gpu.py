@@ -31,6 +31,11 @@ GEMM_SHAPES = [
     (64, 6144, 4096),    # decode-sized M, Llama-3-8B QKV
     (1000, 1536, 512),
     (2000, 4000, 4104),  # CTA-pair tiles (residual and fp32 epilogues): ragged M, N and K
+    (1024, 4864, 1032),  # exactly one wave of pair tiles (76 pairs), K tail
+    (1000, 4864, 1032),  # the same with a ragged last pair tile (232 live rows)
+    (768, 5000, 512),    # just under one wave of pair tiles: single-CTA tiles
+    (4096, 1280, 2048),  # a plan with a split tail on single CTAs, whole tiles on pairs
+    (3000, 2000, 4104),  # ragged M, N, K on pairs, 12 x 8 pair tiles
 ]
 
 
