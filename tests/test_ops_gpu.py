@@ -163,6 +163,13 @@ ATTN_CASES = [
     (1, 50, 0, 12, 2, 64, "bf16"),    # n_rep 6: 16 positions per tile, 32 rows left zero
     (1, 90, 11, 14, 2, 128, "bf16"),  # n_rep 7: 16 positions, 112 live rows, cache prefix
     (2, 100, 3, 6, 2, 64, "bf16"),    # n_rep 3: 40 positions per tile (120 rows)
+    # D = 128 prefill edge cases: a single key tile, a one-key last tile, MHA, n_rep 8, a long cached prefix
+    (1, 64, 0, 8, 2, 128, "bf16"),    # one key tile, half of it past the end; one query block
+    (1, 129, 0, 32, 8, 128, "bf16"),  # Llama-3-8B grouping; the last key tile holds one key
+    (2, 257, 100, 16, 16, 128, "bf16"),  # MHA (128 positions per query tile), cache prefix
+    (1, 100, 0, 16, 2, 128, "bf16"),  # n_rep 8: 16 positions per tile
+    (1, 600, 1500, 32, 8, 128, "bf16"),  # a chunk after a long cached prefix (17 key tiles)
+    (3, 2, 5, 8, 2, 128, "bf16"),     # two-position prefill
     (5, 1, 300, 8, 2, 128, "bf16"),   # decode step, S = 1, two key chunks
     (3, 1, 77, 9, 3, 64, "bf16"),     # decode, one chunk, n_rep 3
     (2, 1, 1000, 32, 8, 128, "bf16"), # decode, ragged last chunk
