@@ -106,8 +106,9 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(DecArgs a) {
     const int keys = min(DEC_SUB, k1 - k0 - j * DEC_SUB);
     const uint32_t bytes = (uint32_t)keys * L::ROW;
     ptx::mbar_arrive_expect_tx(full(s), 2 * bytes);
-    ptx::bulk_load(s0 + s * L::STAGE, kg + (size_t)j * DEC_SUB * D, bytes, full(s));
-    ptx::bulk_load(s0 + s * L::STAGE + DEC_SUB * L::ROW, vg + (size_t)j * DEC_SUB * D, bytes, full(s));
+    const uint64_t once = ptx::policy_evict_first();  // each cached key is read once per step
+    ptx::bulk_load_hint(s0 + s * L::STAGE, kg + (size_t)j * DEC_SUB * D, bytes, full(s), once);
+    ptx::bulk_load_hint(s0 + s * L::STAGE + DEC_SUB * L::ROW, vg + (size_t)j * DEC_SUB * D, bytes, full(s), once);
   };
   volatile int abort_local = 0;
   int issued = 0;  // thread 0: sub-tiles whose copies have been issued

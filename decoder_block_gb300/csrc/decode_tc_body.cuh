@@ -207,9 +207,12 @@ __device__ __forceinline__ void attn_decode_tc_run(const CUtensorMap *tmQ, const
           }
           ptx::mbar_arrive_expect_tx(kv_full(st), 2 * L::KV_BYTES);
           const int key = k0 + j * DT_TILE;
+          const uint64_t once = ptx::policy_evict_first();  // each cached key is read once per step
           for (int at = 0; at < 2; ++at) {
-            ptx::tma_load_4d(s0 + L::OFF_K + st * L::KV_BYTES + at * L::ATOM, tmK, at * 64, key, g, b, kv_full(st));
-            ptx::tma_load_4d(s0 + L::OFF_V + st * L::KV_BYTES + at * L::ATOM, tmV, at * 64, key, g, b, kv_full(st));
+            ptx::tma_load_4d_hint(s0 + L::OFF_K + st * L::KV_BYTES + at * L::ATOM, tmK, at * 64, key, g, b,
+                                  kv_full(st), once);
+            ptx::tma_load_4d_hint(s0 + L::OFF_V + st * L::KV_BYTES + at * L::ATOM, tmV, at * 64, key, g, b,
+                                  kv_full(st), once);
           }
         }
         if (!ok) {

@@ -660,9 +660,14 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
           ptx::mbar_arrive_expect_tx(full_bar(s), G::STAGE_BYTES);
         }
       };
+      // with a single row of tiles (decode shapes) every weight tile is read
+      // once: it goes into L2 as first to evict
+      const bool w_once = !PAIR && args.M <= BM;
       auto load = [&](uint32_t dst, const CUtensorMap *map, int x, int y, int s) {
         if constexpr (PAIR)
           ptx::tma_load_2d_pair(dst, map, x, y, leader(full_bar(s)));
+        else if (w_once && map == tmB)
+          ptx::tma_load_2d_hint(dst, map, x, y, full_bar(s), ptx::policy_evict_first());
         else
           ptx::tma_load_2d(dst, map, x, y, full_bar(s));
       };
@@ -1011,23 +1016,32 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
       float sq = 0.f;
       const float rs = row_scale<EPI>(args, m);
       for (int ch = (int)rank; ch < BN / 32 && m < args.M; ch += args.splits) {
-        float4 cs[8];  // issued ahead of the piece loads
+        // the chunk's rotation pairs and residual are requested ahead of the piece loads
+        float4 cs[8];
         load_rope32<EPI>(args, m, nt * BN + ch * 32, cs);
+        uint4 rc[4];
+        bool vc = false;
+        if constexpr (EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_SQSUM) load_residual32(args, m, nt * BN + ch * 32, rc, vc);
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0.f;
         for (int pc = 0; pc < args.splits; ++pc) {
           const uint32_t base = ptx::mapa_shared(smem0, (uint32_t)pc);
+          // a piece's eight loads are in flight together (one distributed
+          // shared-memory round trip per piece, not per load), then added in
+          // piece order
+          float4 p4[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) p4[i] = ptx::ld_cluster_v4(base + (uint32_t)((((ch * 32) >> 2) + i) * BM + r) * 16);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float4 p4 = ptx::ld_cluster_v4(base + (uint32_t)((((ch * 32) >> 2) + i) * BM + r) * 16);
-            v[4 * i] += p4.x;
-            v[4 * i + 1] += p4.y;
-            v[4 * i + 2] += p4.z;
-            v[4 * i + 3] += p4.w;
+            v[4 * i] += p4[i].x;
+            v[4 * i + 1] += p4[i].y;
+            v[4 * i + 2] += p4[i].z;
+            v[4 * i + 3] += p4[i].w;
           }
         }
-        sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + ch * 32, rs, nullptr, cs);
+        sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + ch * 32, rs, vc ? rc : nullptr, cs);
       }
       if constexpr (EPI == EPI_RESIDUAL_SQSUM) {
         if (m < args.M) {
