@@ -1025,21 +1025,30 @@ __device__ __forceinline__ void gemm_tc_run(const CUtensorMap *tmA, const CUtens
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0.f;
-        for (int pc = 0; pc < args.splits; ++pc) {
-          const uint32_t base = ptx::mapa_shared(smem0, (uint32_t)pc);
-          // a piece's eight loads are in flight together (one distributed
-          // shared-memory round trip per piece, not per load), then added in
-          // piece order
-          float4 p4[8];
+        // the pieces' loads are in flight together (one distributed shared-memory
+        // round trip per group of four pieces, not per load), then added in piece order
+        for (int p0 = 0; p0 < args.splits; p0 += 4) {
+          const int np = min(4, args.splits - p0);
+          float4 p4[4][8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) p4[i] = ptx::ld_cluster_v4(base + (uint32_t)((((ch * 32) >> 2) + i) * BM + r) * 16);
+          for (int q = 0; q < 4; ++q)
+            if (q < np) {
+              const uint32_t base = ptx::mapa_shared(smem0, (uint32_t)(p0 + q));
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            v[4 * i] += p4[i].x;
-            v[4 * i + 1] += p4[i].y;
-            v[4 * i + 2] += p4[i].z;
-            v[4 * i + 3] += p4[i].w;
-          }
+              for (int i = 0; i < 8; ++i)
+                p4[q][i] = ptx::ld_cluster_v4(base + (uint32_t)((((ch * 32) >> 2) + i) * BM + r) * 16);
+            }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (q < np) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                v[4 * i] += p4[q][i].x;
+                v[4 * i + 1] += p4[q][i].y;
+                v[4 * i + 2] += p4[q][i].z;
+                v[4 * i + 3] += p4[q][i].w;
+              }
+            }
         }
         sq += epilogue_chunk32<EPI>(v, args, m, nt * BN + ch * 32, rs, vc ? rc : nullptr, cs);
       }
